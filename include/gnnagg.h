@@ -1,0 +1,262 @@
+/*
+ * gnnagg.h -- C ABI of the boundary-quantised GCN aggregation library
+ * (libgnnagg.so, CUDA kernels for sm_103a).
+ *
+ * What it computes is the per-layer data path of distributed full-graph GCN
+ * training described in the SYLVIE guide ("SYLVIE: 3D-adaptive and Universal
+ * System for Large-scale Graph Neural Network Training"): the normalised
+ * aggregation of section 2, the boundary messages of section 3, the
+ * stochastic integer quantisation of section 6 and the node-importance widths
+ * of sections 7 and 9.  Partitions are contiguous node blocks of one graph on
+ * one GPU; a message "exchange" is a buffer that stays in device memory.
+ *
+ * Conventions shared by every call:
+ *   - Every function returns a gnn_status; GNN_OK is 0.  Nothing throws.
+ *     gnn_last_error() gives a message for the calling thread's last failure.
+ *   - Arrays are device pointers owned by the caller.  The library neither
+ *     allocates nor frees them; setup calls take an explicit workspace whose
+ *     size the matching *_workspace call reports.
+ *   - Calls are asynchronous and ordered on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream) unless the comment says the call
+ *     synchronises.  Argument errors are detected on the host and returned
+ *     before anything is launched.
+ *   - Feature matrices are row-major fp32 with a row stride `ld` (elements)
+ *     that is a multiple of 4 and at least F; rows must be 16-byte aligned.
+ *     Output columns F..round_up(F,4)-1 are written as zero; columns beyond
+ *     that are not touched.
+ *   - Bit widths are 1, 2, 4 or 8 (quantised) or 32 (fp32 passed through,
+ *     for testing).  F is 1..1024.
+ */
+#ifndef GNNAGG_H
+#define GNNAGG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gnn_status {
+  GNN_OK = 0,
+  GNN_ERR_INVALID_ARG = 1, /* a NULL pointer, size, stride or alignment out of range */
+  GNN_ERR_UNSUPPORTED = 2, /* a valid request this build does not serve (e.g. F > 1024) */
+  GNN_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed */
+  GNN_ERR_DEVICE_CHECK = 4,/* a device-side check flagged bad data */
+  GNN_ERR_TIMEOUT = 5,     /* a bounded device wait gave up */
+  GNN_ERR_CAPACITY = 6     /* an output buffer is smaller than the result */
+} gnn_status;
+
+typedef void* gnn_stream_t; /* cudaStream_t */
+
+/* Thread-local text of the last failure in this thread ("" if none). */
+const char* gnn_last_error(void);
+/* Library version, major*10000 + minor*100 + patch. */
+int gnn_version(void);
+
+/* ------------------------------------------------------------------------ */
+/* CSR adjacency with GCN normalisation.                                    */
+/* ------------------------------------------------------------------------ */
+#define GNN_CSR_SYMMETRIZE 1u /* add v->u for every u->v                     */
+#define GNN_CSR_DEDUP 2u      /* keep one copy of repeated edges             */
+#define GNN_CSR_SELF_LOOPS 4u /* drop given self-loops, add one per node     */
+
+/* Row v lists the sources u it aggregates (ascending); val[e] is the GCN
+ * weight 1/sqrt(d_v d_u), computed in fp64 and rounded to fp32, d = row
+ * length including the self-loop.  `symmetric` is 1 when the rows were
+ * symmetrised (the backward call requires it). */
+typedef struct gnn_csr {
+  int32_t n;         /* nodes                                     */
+  int32_t symmetric; /* 1 if A = A^T by construction              */
+  int64_t nnz;       /* entries, self-loops included              */
+  int64_t* rowptr;   /* [n+1]                                     */
+  int32_t* col;      /* [nnz]                                     */
+  float* val;        /* [nnz]                                     */
+  /* Optional load-balancing plan filled by gnn_csr_split (all zero/NULL:
+   * none).  Rows with more than split_len entries ("long rows", the hubs of
+   * a power-law graph) are cut into pieces of split_len entries that run in
+   * parallel; the aggregation calls then keep one partial row per piece in
+   * their workspace and add the pieces of a row in piece order.             */
+  int32_t split_len;  /* 0 = no plan                                         */
+  int32_t n_long;     /* long rows                                           */
+  int64_t n_pieces;   /* pieces of all long rows                             */
+  int32_t* long_rows; /* [n_long] ascending                                  */
+  int64_t* piece_ptr; /* [n_long+1] first piece of long row i                */
+  int32_t* piece_row; /* [n_pieces] row of piece p                           */
+  int64_t* piece_beg; /* [n_pieces] first entry of piece p                   */
+} gnn_csr;
+
+/* Workspace bytes for gnn_csr_build with these sizes. */
+gnn_status gnn_csr_build_workspace(int32_t n, int64_t n_edges, uint32_t flags,
+                                   size_t* ws_bytes);
+
+/* Edge list (src[i] -> dst[i], device int32) to CSR, following the GCN layer
+ * of the SYLVIE guide, section 2 (aggregation over N(v) plus v itself with
+ * weight 1/sqrt(d_v d_u)).  out->rowptr [n+1], out->col and out->val
+ * [capacity] are caller buffers; out->n, out->nnz and out->symmetric are set.
+ * Synchronises `stream` (the entry count is data-dependent).  Returns
+ * GNN_ERR_CAPACITY, with out->nnz set to the needed count, when capacity is
+ * too small.  Endpoints must lie in [0, n). */
+gnn_status gnn_csr_build(int32_t n, int64_t n_edges, const int32_t* src,
+                         const int32_t* dst, uint32_t flags, int64_t capacity,
+                         gnn_csr* out, void* ws, size_t ws_bytes,
+                         gnn_stream_t stream);
+
+/* Row-split plan for load balance.  gnn_csr_split_count (synchronises)
+ * reports the long rows and pieces for split_len >= 32; the caller allocates
+ * long_rows [n_long], piece_ptr [n_long+1], piece_row and piece_beg
+ * [n_pieces], sets those pointers, split_len, n_long and n_pieces in `csr`,
+ * and gnn_csr_split fills them.  Workspace: gnn_csr_split_workspace. */
+gnn_status gnn_csr_split_workspace(const gnn_csr* csr, size_t* ws_bytes);
+gnn_status gnn_csr_split_count(const gnn_csr* csr, int32_t split_len, int32_t* n_long,
+                               int64_t* n_pieces, void* ws, size_t ws_bytes,
+                               gnn_stream_t stream);
+gnn_status gnn_csr_split(gnn_csr* csr, void* ws, size_t ws_bytes, gnn_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Partitions, boundary slots and per-node bit widths.                       */
+/* ------------------------------------------------------------------------ */
+/* Width rule.  A boundary node u (one that some other partition aggregates)
+ * gets c_u = #{w in pool : d_w <= d_u}, n = pool size (importance c_u/n: the
+ * max-degree node has 1, equal degrees share a value, SYLVIE guide section
+ * 7), level = #{i < n_levels-1 : 100*c_u > pct[i]*n}, mask = bits[level],
+ * and width min(8, mask * base_bits) (section 9); mask 32 passes through.
+ * Nodes outside the pool get 0 (they are never sent).  A top-Q% rule is
+ * n_levels=2, pct[0]=100-Q. */
+typedef struct gnn_bit_rule {
+  int32_t n_levels; /* 1..4                                 */
+  int32_t pct[3];   /* ascending thresholds in percent      */
+  uint8_t bits[4];  /* 1, 2, 4, 8 or 32 per level           */
+} gnn_bit_rule;
+
+/* Partition p holds nodes [part_start[p], part_start[p+1]) with
+ * part_start[p] = floor(p*n/P).  A slot s is a pair (q, u): node u is
+ * aggregated by some node of partition q != part(u), as the boundary nodes of
+ * the SYLVIE guide, section 3.  Slots are ordered by q, then u. */
+typedef struct gnn_boundary {
+  int32_t P;
+  int32_t n;
+  int64_t n_slots;      /* S                                                   */
+  int64_t nnz_cut;      /* CSR entries whose source lies in another partition  */
+  int32_t F;            /* feature width slot_off was computed for             */
+  int32_t reserved;
+  int64_t* part_start;  /* [P+1]                                               */
+  int64_t* send_start;  /* [P+1] first slot received by partition q            */
+  int32_t* slot_node;   /* [S] u of slot s                                     */
+  int32_t* col_remap;   /* [nnz] col[e] if local, else ~s of (part(row), col)  */
+  int64_t* slot_rowptr; /* [S+1] backward entries of slot s ...                */
+  int32_t* slot_col;    /* [nnz_cut] ... the rows v of q that aggregate u,     */
+  float* slot_val;      /* [nnz_cut] ... ascending, with their weights A_vu    */
+  int64_t* own_ptr;     /* [n+1] slots whose node is u ...                     */
+  int32_t* own_slot;    /* [S]   ... ascending s                               */
+  uint8_t* node_bits;   /* [n]                                                 */
+  uint8_t* slot_bits;   /* [S] = node_bits[slot_node[s]]                       */
+  int64_t* slot_off;    /* [S+1] byte offset of slot s in a message buffer     */
+} gnn_boundary;
+
+/* Workspace bytes for gnn_boundary_count / _index / _set_bits on this CSR. */
+gnn_status gnn_boundary_workspace(const gnn_csr* csr, int32_t P, size_t* ws_bytes);
+
+/* Number of slots and of cut entries for P partitions.  Synchronises. */
+gnn_status gnn_boundary_count(const gnn_csr* csr, int32_t P, int64_t* n_slots,
+                              int64_t* nnz_cut, void* ws, size_t ws_bytes,
+                              gnn_stream_t stream);
+
+/* Fill every array of `out` (allocated by the caller with the sizes from
+ * gnn_boundary_count; out->P, out->n_slots and out->nnz_cut set) and the
+ * widths and byte offsets for feature width F.  Follows the SYLVIE guide:
+ * section 3 (boundary nodes per receiving partition), section 5 step 1 and
+ * section 7 (global in-degree importance, node mask), section 9 (combination
+ * with the base width).  Synchronises. */
+gnn_status gnn_boundary_index(const gnn_csr* csr, const gnn_bit_rule* rule,
+                              uint8_t base_bits, int32_t F, gnn_boundary* out,
+                              void* ws, size_t ws_bytes, gnn_stream_t stream);
+
+/* Recompute node_bits, slot_bits and slot_off (for F) after the base width
+ * changes (section 8: the base width moves between epochs). */
+gnn_status gnn_boundary_set_bits(const gnn_csr* csr, const gnn_bit_rule* rule,
+                                 uint8_t base_bits, int32_t F, gnn_boundary* bnd,
+                                 void* ws, size_t ws_bytes, gnn_stream_t stream);
+
+/* slot_off[s] = sum_{t<s} rowbytes(slot_bits[t], F), slot_off[S] = total,
+ * rowbytes(b,F) = 16*ceil(F*b/128) (b=32: 16*ceil(4F/16)).  Every row starts
+ * on a 16-byte boundary.  `ws` needs gnn_slot_offsets_workspace bytes. */
+gnn_status gnn_slot_offsets_workspace(int64_t n_slots, size_t* ws_bytes);
+gnn_status gnn_slot_offsets(const uint8_t* slot_bits, int64_t n_slots, int32_t F,
+                            int64_t* slot_off, void* ws, size_t ws_bytes,
+                            gnn_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Hot path.                                                                 */
+/* ------------------------------------------------------------------------ */
+/* Stochastic integer quantisation and packing of message rows, SYLVIE guide
+ * section 6: for row r, x = X[row_idx[r]][0..F) (row_idx NULL: row r), width
+ * b = row_bits[r]; mn = min x, mx = max x (a zero stored as +0);
+ * scale = (mx-mn)/(2^b-1) (0 if mx == mn, all codes 0);
+ * code_j = min(2^b-1, floor((x_j-mn)/scale + u_j)),
+ * u_j = (hash32(seed, r, j) >> 8) * 2^-24,
+ * hash32(seed,r,j) = fmix32(fmix32(seed ^ fmix32(r)) ^ j) (MurmurHash3's
+ * 32-bit finaliser), every step IEEE fp32 round-to-nearest without
+ * contraction.  Code j goes to bits [b*(j mod 32/b), +b) of little-endian
+ * 32-bit word floor(j*b/32) of the row at packed + row_off[r]; the row is
+ * zero-padded to rowbytes(b, F).  meta[2r] = mn, meta[2r+1] = scale.  Width
+ * 32 stores the fp32 values and meta (0, 0).  row_off[r] must be a multiple
+ * of 16.  The row key r is the slot index, so forward and backward messages
+ * of a slot draw from the same stream for equal seeds. */
+gnn_status gnn_quant_pack(const float* X, int64_t ldx, int32_t F,
+                          const int32_t* row_idx, int64_t n_rows,
+                          const uint8_t* row_bits, const int64_t* row_off,
+                          uint32_t seed, uint8_t* packed, float* meta,
+                          gnn_stream_t stream);
+
+/* Receive side of section 6: out[r][j] = scale*code_j + mn (fp32 multiply,
+ * then fp32 add; width 32 copies the stored value). */
+gnn_status gnn_dequant_unpack(const uint8_t* packed, const float* meta,
+                              const int64_t* row_off, const uint8_t* row_bits,
+                              int64_t n_rows, int32_t F, float* out, int64_t ldo,
+                              gnn_stream_t stream);
+
+/* Forward aggregation, SYLVIE guide sections 2, 3 and 11 (receive, dequantise,
+ * aggregate): M[v] = sum_e val[e] * x_e with x_e = H[u] for a source u in
+ * v's partition and, for a remote u, the dequantised message of slot
+ * (part(v), u) read from packed/meta (as gnn_quant_pack wrote them with
+ * bnd->slot_bits and bnd->slot_off).  bnd NULL: plain M = A H.  fp32
+ * accumulation in any order.  Mb (optional, may be NULL) receives M rounded
+ * to bf16 (nearest-even) with row stride ldmb >= round_up(F, 16); its columns
+ * F..round_up(F,16)-1 are written as zero so it can feed the dense
+ * transform.  ws/ws_bytes: gnn_spmm_workspace bytes (NULL/0 without a split
+ * plan); calls that share a workspace must not overlap on the GPU. */
+gnn_status gnn_spmm_fwd(const gnn_csr* csr, const gnn_boundary* bnd,
+                        const float* H, int64_t ldh, int32_t F,
+                        const uint8_t* packed, const float* meta, float* M,
+                        int64_t ldm, uint16_t* Mb, int64_t ldmb, void* ws,
+                        size_t ws_bytes, gnn_stream_t stream);
+
+/* Workspace bytes the aggregation calls need for `csr`'s split plan at
+ * feature width F: n_pieces * round_up(F, 4) * 4 (0 without a plan). */
+gnn_status gnn_spmm_workspace(const gnn_csr* csr, int32_t F, size_t* ws_bytes);
+
+/* Backward aggregation dH = A^T G for symmetric A (section 3: embedding
+ * gradients travel back along the same cross-partition dependencies).  With
+ * bnd: each slot s = (q, u) first forms the halo partial
+ * P_s = sum over its entries (ascending v) of slot_val * G[v], in fp32 with
+ * every product and sum rounded (start +0), and quantises/packs it like
+ * gnn_quant_pack (row key s, width slot_bits[s], offsets slot_off) into
+ * packed_ws / meta_ws (sizes slot_off[S] bytes and 2S floats); then
+ * dH[u] = sum over u's local entries of val * G[v] + sum over the slots u
+ * owns of their dequantised partials.  bnd NULL: plain A^T G. */
+gnn_status gnn_spmm_bwd(const gnn_csr* csr, const gnn_boundary* bnd,
+                        const float* G, int64_t ldg, int32_t F, uint32_t seed,
+                        uint8_t* packed_ws, float* meta_ws, float* dH,
+                        int64_t ldh, void* ws, size_t ws_bytes,
+                        gnn_stream_t stream);
+
+/* Synchronise `stream` and report device-side failures (GNN_ERR_CUDA for a
+ * CUDA error, GNN_ERR_DEVICE_CHECK / GNN_ERR_TIMEOUT for flags the kernels
+ * raised).  Clears the flags. */
+gnn_status gnn_sync_check(gnn_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GNNAGG_H */

@@ -1,0 +1,286 @@
+"""Python binding of libgnnagg.so (boundary-quantised GCN aggregation on
+GB300).  Functions carry the C entry points' names and only marshal torch
+tensors (device memory) and the current CUDA stream into the C ABI; every
+step of the computation runs in the library's CUDA kernels.  There is no CPU
+path: without the library or a CUDA device the calls raise."""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass, field
+from typing import Optional, Sequence
+
+from . import _abi
+from ._abi import (CSR_DEDUP, CSR_GCN, CSR_SELF_LOOPS, CSR_SYMMETRIZE, GnnBitRule,  # noqa: F401
+                   GnnBoundary, GnnCsr, GnnError, call, load)
+
+__all__ = [
+    "Csr", "Boundary", "BitRule", "GnnError", "load", "build",
+    "gnn_csr_build", "gnn_csr_split", "gnn_spmm_workspace", "spmm_ws", "gnn_boundary_index", "gnn_boundary_set_bits", "gnn_slot_offsets",
+    "gnn_quant_pack", "gnn_dequant_unpack", "gnn_spmm_fwd", "gnn_spmm_bwd", "gnn_sync_check",
+    "rowbytes", "ld_for", "ldb_for",
+]
+
+
+def build(force: bool = False) -> str:
+    from . import builder as _b
+    return _b.build(force=force)
+
+
+def _torch():
+    import torch
+    if not torch.cuda.is_available():
+        raise RuntimeError("sparse_aggregation_message_gb300 needs a CUDA device")
+    return torch
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream=None) -> int:
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def ld_for(F: int) -> int:
+    """fp32 row stride: F rounded up to a multiple of 4."""
+    return (F + 3) // 4 * 4
+
+
+def ldb_for(F: int) -> int:
+    """bf16 row stride for dense-transform inputs: F rounded up to 16."""
+    return (F + 15) // 16 * 16
+
+
+def rowbytes(b: int, F: int) -> int:
+    return 16 * ((4 * F + 15) // 16) if b == 32 else 16 * ((F * b + 127) // 128)
+
+
+@dataclass
+class BitRule:
+    """Boundary-pool width rule: level = #{i : 100*c > pct[i]*n}, mask =
+    bits[level], width = min(8, mask * base)."""
+    pct: Sequence[int]
+    bits: Sequence[int]
+
+    def to_c(self) -> GnnBitRule:
+        r = GnnBitRule()
+        r.n_levels = len(self.bits)
+        assert len(self.pct) == len(self.bits) - 1
+        for i, p in enumerate(self.pct):
+            r.pct[i] = int(p)
+        for i, b in enumerate(self.bits):
+            r.bits[i] = int(b)
+        return r
+
+
+@dataclass
+class Csr:
+    n: int
+    nnz: int
+    symmetric: bool
+    rowptr: object
+    col: object
+    val: object
+    split_len: int = 0
+    n_long: int = 0
+    n_pieces: int = 0
+    split: dict = field(default_factory=dict)
+
+    def c(self) -> GnnCsr:
+        s = self.split
+        return GnnCsr(self.n, int(self.symmetric), self.nnz, _ptr(self.rowptr), _ptr(self.col),
+                      _ptr(self.val), self.split_len, self.n_long, self.n_pieces,
+                      _ptr(s.get("long_rows")), _ptr(s.get("piece_ptr")), _ptr(s.get("piece_row")),
+                      _ptr(s.get("piece_beg")))
+
+
+@dataclass
+class Boundary:
+    P: int
+    n: int
+    n_slots: int
+    nnz_cut: int
+    F: int
+    arrays: dict = field(default_factory=dict)
+
+    def __getattr__(self, k):
+        arrays = self.__dict__.get("arrays", {})
+        if k in arrays:
+            return arrays[k]
+        raise AttributeError(k)
+
+    def c(self, slot_off=None, F=None) -> GnnBoundary:
+        a = self.arrays
+        b = GnnBoundary()
+        b.P, b.n, b.n_slots, b.nnz_cut = self.P, self.n, self.n_slots, self.nnz_cut
+        b.F = self.F if F is None else F
+        for k in ("part_start", "send_start", "slot_node", "col_remap", "slot_rowptr", "slot_col",
+                  "slot_val", "own_ptr", "own_slot", "node_bits", "slot_bits"):
+            setattr(b, k, _ptr(a[k]))
+        b.slot_off = _ptr(a["slot_off"] if slot_off is None else slot_off)
+        return b
+
+
+def _workspace(nbytes: int, device):
+    torch = _torch()
+    return torch.empty(max(int(nbytes), 1), dtype=torch.uint8, device=device)
+
+
+def gnn_csr_build(n: int, src, dst, flags: int = CSR_GCN, stream=None) -> Csr:
+    """Edge list (int32 device tensors) -> Csr with GCN weights."""
+    torch = _torch()
+    dev = src.device
+    m = int(src.numel())
+    ws_bytes = ctypes.c_size_t()
+    call("gnn_csr_build_workspace", n, m, flags, ctypes.byref(ws_bytes))
+    ws = _workspace(ws_bytes.value, dev)
+    cap = (2 * m if flags & CSR_SYMMETRIZE else m) + (n if flags & CSR_SELF_LOOPS else 0)
+    rowptr = torch.empty(n + 1, dtype=torch.int64, device=dev)
+    col = torch.empty(max(cap, 1), dtype=torch.int32, device=dev)
+    val = torch.empty(max(cap, 1), dtype=torch.float32, device=dev)
+    out = GnnCsr(n, 0, 0, rowptr.data_ptr(), col.data_ptr(), val.data_ptr())
+    call("gnn_csr_build", n, m, _ptr(src), _ptr(dst), flags, cap, ctypes.byref(out), _ptr(ws),
+         ws.numel(), _stream(stream))
+    nnz = int(out.nnz)
+    return Csr(n=n, nnz=nnz, symmetric=bool(out.symmetric), rowptr=rowptr, col=col[:nnz],
+               val=val[:nnz])
+
+
+def gnn_csr_split(csr: Csr, split_len: int = 512, stream=None) -> Csr:
+    """Attach a row-split plan: rows longer than split_len are cut into pieces
+    of split_len entries (load balance for high-degree rows)."""
+    torch = _torch()
+    dev = csr.rowptr.device
+    c = csr.c()
+    ws_bytes = ctypes.c_size_t()
+    call("gnn_csr_split_workspace", ctypes.byref(c), ctypes.byref(ws_bytes))
+    ws = _workspace(ws_bytes.value, dev)
+    nl, npc = ctypes.c_int32(), ctypes.c_int64()
+    st = _stream(stream)
+    call("gnn_csr_split_count", ctypes.byref(c), split_len, ctypes.byref(nl), ctypes.byref(npc),
+         _ptr(ws), ws.numel(), st)
+    nl, npc = nl.value, npc.value
+    split = dict(long_rows=torch.empty(max(nl, 1), dtype=torch.int32, device=dev),
+                 piece_ptr=torch.empty(nl + 1, dtype=torch.int64, device=dev),
+                 piece_row=torch.empty(max(npc, 1), dtype=torch.int32, device=dev),
+                 piece_beg=torch.empty(max(npc, 1), dtype=torch.int64, device=dev))
+    out = Csr(csr.n, csr.nnz, csr.symmetric, csr.rowptr, csr.col, csr.val, split_len, nl, npc, split)
+    c2 = out.c()
+    call("gnn_csr_split", ctypes.byref(c2), _ptr(ws), ws.numel(), st)
+    return out
+
+
+def gnn_spmm_workspace(csr: Csr, F: int) -> int:
+    nb = ctypes.c_size_t()
+    c = csr.c()
+    call("gnn_spmm_workspace", ctypes.byref(c), F, ctypes.byref(nb))
+    return nb.value
+
+
+def spmm_ws(csr: Csr, F: int, device="cuda"):
+    """A workspace tensor sized for the aggregation calls (or None)."""
+    nb = gnn_spmm_workspace(csr, F)
+    return _workspace(nb, device) if nb else None
+
+
+def gnn_boundary_index(csr: Csr, P: int, rule: BitRule, base_bits: int, F: int,
+                       stream=None) -> Boundary:
+    torch = _torch()
+    dev = csr.rowptr.device
+    c = csr.c()
+    ws_bytes = ctypes.c_size_t()
+    call("gnn_boundary_workspace", ctypes.byref(c), P, ctypes.byref(ws_bytes))
+    ws = _workspace(ws_bytes.value, dev)
+    S, nc = ctypes.c_int64(), ctypes.c_int64()
+    st = _stream(stream)
+    call("gnn_boundary_count", ctypes.byref(c), P, ctypes.byref(S), ctypes.byref(nc), _ptr(ws),
+         ws.numel(), st)
+    S, nc, n = S.value, nc.value, csr.n
+    i32, i64, u8, f32 = torch.int32, torch.int64, torch.uint8, torch.float32
+
+    def e(k, dt):
+        return torch.empty(max(k, 1), dtype=dt, device=dev)
+
+    a = dict(part_start=e(P + 1, i64), send_start=e(P + 1, i64), slot_node=e(S, i32),
+             col_remap=e(csr.nnz, i32), slot_rowptr=e(S + 1, i64), slot_col=e(nc, i32),
+             slot_val=e(nc, f32), own_ptr=e(n + 1, i64), own_slot=e(S, i32), node_bits=e(n, u8),
+             slot_bits=e(S, u8), slot_off=e(S + 1, i64))
+    b = Boundary(P=P, n=n, n_slots=S, nnz_cut=nc, F=F, arrays=a)
+    cb = b.c()
+    call("gnn_boundary_index", ctypes.byref(c), ctypes.byref(rule.to_c()), base_bits, F,
+         ctypes.byref(cb), _ptr(ws), ws.numel(), st)
+    sizes = dict(part_start=P + 1, send_start=P + 1, slot_node=S, col_remap=csr.nnz,
+                 slot_rowptr=S + 1, slot_col=nc, slot_val=nc, own_ptr=n + 1, own_slot=S,
+                 node_bits=n, slot_bits=S, slot_off=S + 1)
+    b.arrays = {k: v[:sizes[k]] for k, v in a.items()}
+    return b
+
+
+def gnn_boundary_set_bits(csr: Csr, bnd: Boundary, rule: BitRule, base_bits: int, F: int,
+                          stream=None) -> None:
+    dev = csr.rowptr.device
+    c = csr.c()
+    ws_bytes = ctypes.c_size_t()
+    call("gnn_boundary_workspace", ctypes.byref(c), bnd.P, ctypes.byref(ws_bytes))
+    ws = _workspace(ws_bytes.value, dev)
+    cb = bnd.c()
+    call("gnn_boundary_set_bits", ctypes.byref(c), ctypes.byref(rule.to_c()), base_bits, F,
+         ctypes.byref(cb), _ptr(ws), ws.numel(), _stream(stream))
+    bnd.F = F
+
+
+def gnn_slot_offsets(slot_bits, n_slots: int, F: int, stream=None):
+    """Byte offsets [S+1] of each slot's packed row for feature width F."""
+    torch = _torch()
+    dev = slot_bits.device
+    ws_bytes = ctypes.c_size_t()
+    call("gnn_slot_offsets_workspace", n_slots, ctypes.byref(ws_bytes))
+    ws = _workspace(ws_bytes.value, dev)
+    off = torch.empty(n_slots + 1, dtype=torch.int64, device=dev)
+    call("gnn_slot_offsets", _ptr(slot_bits), n_slots, F, _ptr(off), _ptr(ws), ws.numel(),
+         _stream(stream))
+    return off
+
+
+def gnn_quant_pack(X, F: int, row_idx, n_rows: int, row_bits, row_off, seed: int, packed, meta,
+                   stream=None) -> None:
+    call("gnn_quant_pack", _ptr(X), X.stride(0), F, _ptr(row_idx), n_rows, _ptr(row_bits),
+         _ptr(row_off), seed & 0xFFFFFFFF, _ptr(packed), _ptr(meta), _stream(stream))
+
+
+def gnn_dequant_unpack(packed, meta, row_off, row_bits, n_rows: int, F: int, out,
+                       stream=None) -> None:
+    call("gnn_dequant_unpack", _ptr(packed), _ptr(meta), _ptr(row_off), _ptr(row_bits), n_rows, F,
+         _ptr(out), out.stride(0), _stream(stream))
+
+
+def _ws_args(csr: Csr, F: int, ws, device):
+    if ws is None and csr.split_len:
+        ws = spmm_ws(csr, F, device)
+    return _ptr(ws), (ws.numel() * ws.element_size() if ws is not None else 0)
+
+
+def gnn_spmm_fwd(csr: Csr, bnd: Optional[Boundary], H, F: int, packed=None, meta=None, M=None,
+                 Mb=None, slot_off=None, ws=None, stream=None) -> None:
+    c = csr.c()
+    cb = bnd.c(slot_off, F if slot_off is not None else None) if bnd is not None else None
+    wp, wn = _ws_args(csr, F, ws, H.device)
+    call("gnn_spmm_fwd", ctypes.byref(c), ctypes.byref(cb) if cb is not None else None, _ptr(H),
+         H.stride(0), F, _ptr(packed), _ptr(meta), _ptr(M), M.stride(0) if M is not None else 0,
+         _ptr(Mb), Mb.stride(0) if Mb is not None else 0, wp, wn, _stream(stream))
+
+
+def gnn_spmm_bwd(csr: Csr, bnd: Optional[Boundary], G, F: int, seed: int, packed_ws, meta_ws, dH,
+                 slot_off=None, ws=None, stream=None) -> None:
+    c = csr.c()
+    cb = bnd.c(slot_off, F if slot_off is not None else None) if bnd is not None else None
+    wp, wn = _ws_args(csr, F, ws, G.device)
+    call("gnn_spmm_bwd", ctypes.byref(c), ctypes.byref(cb) if cb is not None else None, _ptr(G),
+         G.stride(0), F, seed & 0xFFFFFFFF, _ptr(packed_ws), _ptr(meta_ws), _ptr(dH), dH.stride(0),
+         wp, wn, _stream(stream))
+
+
+def gnn_sync_check(stream=None) -> None:
+    call("gnn_sync_check", _stream(stream))

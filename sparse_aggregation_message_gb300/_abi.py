@@ -1,0 +1,106 @@
+"""ctypes view of libgnnagg.so: struct layouts and function prototypes that
+mirror include/gnnagg.h one to one."""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import builder as _build
+
+c_i32, c_i64, c_u8, c_u16, c_u32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint8, ctypes.c_uint16, ctypes.c_uint32
+c_size, c_vp, c_char_p = ctypes.c_size_t, ctypes.c_void_p, ctypes.c_char_p
+P_i64 = ctypes.POINTER(c_i64)
+P_size = ctypes.POINTER(c_size)
+
+STATUS = {0: "GNN_OK", 1: "GNN_ERR_INVALID_ARG", 2: "GNN_ERR_UNSUPPORTED", 3: "GNN_ERR_CUDA",
+          4: "GNN_ERR_DEVICE_CHECK", 5: "GNN_ERR_TIMEOUT", 6: "GNN_ERR_CAPACITY"}
+
+CSR_SYMMETRIZE, CSR_DEDUP, CSR_SELF_LOOPS = 1, 2, 4
+CSR_GCN = CSR_SYMMETRIZE | CSR_DEDUP | CSR_SELF_LOOPS
+
+
+class GnnCsr(ctypes.Structure):
+    _fields_ = [("n", c_i32), ("symmetric", c_i32), ("nnz", c_i64), ("rowptr", c_vp),
+                ("col", c_vp), ("val", c_vp), ("split_len", c_i32), ("n_long", c_i32),
+                ("n_pieces", c_i64), ("long_rows", c_vp), ("piece_ptr", c_vp),
+                ("piece_row", c_vp), ("piece_beg", c_vp)]
+
+
+class GnnBitRule(ctypes.Structure):
+    _fields_ = [("n_levels", c_i32), ("pct", c_i32 * 3), ("bits", c_u8 * 4)]
+
+
+class GnnBoundary(ctypes.Structure):
+    _fields_ = [("P", c_i32), ("n", c_i32), ("n_slots", c_i64), ("nnz_cut", c_i64), ("F", c_i32),
+                ("reserved", c_i32), ("part_start", c_vp), ("send_start", c_vp),
+                ("slot_node", c_vp), ("col_remap", c_vp), ("slot_rowptr", c_vp),
+                ("slot_col", c_vp), ("slot_val", c_vp), ("own_ptr", c_vp), ("own_slot", c_vp),
+                ("node_bits", c_vp), ("slot_bits", c_vp), ("slot_off", c_vp)]
+
+
+P_csr = ctypes.POINTER(GnnCsr)
+P_bnd = ctypes.POINTER(GnnBoundary)
+P_rule = ctypes.POINTER(GnnBitRule)
+
+# name -> (restype, argtypes)
+PROTOTYPES = {
+    "gnn_last_error": (c_char_p, []),
+    "gnn_version": (ctypes.c_int, []),
+    "gnn_csr_build_workspace": (ctypes.c_int, [c_i32, c_i64, c_u32, P_size]),
+    "gnn_csr_build": (ctypes.c_int, [c_i32, c_i64, c_vp, c_vp, c_u32, c_i64, P_csr, c_vp, c_size, c_vp]),
+    "gnn_csr_split_workspace": (ctypes.c_int, [P_csr, P_size]),
+    "gnn_csr_split_count": (ctypes.c_int, [P_csr, c_i32, ctypes.POINTER(c_i32), P_i64, c_vp, c_size, c_vp]),
+    "gnn_csr_split": (ctypes.c_int, [P_csr, c_vp, c_size, c_vp]),
+    "gnn_boundary_workspace": (ctypes.c_int, [P_csr, c_i32, P_size]),
+    "gnn_boundary_count": (ctypes.c_int, [P_csr, c_i32, P_i64, P_i64, c_vp, c_size, c_vp]),
+    "gnn_boundary_index": (ctypes.c_int, [P_csr, P_rule, c_u8, c_i32, P_bnd, c_vp, c_size, c_vp]),
+    "gnn_boundary_set_bits": (ctypes.c_int, [P_csr, P_rule, c_u8, c_i32, P_bnd, c_vp, c_size, c_vp]),
+    "gnn_slot_offsets_workspace": (ctypes.c_int, [c_i64, P_size]),
+    "gnn_slot_offsets": (ctypes.c_int, [c_vp, c_i64, c_i32, c_vp, c_vp, c_size, c_vp]),
+    "gnn_quant_pack": (ctypes.c_int, [c_vp, c_i64, c_i32, c_vp, c_i64, c_vp, c_vp, c_u32, c_vp, c_vp, c_vp]),
+    "gnn_dequant_unpack": (ctypes.c_int, [c_vp, c_vp, c_vp, c_vp, c_i64, c_i32, c_vp, c_i64, c_vp]),
+    "gnn_spmm_workspace": (ctypes.c_int, [P_csr, c_i32, P_size]),
+    "gnn_spmm_fwd": (ctypes.c_int, [P_csr, P_bnd, c_vp, c_i64, c_i32, c_vp, c_vp, c_vp, c_i64, c_vp, c_i64,
+                                    c_vp, c_size, c_vp]),
+    "gnn_spmm_bwd": (ctypes.c_int, [P_csr, P_bnd, c_vp, c_i64, c_i32, c_u32, c_vp, c_vp, c_vp, c_i64,
+                                    c_vp, c_size, c_vp]),
+    "gnn_sync_check": (ctypes.c_int, [c_vp]),
+}
+
+_LIB = None
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Load libgnnagg.so (building it first if it is missing or stale)."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    if build_if_missing:
+        _build.build()
+    if not os.path.exists(_build.LIB):
+        raise RuntimeError(f"libgnnagg.so not found at {_build.LIB}; run build() first")
+    lib = ctypes.CDLL(_build.LIB)
+    for name, (res, args) in PROTOTYPES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _LIB = lib
+    return lib
+
+
+class GnnError(RuntimeError):
+    def __init__(self, name, status, msg):
+        super().__init__(f"{name} -> {STATUS.get(status, status)}: {msg}")
+        self.status = status
+
+
+def call(name, *args):
+    lib = load()
+    st = getattr(lib, name)(*args)
+    if st != 0:
+        raise GnnError(name, st, lib.gnn_last_error().decode(errors="replace"))
+    return st

@@ -1,0 +1,178 @@
+// Device helpers: hashing, the fp32 quantiser, packing and unpacking of
+// message rows held in registers.
+//
+// Register layout used by every row kernel: a group of G lanes (G a power of
+// two, G divides 32) owns one row; lane g of the group holds the 4-element
+// chunks c = g + i*G for i < CPL, chunk c covering elements 4c..4c+3.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gnn {
+
+// MurmurHash3's 32-bit finaliser (Appleby, SMHasher, public domain).
+__device__ __forceinline__ uint32_t fmix32(uint32_t h) {
+  h ^= h >> 16;
+  h *= 0x85ebca6bu;
+  h ^= h >> 13;
+  h *= 0xc2b2ae35u;
+  h ^= h >> 16;
+  return h;
+}
+
+// Per-row part of hash32(seed, r, j) = fmix32(fmix32(seed ^ fmix32(r)) ^ j).
+__device__ __forceinline__ uint32_t row_key(uint32_t seed, uint32_t r) {
+  return fmix32(seed ^ fmix32(r));
+}
+
+// Stochastic-rounding offset u = (hash32 >> 8) * 2^-24, exact in fp32.
+__device__ __forceinline__ float sr_offset(uint32_t key, uint32_t j) {
+  return __fmul_rn(static_cast<float>(fmix32(key ^ j) >> 8), 5.9604644775390625e-08f);
+}
+
+__device__ __forceinline__ uint32_t group_mask(int G, int lane) {
+  return G == 32 ? 0xffffffffu : (((1u << G) - 1u) << (lane & ~(G - 1)));
+}
+
+__device__ __forceinline__ float elem(const float4& v, int k) {
+  return k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w));
+}
+
+__device__ __forceinline__ uint32_t rowbytes_dev(int b, int F) {
+  return b == 32 ? 16u * ((4u * F + 15u) / 16u) : 16u * ((uint32_t)(F * b + 127) / 128u);
+}
+
+// Quantises the group's row held in v[] (elements >= F ignored) with width b
+// and row key `key`, writes the packed row at `out` (16-byte aligned) and
+// (mn, scale) at meta (lane 0 of the group).  All lanes of the group must call.
+template <int G, int CPL>
+__device__ __forceinline__ void quantize_pack_row(const float4 (&v)[CPL], int F, int b,
+                                                  uint32_t key, uint8_t* __restrict__ out,
+                                                  float2* __restrict__ meta, int gl,
+                                                  uint32_t gmask) {
+  const int nch = (F + 3) >> 2;
+  if (b == 32) {
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+      const int c = gl + i * G;
+      if (c < nch) {
+        float4 x = v[i];
+        const int j0 = 4 * c;
+        if (j0 + 1 >= F) x.y = 0.f;
+        if (j0 + 2 >= F) x.z = 0.f;
+        if (j0 + 3 >= F) x.w = 0.f;
+        reinterpret_cast<float4*>(out)[c] = x;
+      }
+    }
+    if (gl == 0) *meta = make_float2(0.f, 0.f);
+    return;
+  }
+  float mn = __int_as_float(0x7f800000), mx = -__int_as_float(0x7f800000);
+#pragma unroll
+  for (int i = 0; i < CPL; ++i) {
+    const int c = gl + i * G;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (c < nch && 4 * c + k < F) {
+        const float x = elem(v[i], k);
+        mn = fminf(mn, x);
+        mx = fmaxf(mx, x);
+      }
+    }
+  }
+#pragma unroll
+  for (int o = G / 2; o > 0; o >>= 1) {
+    mn = fminf(mn, __shfl_xor_sync(gmask, mn, o));
+    mx = fmaxf(mx, __shfl_xor_sync(gmask, mx, o));
+  }
+  if (__float_as_uint(mn) == 0x80000000u) mn = 0.f;  // a zero min/max is stored as +0
+  if (__float_as_uint(mx) == 0x80000000u) mx = 0.f;
+  const float top = static_cast<float>((1u << b) - 1u);
+  const bool flat = !(mx > mn);
+  const float scale = flat ? 0.f : __fdiv_rn(__fsub_rn(mx, mn), top);
+  // chunk slots covered by the padded row: rowbytes*2/b chunks
+  const int slots = (int)(rowbytes_dev(b, F) * 2u) / b;
+  const int per_word = 8 / b;  // chunks per 32-bit word
+  uint32_t* words = reinterpret_cast<uint32_t*>(out);
+#pragma unroll
+  for (int i = 0; i < CPL; ++i) {
+    const int c = gl + i * G;
+    uint32_t part = 0;
+    if (c < nch && !flat) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int j = 4 * c + k;
+        if (j < F) {
+          const float t = __fdiv_rn(__fsub_rn(elem(v[i], k), mn), scale);
+          const float u = sr_offset(key, (uint32_t)j);
+          const float q = fminf(floorf(__fadd_rn(t, u)), top);
+          part |= static_cast<uint32_t>(q) << (k * b);
+        }
+      }
+    }
+    // the per_word chunks of one word sit on consecutive lanes of the group
+    part <<= (c % per_word) * 4 * b;
+    for (int o = 1; o < per_word; o <<= 1) part |= __shfl_xor_sync(gmask, part, o);
+    if (c < slots && (c % per_word) == 0) words[(c * b) >> 3] = part;
+  }
+  if (gl == 0) *meta = make_float2(mn, scale);
+}
+
+// The 4 dequantised values of chunk c of a packed row (width b, meta m).
+__device__ __forceinline__ float4 dequant_chunk(const uint8_t* __restrict__ row, int b,
+                                                float mn, float scale, int c) {
+  if (b == 32) return __ldg(reinterpret_cast<const float4*>(row) + c);
+  const uint32_t bitpos = (uint32_t)(4 * c * b);
+  const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(row) + (bitpos >> 5));
+  const uint32_t bits4 = w >> (bitpos & 31u);
+  const uint32_t m = (1u << b) - 1u;
+  float4 r;
+  r.x = __fadd_rn(__fmul_rn(scale, (float)(bits4 & m)), mn);
+  r.y = __fadd_rn(__fmul_rn(scale, (float)((bits4 >> b) & m)), mn);
+  r.z = __fadd_rn(__fmul_rn(scale, (float)((bits4 >> (2 * b)) & m)), mn);
+  r.w = __fadd_rn(__fmul_rn(scale, (float)((bits4 >> (3 * b)) & m)), mn);
+  return r;
+}
+
+__device__ __forceinline__ void fma4(float4& acc, float w, const float4& x) {
+  acc.x = fmaf(w, x.x, acc.x);
+  acc.y = fmaf(w, x.y, acc.y);
+  acc.z = fmaf(w, x.z, acc.z);
+  acc.w = fmaf(w, x.w, acc.w);
+}
+
+__device__ __forceinline__ void add4(float4& acc, const float4& x) {
+  acc.x += x.x;
+  acc.y += x.y;
+  acc.z += x.z;
+  acc.w += x.w;
+}
+
+// Stores chunk c of an fp32 row, zeroing elements >= F.
+__device__ __forceinline__ void store_chunk_f32(float* __restrict__ row, int c, int F, float4 x) {
+  const int j0 = 4 * c;
+  if (j0 + 1 >= F) x.y = 0.f;
+  if (j0 + 2 >= F) x.z = 0.f;
+  if (j0 + 3 >= F) x.w = 0.f;
+  reinterpret_cast<float4*>(row)[c] = x;
+}
+
+// Stores chunk c of a bf16 row (4 values, 8 bytes), zeroing elements >= F.
+__device__ __forceinline__ void store_chunk_bf16(__nv_bfloat16* __restrict__ row, int c, int F,
+                                                 float4 x) {
+  const int j0 = 4 * c;
+  if (j0 >= F) x.x = 0.f;
+  if (j0 + 1 >= F) x.y = 0.f;
+  if (j0 + 2 >= F) x.z = 0.f;
+  if (j0 + 3 >= F) x.w = 0.f;
+  __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y);
+  __nv_bfloat162 hi = __floats2bfloat162_rn(x.z, x.w);
+  uint2 p;
+  p.x = *reinterpret_cast<uint32_t*>(&lo);
+  p.y = *reinterpret_cast<uint32_t*>(&hi);
+  reinterpret_cast<uint2*>(row)[c] = p;
+}
+
+}  // namespace gnn

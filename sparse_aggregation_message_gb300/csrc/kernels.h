@@ -1,0 +1,36 @@
+// Launch wrappers shared between the library's translation units.  They do
+// no argument checking; the extern "C" entry points do that first.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gnnagg.h"
+
+namespace gnn {
+
+gnn_status launch_quant_pack(const float* X, int64_t ldx, int F, const int32_t* row_idx,
+                             int64_t n_rows, const uint8_t* bits, const int64_t* off,
+                             uint32_t seed, uint8_t* packed, float2* meta, cudaStream_t st);
+
+gnn_status launch_dequant_unpack(const uint8_t* packed, const float2* meta, const int64_t* off,
+                                 const uint8_t* bits, int64_t n_rows, int F, float* out,
+                                 int64_t ldo, cudaStream_t st);
+
+// M = A H (bnd NULL) or the partitioned forward aggregation; fp32 and/or bf16
+// outputs (either may be NULL).
+// `partial` holds one fp32 row per piece of csr's split plan (may be NULL
+// without a plan).
+gnn_status launch_spmm_fwd(const gnn_csr& csr, const gnn_boundary* bnd, const float* H,
+                           int64_t ldh, int F, const uint8_t* packed, const float2* meta,
+                           float* M, int64_t ldm, uint16_t* Mb, int64_t ldmb, float* partial,
+                           cudaStream_t st);
+
+gnn_status launch_spmm_bwd(const gnn_csr& csr, const gnn_boundary* bnd, const float* G,
+                           int64_t ldg, int F, uint32_t seed, uint8_t* packed_ws,
+                           float2* meta_ws, float* dH, int64_t ldh, float* partial,
+                           cudaStream_t st);
+
+size_t spmm_workspace_bytes(const gnn_csr& csr, int F);
+
+}  // namespace gnn

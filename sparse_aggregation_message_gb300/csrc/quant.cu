@@ -1,0 +1,143 @@
+// Stochastic integer quantisation + packing of message rows, and the
+// standalone receive-side unpacking (SYLVIE guide, section 6).
+#include <cuda_runtime.h>
+
+#include "device.cuh"
+#include "internal.h"
+#include "kernels.h"
+
+namespace gnn {
+
+template <int G, int CPL>
+__global__ void __launch_bounds__(256) quant_pack_kernel(
+    const float* __restrict__ X, int64_t ldx, int F, const int32_t* __restrict__ row_idx,
+    int64_t n_rows, const uint8_t* __restrict__ row_bits, const int64_t* __restrict__ row_off,
+    uint32_t seed, uint8_t* __restrict__ packed, float2* __restrict__ meta) {
+  const int lane = threadIdx.x & 31;
+  const int gl = lane & (G - 1);
+  const int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / G;
+  if (r >= n_rows) return;  // uniform across the group
+  const uint32_t gmask = group_mask(G, lane);
+  const int64_t src = row_idx ? (int64_t)__ldg(row_idx + r) : r;
+  const float4* x = reinterpret_cast<const float4*>(X + src * ldx);
+  const int nch = (F + 3) >> 2;
+  float4 v[CPL];
+#pragma unroll
+  for (int i = 0; i < CPL; ++i) {
+    const int c = gl + i * G;
+    v[i] = c < nch ? __ldg(x + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  const int b = __ldg(row_bits + r);
+  quantize_pack_row<G, CPL>(v, F, b, row_key(seed, (uint32_t)r), packed + __ldg(row_off + r),
+                            meta + r, gl, gmask);
+}
+
+template <int G>
+__global__ void __launch_bounds__(256) dequant_unpack_kernel(
+    const uint8_t* __restrict__ packed, const float2* __restrict__ meta,
+    const int64_t* __restrict__ row_off, const uint8_t* __restrict__ row_bits, int64_t n_rows,
+    int F, float* __restrict__ out, int64_t ldo) {
+  const int lane = threadIdx.x & 31;
+  const int gl = lane & (G - 1);
+  const int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / G;
+  if (r >= n_rows) return;
+  const int b = __ldg(row_bits + r);
+  const float2 m = __ldg(meta + r);
+  const uint8_t* row = packed + __ldg(row_off + r);
+  float* o = out + r * ldo;
+  const int nch = (F + 3) >> 2;
+  for (int c = gl; c < nch; c += G) store_chunk_f32(o, c, F, dequant_chunk(row, b, m.x, m.y, c));
+}
+
+// Chunk slots a packed row of width 1 (the widest padding) spans.
+static int quant_chunk_slots(int F) { return 32 * ((F + 127) / 128) > (F + 3) / 4 ? 32 * ((F + 127) / 128) : (F + 3) / 4; }
+
+template <int G, int CPL>
+static void launch_qp(const float* X, int64_t ldx, int F, const int32_t* row_idx, int64_t n_rows,
+                      const uint8_t* bits, const int64_t* off, uint32_t seed, uint8_t* packed,
+                      float2* meta, cudaStream_t st) {
+  const int64_t threads = n_rows * G;
+  const int block = 256;
+  const int64_t grid = (threads + block - 1) / block;
+  quant_pack_kernel<G, CPL><<<(unsigned)grid, block, 0, st>>>(X, ldx, F, row_idx, n_rows, bits,
+                                                               off, seed, packed, meta);
+}
+
+gnn_status launch_quant_pack(const float* X, int64_t ldx, int F, const int32_t* row_idx,
+                             int64_t n_rows, const uint8_t* bits, const int64_t* off,
+                             uint32_t seed, uint8_t* packed, float2* meta, cudaStream_t st) {
+  if (n_rows == 0) return GNN_OK;
+  const int slots = quant_chunk_slots(F);
+  if (slots <= 32) {
+    launch_qp<8, 4>(X, ldx, F, row_idx, n_rows, bits, off, seed, packed, meta, st);
+  } else {
+    switch ((slots + 31) / 32) {
+      case 1: launch_qp<32, 1>(X, ldx, F, row_idx, n_rows, bits, off, seed, packed, meta, st); break;
+      case 2: launch_qp<32, 2>(X, ldx, F, row_idx, n_rows, bits, off, seed, packed, meta, st); break;
+      case 3: launch_qp<32, 3>(X, ldx, F, row_idx, n_rows, bits, off, seed, packed, meta, st); break;
+      case 4: launch_qp<32, 4>(X, ldx, F, row_idx, n_rows, bits, off, seed, packed, meta, st); break;
+      case 5: launch_qp<32, 5>(X, ldx, F, row_idx, n_rows, bits, off, seed, packed, meta, st); break;
+      case 6: launch_qp<32, 6>(X, ldx, F, row_idx, n_rows, bits, off, seed, packed, meta, st); break;
+      case 7: launch_qp<32, 7>(X, ldx, F, row_idx, n_rows, bits, off, seed, packed, meta, st); break;
+      case 8: launch_qp<32, 8>(X, ldx, F, row_idx, n_rows, bits, off, seed, packed, meta, st); break;
+      default: return fail(GNN_ERR_UNSUPPORTED, "quant_pack: F=%d exceeds %d", F, kMaxF);
+    }
+  }
+  GNN_CHECK_LAUNCH();
+  return GNN_OK;
+}
+
+gnn_status launch_dequant_unpack(const uint8_t* packed, const float2* meta, const int64_t* off,
+                                 const uint8_t* bits, int64_t n_rows, int F, float* out,
+                                 int64_t ldo, cudaStream_t st) {
+  if (n_rows == 0) return GNN_OK;
+  const int nch = (F + 3) / 4;
+  const int block = 256;
+  if (nch <= 8) {
+    const int64_t grid = (n_rows * 8 + block - 1) / block;
+    dequant_unpack_kernel<8><<<(unsigned)grid, block, 0, st>>>(packed, meta, off, bits, n_rows, F,
+                                                               out, ldo);
+  } else {
+    const int64_t grid = (n_rows * 32 + block - 1) / block;
+    dequant_unpack_kernel<32><<<(unsigned)grid, block, 0, st>>>(packed, meta, off, bits, n_rows,
+                                                                F, out, ldo);
+  }
+  GNN_CHECK_LAUNCH();
+  return GNN_OK;
+}
+
+}  // namespace gnn
+
+using namespace gnn;
+
+extern "C" gnn_status gnn_quant_pack(const float* X, int64_t ldx, int32_t F, const int32_t* row_idx,
+                                     int64_t n_rows, const uint8_t* row_bits,
+                                     const int64_t* row_off, uint32_t seed, uint8_t* packed,
+                                     float* meta, gnn_stream_t stream) {
+  GNN_REQUIRE(n_rows >= 0, "gnn_quant_pack: n_rows < 0");
+  GNN_REQUIRE(F >= 1, "gnn_quant_pack: F must be >= 1");
+  if (F > kMaxF) return fail(GNN_ERR_UNSUPPORTED, "gnn_quant_pack: F=%d > %d", F, kMaxF);
+  if (n_rows == 0) return GNN_OK;
+  GNN_REQUIRE(X && row_bits && row_off && packed && meta, "gnn_quant_pack: NULL pointer");
+  GNN_REQUIRE(ldx >= F && ldx % 4 == 0, "gnn_quant_pack: ldx must be >= F and a multiple of 4");
+  GNN_REQUIRE(((uintptr_t)X & 15) == 0 && ((uintptr_t)packed & 15) == 0 && ((uintptr_t)meta & 7) == 0,
+              "gnn_quant_pack: X and packed must be 16-byte aligned, meta 8-byte aligned");
+  return launch_quant_pack(X, ldx, F, row_idx, n_rows, row_bits, row_off, seed, packed,
+                           reinterpret_cast<float2*>(meta), as_stream(stream));
+}
+
+extern "C" gnn_status gnn_dequant_unpack(const uint8_t* packed, const float* meta,
+                                         const int64_t* row_off, const uint8_t* row_bits,
+                                         int64_t n_rows, int32_t F, float* out, int64_t ldo,
+                                         gnn_stream_t stream) {
+  GNN_REQUIRE(n_rows >= 0, "gnn_dequant_unpack: n_rows < 0");
+  GNN_REQUIRE(F >= 1, "gnn_dequant_unpack: F must be >= 1");
+  if (F > kMaxF) return fail(GNN_ERR_UNSUPPORTED, "gnn_dequant_unpack: F=%d > %d", F, kMaxF);
+  if (n_rows == 0) return GNN_OK;
+  GNN_REQUIRE(packed && meta && row_off && row_bits && out, "gnn_dequant_unpack: NULL pointer");
+  GNN_REQUIRE(ldo >= F && ldo % 4 == 0, "gnn_dequant_unpack: ldo must be >= F and a multiple of 4");
+  GNN_REQUIRE(((uintptr_t)out & 15) == 0 && ((uintptr_t)packed & 15) == 0 && ((uintptr_t)meta & 7) == 0,
+              "gnn_dequant_unpack: out and packed must be 16-byte aligned, meta 8-byte aligned");
+  return launch_dequant_unpack(packed, reinterpret_cast<const float2*>(meta), row_off, row_bits,
+                               n_rows, F, out, ldo, as_stream(stream));
+}

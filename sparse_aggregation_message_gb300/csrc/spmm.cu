@@ -1,0 +1,533 @@
+// GCN aggregation kernels (SYLVIE guide sections 2, 3 and 11):
+//   forward  M = A H, remote sources replaced by their dequantised messages;
+//   backward halo partials of every slot (fixed fp32 order) fused with their
+//            quantisation and packing, then dH = local A^T G + owned messages.
+//
+// One group of G lanes owns one output row (or one piece of a long row); lane
+// g holds the float4 chunks c = g + i*G (i < CPL) of the row in registers, so
+// every gathered source row is read with coalesced 16-byte loads.  A group
+// walks its entries G at a time: the G lanes load G (col, val) pairs -- and,
+// for remote entries, the slot's width, offset and meta -- in one coalesced
+// step, then broadcast them with shuffles while all lanes gather U entries at
+// a time (U loads in flight per lane and chunk).
+//
+// Load balance on power-law graphs: rows longer than the CSR's split_len are
+// cut into pieces of split_len entries.  Pieces run as their own groups at
+// the front of the grid and leave fp32 partial rows in the workspace; a fixup
+// kernel adds a row's pieces in piece order (deterministic) and writes it.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "device.cuh"
+#include "internal.h"
+#include "kernels.h"
+
+namespace gnn {
+
+enum SpmmMode { kPlain = 0, kFwdRemote = 1, kBwdOwned = 2 };
+
+struct SlotMsgs {
+  const uint8_t* packed;
+  const float2* meta;
+  const int64_t* off;
+  const uint8_t* bits;
+};
+
+struct RowSplit {
+  int T;  // split_len; 0 = no plan
+  int n_long;
+  int64_t n_pieces;
+  const int32_t* long_rows;
+  const int64_t* piece_ptr;
+  const int32_t* piece_row;
+  const int64_t* piece_beg;
+};
+
+// acc += sum over entries [beg, end) of val * x, x = H[col] or the remote
+// slot's dequantised message (kFwdRemote); remote entries are skipped in the
+// backward (their contribution arrives as the owner's message).
+template <int G, int CPL, int MODE, int U>
+__device__ __forceinline__ void gather_range(int64_t beg, int64_t end, int64_t self_row,
+                                             const int32_t* __restrict__ col,
+                                             const float* __restrict__ val,
+                                             const float4* __restrict__ H4, int64_t ldh4, int nch,
+                                             const SlotMsgs& msg, int gl, uint32_t gmask,
+                                             float4 (&acc)[CPL]) {
+  float4 acc1[CPL];
+#pragma unroll
+  for (int i = 0; i < CPL; ++i) acc1[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int64_t base = beg; base < end; base += G) {
+    const int64_t e = base + gl;
+    int cc = (int)self_row;
+    float w = 0.f;
+    int sb = 0;
+    uint32_t so16 = 0;
+    float2 sm = make_float2(0.f, 0.f);
+    if (e < end) {
+      cc = __ldg(col + e);
+      w = __ldg(val + e);
+      if (MODE == kFwdRemote && cc < 0) {
+        const int s = ~cc;
+        sb = __ldg(msg.bits + s);
+        so16 = (uint32_t)(__ldg(msg.off + s) >> 4);
+        sm = __ldg(msg.meta + s);
+      }
+      if (MODE == kBwdOwned && cc < 0) {
+        cc = (int)self_row;
+        w = 0.f;
+      }
+    }
+    const int cnt = (int)min((int64_t)G, end - base);
+    for (int k = 0; k < cnt; k += U) {
+      float4 x[U][CPL];
+      float wk[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int src = (k + u < cnt) ? k + u : k;
+        const int ck = __shfl_sync(gmask, cc, src, G);
+        wk[u] = __shfl_sync(gmask, w, src, G);
+        if (k + u >= cnt) wk[u] = 0.f;
+        if (MODE == kFwdRemote) {
+          const int bk = __shfl_sync(gmask, sb, src, G);
+          const uint32_t ok = __shfl_sync(gmask, so16, src, G);
+          const float mnk = __shfl_sync(gmask, sm.x, src, G);
+          const float sck = __shfl_sync(gmask, sm.y, src, G);
+#pragma unroll
+          for (int i = 0; i < CPL; ++i) {
+            const int c = gl + i * G;
+            if (c < nch)
+              x[u][i] = ck >= 0 ? __ldg(H4 + (int64_t)ck * ldh4 + c)
+                                : dequant_chunk(msg.packed + ((size_t)ok << 4), bk, mnk, sck, c);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < CPL; ++i) {
+            const int c = gl + i * G;
+            if (c < nch) x[u][i] = __ldg(H4 + (int64_t)ck * ldh4 + c);
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) {
+          if (gl + i * G < nch) {
+            if (u & 1) fma4(acc1[i], wk[u], x[u][i]);
+            else fma4(acc[i], wk[u], x[u][i]);
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < CPL; ++i) add4(acc[i], acc1[i]);
+}
+
+// acc += dequantised messages of the slots row r owns (backward).
+template <int G, int CPL>
+__device__ __forceinline__ void add_owned(int64_t r, const int64_t* __restrict__ own_ptr,
+                                          const int32_t* __restrict__ own_slot,
+                                          const SlotMsgs& msg, int nch, int gl,
+                                          float4 (&acc)[CPL]) {
+  const int64_t ob = __ldg(own_ptr + r), oe = __ldg(own_ptr + r + 1);
+  for (int64_t o = ob; o < oe; ++o) {
+    const int s = __ldg(own_slot + o);
+    const int b = __ldg(msg.bits + s);
+    const float2 m = __ldg(msg.meta + s);
+    const uint8_t* row = msg.packed + __ldg(msg.off + s);
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+      const int c = gl + i * G;
+      if (c < nch) add4(acc[i], dequant_chunk(row, b, m.x, m.y, c));
+    }
+  }
+}
+
+template <int G, int CPL>
+__device__ __forceinline__ void store_row(int64_t r, const float4 (&acc)[CPL], int F, int nch,
+                                          int nch_b, int gl, float* __restrict__ M, int64_t ldm,
+                                          __nv_bfloat16* __restrict__ Mb, int64_t ldmb) {
+  if (M) {
+    float* mrow = M + r * ldm;
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+      const int c = gl + i * G;
+      if (c < nch) store_chunk_f32(mrow, c, F, acc[i]);
+    }
+  }
+  if (Mb) {
+    __nv_bfloat16* brow = Mb + r * ldmb;
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+      const int c = gl + i * G;
+      if (c < nch_b)
+        store_chunk_bf16(brow, c, F, c < nch ? acc[i] : make_float4(0.f, 0.f, 0.f, 0.f));
+    }
+  }
+}
+
+template <int G, int CPL, int MODE, int U>
+__global__ void __launch_bounds__(256) spmm_rows_kernel(
+    int n, const int64_t* __restrict__ rowptr, const int32_t* __restrict__ col,
+    const float* __restrict__ val, const float* __restrict__ H, int64_t ldh, int F,
+    SlotMsgs msg, const int64_t* __restrict__ own_ptr, const int32_t* __restrict__ own_slot,
+    RowSplit sp, float* __restrict__ partial, float* __restrict__ M, int64_t ldm,
+    __nv_bfloat16* __restrict__ Mb, int64_t ldmb, int nch_b) {
+  const int lane = threadIdx.x & 31;
+  const int gl = lane & (G - 1);
+  const int64_t g = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / G;
+  const uint32_t gmask = group_mask(G, lane);
+  const int nch = (F + 3) >> 2;
+  const float4* H4 = reinterpret_cast<const float4*>(H);
+  const int64_t ldh4 = ldh >> 2;
+  float4 acc[CPL];
+#pragma unroll
+  for (int i = 0; i < CPL; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+
+  if (g < sp.n_pieces) {  // a piece of a long row -> partial row g
+    const int64_t row = __ldg(sp.piece_row + g);
+    const int64_t beg = __ldg(sp.piece_beg + g);
+    const int64_t end = min(beg + (int64_t)sp.T, __ldg(rowptr + row + 1));
+    gather_range<G, CPL, MODE, U>(beg, end, row, col, val, H4, ldh4, nch, msg, gl, gmask, acc);
+    float4* prow = reinterpret_cast<float4*>(partial) + g * nch;
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+      const int c = gl + i * G;
+      if (c < nch) prow[c] = acc[i];
+    }
+    return;
+  }
+  const int64_t r = g - sp.n_pieces;
+  if (r >= n) return;  // uniform across the group
+  const int64_t beg = __ldg(rowptr + r), end = __ldg(rowptr + r + 1);
+  if (sp.T > 0 && end - beg > sp.T) return;  // a long row: its pieces cover it
+  gather_range<G, CPL, MODE, U>(beg, end, r, col, val, H4, ldh4, nch, msg, gl, gmask, acc);
+  if (MODE == kBwdOwned) add_owned<G, CPL>(r, own_ptr, own_slot, msg, nch, gl, acc);
+  store_row<G, CPL>(r, acc, F, nch, nch_b, gl, M, ldm, Mb, ldmb);
+}
+
+// Long rows: sum of their pieces' partial rows in piece order.
+template <int G, int CPL, int MODE>
+__global__ void __launch_bounds__(256) spmm_fixup_kernel(
+    RowSplit sp, const float* __restrict__ partial, int F, SlotMsgs msg,
+    const int64_t* __restrict__ own_ptr, const int32_t* __restrict__ own_slot,
+    float* __restrict__ M, int64_t ldm, __nv_bfloat16* __restrict__ Mb, int64_t ldmb,
+    int nch_b) {
+  const int lane = threadIdx.x & 31;
+  const int gl = lane & (G - 1);
+  const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / G;
+  if (i >= sp.n_long) return;
+  const int nch = (F + 3) >> 2;
+  const int64_t row = __ldg(sp.long_rows + i);
+  const int64_t pb = __ldg(sp.piece_ptr + i), pe = __ldg(sp.piece_ptr + i + 1);
+  float4 acc[CPL];
+#pragma unroll
+  for (int k = 0; k < CPL; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  const float4* P4 = reinterpret_cast<const float4*>(partial);
+  for (int64_t p = pb; p < pe; ++p) {
+#pragma unroll
+    for (int k = 0; k < CPL; ++k) {
+      const int c = gl + k * G;
+      if (c < nch) add4(acc[k], __ldg(P4 + p * nch + c));
+    }
+  }
+  if (MODE == kBwdOwned) add_owned<G, CPL>(row, own_ptr, own_slot, msg, nch, gl, acc);
+  store_row<G, CPL>(row, acc, F, nch, nch_b, gl, M, ldm, Mb, ldmb);
+}
+
+// Backward messages: halo partial of slot s over its entries in ascending v,
+// every product and sum rounded to fp32 (start +0), then quantised and packed
+// in registers with row key s.  U entries are loaded ahead of their adds; the
+// adds stay in entry order.
+template <int G, int CPL, int U>
+__global__ void __launch_bounds__(256) halo_quant_pack_kernel(
+    int64_t S, const int64_t* __restrict__ srp, const int32_t* __restrict__ scol,
+    const float* __restrict__ sval, const float* __restrict__ Gm, int64_t ldg, int F,
+    const uint8_t* __restrict__ slot_bits, const int64_t* __restrict__ slot_off, uint32_t seed,
+    uint8_t* __restrict__ packed, float2* __restrict__ meta) {
+  const int lane = threadIdx.x & 31;
+  const int gl = lane & (G - 1);
+  const int64_t s = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / G;
+  if (s >= S) return;
+  const uint32_t gmask = group_mask(G, lane);
+  const int nch = (F + 3) >> 2;
+  const float4* G4 = reinterpret_cast<const float4*>(Gm);
+  const int64_t ldg4 = ldg >> 2;
+  float4 acc[CPL];
+#pragma unroll
+  for (int i = 0; i < CPL; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int64_t beg = __ldg(srp + s), end = __ldg(srp + s + 1);
+  for (int64_t base = beg; base < end; base += G) {
+    const int64_t e = base + gl;
+    int v = 0;
+    float w = 0.f;
+    if (e < end) {
+      v = __ldg(scol + e);
+      w = __ldg(sval + e);
+    }
+    const int cnt = (int)min((int64_t)G, end - base);
+    for (int k = 0; k < cnt; k += U) {
+      float4 x[U][CPL];
+      float wk[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int src = (k + u < cnt) ? k + u : k;
+        const int vk = __shfl_sync(gmask, v, src, G);
+        wk[u] = __shfl_sync(gmask, w, src, G);
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) {
+          const int c = gl + i * G;
+          if (c < nch) x[u][i] = __ldg(G4 + (int64_t)vk * ldg4 + c);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (k + u < cnt) {
+#pragma unroll
+          for (int i = 0; i < CPL; ++i) {
+            if (gl + i * G < nch) {
+              acc[i].x = __fadd_rn(acc[i].x, __fmul_rn(wk[u], x[u][i].x));
+              acc[i].y = __fadd_rn(acc[i].y, __fmul_rn(wk[u], x[u][i].y));
+              acc[i].z = __fadd_rn(acc[i].z, __fmul_rn(wk[u], x[u][i].z));
+              acc[i].w = __fadd_rn(acc[i].w, __fmul_rn(wk[u], x[u][i].w));
+            }
+          }
+        }
+      }
+    }
+  }
+  quantize_pack_row<G, CPL>(acc, F, __ldg(slot_bits + s), row_key(seed, (uint32_t)s),
+                            packed + __ldg(slot_off + s), meta + s, gl, gmask);
+}
+
+// ---------------------------------------------------------------- dispatch
+static RowSplit row_split_of(const gnn_csr& csr) {
+  RowSplit sp{};
+  if (csr.split_len > 0) {
+    sp.T = csr.split_len;
+    sp.n_long = csr.n_long;
+    sp.n_pieces = csr.n_pieces;
+    sp.long_rows = csr.long_rows;
+    sp.piece_ptr = csr.piece_ptr;
+    sp.piece_row = csr.piece_row;
+    sp.piece_beg = csr.piece_beg;
+  }
+  return sp;
+}
+
+template <int MODE>
+static gnn_status dispatch_rows(const gnn_csr& csr, const int32_t* colv, const float* H,
+                                int64_t ldh, int F, SlotMsgs msg, const int64_t* own_ptr,
+                                const int32_t* own_slot, float* partial, float* M, int64_t ldm,
+                                __nv_bfloat16* Mb, int64_t ldmb, cudaStream_t st) {
+  const int nch = (F + 3) / 4;
+  const int nch_b = Mb ? ((F + 15) / 16) * 4 : nch;
+  const int need = nch_b > nch ? nch_b : nch;
+  const RowSplit sp = row_split_of(csr);
+  const int block = 256;
+#define GNN_ROWS(G_, CPL_, U_)                                                                 \
+  do {                                                                                         \
+    const int64_t groups = (int64_t)csr.n + sp.n_pieces;                                       \
+    const int64_t grid = (groups * G_ + block - 1) / block;                                    \
+    spmm_rows_kernel<G_, CPL_, MODE, U_><<<(unsigned)grid, block, 0, st>>>(                    \
+        csr.n, csr.rowptr, colv, csr.val, H, ldh, F, msg, own_ptr, own_slot, sp, partial, M,   \
+        ldm, Mb, ldmb, nch_b);                                                                 \
+    GNN_CHECK_LAUNCH();                                                                        \
+    if (sp.n_long > 0) {                                                                       \
+      const int64_t g2 = ((int64_t)sp.n_long * G_ + block - 1) / block;                        \
+      spmm_fixup_kernel<G_, CPL_, MODE><<<(unsigned)g2, block, 0, st>>>(                       \
+          sp, partial, F, msg, own_ptr, own_slot, M, ldm, Mb, ldmb, nch_b);                    \
+      GNN_CHECK_LAUNCH();                                                                      \
+    }                                                                                          \
+  } while (0)
+  if (need <= 4) GNN_ROWS(4, 1, 4);
+  else if (need <= 8) GNN_ROWS(8, 1, 4);
+  else if (need <= 16) GNN_ROWS(16, 1, 4);
+  else {
+    switch ((need + 31) / 32) {
+      case 1: GNN_ROWS(32, 1, 4); break;
+      case 2: GNN_ROWS(32, 2, 4); break;
+      case 3: GNN_ROWS(32, 3, 2); break;
+      case 4: GNN_ROWS(32, 4, 2); break;
+      case 5: GNN_ROWS(32, 5, 2); break;
+      case 6: GNN_ROWS(32, 6, 2); break;
+      case 7: GNN_ROWS(32, 7, 2); break;
+      case 8: GNN_ROWS(32, 8, 2); break;
+      default: return fail(GNN_ERR_UNSUPPORTED, "spmm: F=%d exceeds %d", F, kMaxF);
+    }
+  }
+#undef GNN_ROWS
+  return GNN_OK;
+}
+
+gnn_status launch_spmm_fwd(const gnn_csr& csr, const gnn_boundary* bnd, const float* H,
+                           int64_t ldh, int F, const uint8_t* packed, const float2* meta,
+                           float* M, int64_t ldm, uint16_t* Mb, int64_t ldmb, float* partial,
+                           cudaStream_t st) {
+  if (csr.n == 0) return GNN_OK;
+  auto* mb = reinterpret_cast<__nv_bfloat16*>(Mb);
+  if (!bnd)
+    return dispatch_rows<kPlain>(csr, csr.col, H, ldh, F, SlotMsgs{}, nullptr, nullptr, partial,
+                                 M, ldm, mb, ldmb, st);
+  SlotMsgs msg{packed, meta, bnd->slot_off, bnd->slot_bits};
+  return dispatch_rows<kFwdRemote>(csr, bnd->col_remap, H, ldh, F, msg, nullptr, nullptr, partial,
+                                   M, ldm, mb, ldmb, st);
+}
+
+static int quant_chunk_slots(int F) {
+  const int a = 32 * ((F + 127) / 128), b = (F + 3) / 4;
+  return a > b ? a : b;
+}
+
+gnn_status launch_halo_quant_pack(const gnn_boundary& b, const float* Gm, int64_t ldg, int F,
+                                  uint32_t seed, uint8_t* packed_ws, float2* meta_ws,
+                                  cudaStream_t st) {
+  const int64_t S = b.n_slots;
+  if (S == 0) return GNN_OK;
+  const int slots = quant_chunk_slots(F);
+  const int block = 256;
+#define GNN_HALO(G_, CPL_, U_)                                                                   \
+  do {                                                                                           \
+    const int64_t grid = (S * G_ + block - 1) / block;                                           \
+    halo_quant_pack_kernel<G_, CPL_, U_><<<(unsigned)grid, block, 0, st>>>(                      \
+        S, b.slot_rowptr, b.slot_col, b.slot_val, Gm, ldg, F, b.slot_bits, b.slot_off, seed,     \
+        packed_ws, meta_ws);                                                                     \
+  } while (0)
+  if (slots <= 32) GNN_HALO(8, 4, 2);
+  else {
+    switch ((slots + 31) / 32) {
+      case 1: GNN_HALO(32, 1, 4); break;
+      case 2: GNN_HALO(32, 2, 4); break;
+      case 3: GNN_HALO(32, 3, 2); break;
+      case 4: GNN_HALO(32, 4, 2); break;
+      case 5: GNN_HALO(32, 5, 2); break;
+      case 6: GNN_HALO(32, 6, 2); break;
+      case 7: GNN_HALO(32, 7, 2); break;
+      case 8: GNN_HALO(32, 8, 2); break;
+      default: return fail(GNN_ERR_UNSUPPORTED, "spmm_bwd: F=%d exceeds %d", F, kMaxF);
+    }
+  }
+#undef GNN_HALO
+  GNN_CHECK_LAUNCH();
+  return GNN_OK;
+}
+
+gnn_status launch_spmm_bwd(const gnn_csr& csr, const gnn_boundary* bnd, const float* Gm,
+                           int64_t ldg, int F, uint32_t seed, uint8_t* packed_ws,
+                           float2* meta_ws, float* dH, int64_t ldh, float* partial,
+                           cudaStream_t st) {
+  if (csr.n == 0) return GNN_OK;
+  if (!bnd)
+    return dispatch_rows<kPlain>(csr, csr.col, Gm, ldg, F, SlotMsgs{}, nullptr, nullptr, partial,
+                                 dH, ldh, nullptr, 0, st);
+  gnn_status s = launch_halo_quant_pack(*bnd, Gm, ldg, F, seed, packed_ws, meta_ws, st);
+  if (s != GNN_OK) return s;
+  SlotMsgs msg{packed_ws, meta_ws, bnd->slot_off, bnd->slot_bits};
+  return dispatch_rows<kBwdOwned>(csr, bnd->col_remap, Gm, ldg, F, msg, bnd->own_ptr,
+                                  bnd->own_slot, partial, dH, ldh, nullptr, 0, st);
+}
+
+size_t spmm_workspace_bytes(const gnn_csr& csr, int F) {
+  if (csr.split_len <= 0) return 0;
+  return (size_t)csr.n_pieces * (size_t)((F + 3) / 4) * 16u;
+}
+
+}  // namespace gnn
+
+using namespace gnn;
+
+static gnn_status check_csr(const gnn_csr* csr, const char* who) {
+  if (!csr) return fail(GNN_ERR_INVALID_ARG, "%s: csr is NULL", who);
+  if (csr->n < 0 || csr->nnz < 0) return fail(GNN_ERR_INVALID_ARG, "%s: negative csr size", who);
+  if (csr->n > 0 && (!csr->rowptr || (csr->nnz > 0 && (!csr->col || !csr->val))))
+    return fail(GNN_ERR_INVALID_ARG, "%s: csr arrays are NULL", who);
+  if (csr->split_len < 0 || (csr->split_len > 0 && csr->split_len < 32))
+    return fail(GNN_ERR_INVALID_ARG, "%s: split_len must be 0 or >= 32", who);
+  if (csr->split_len > 0 &&
+      (csr->n_long < 0 || csr->n_pieces < 0 || !csr->piece_ptr ||
+       (csr->n_long > 0 && !csr->long_rows) ||
+       (csr->n_pieces > 0 && (!csr->piece_row || !csr->piece_beg))))
+    return fail(GNN_ERR_INVALID_ARG, "%s: incomplete split plan", who);
+  return GNN_OK;
+}
+
+static gnn_status check_ws(const gnn_csr* csr, int F, void* ws, size_t ws_bytes, const char* who) {
+  const size_t need = spmm_workspace_bytes(*csr, F);
+  if (need == 0) return GNN_OK;
+  if (!ws || ws_bytes < need || ((uintptr_t)ws & 15) != 0)
+    return fail(GNN_ERR_INVALID_ARG, "%s: workspace needs %zu bytes, 16-byte aligned (got %zu)",
+                who, need, ws_bytes);
+  return GNN_OK;
+}
+
+static gnn_status check_bnd(const gnn_csr* csr, const gnn_boundary* b, int F, bool bwd,
+                            const char* who) {
+  if (!b) return GNN_OK;
+  if (b->n != csr->n || b->P < 1) return fail(GNN_ERR_INVALID_ARG, "%s: boundary does not match csr", who);
+  if (b->F != F)
+    return fail(GNN_ERR_INVALID_ARG, "%s: boundary offsets are for F=%d, call has F=%d", who, b->F, F);
+  if (!b->col_remap || (b->n_slots > 0 && (!b->slot_off || !b->slot_bits)))
+    return fail(GNN_ERR_INVALID_ARG, "%s: boundary arrays are NULL", who);
+  if (bwd && (!b->own_ptr || (b->n_slots > 0 && (!b->slot_rowptr || !b->own_slot)) ||
+              (b->nnz_cut > 0 && (!b->slot_col || !b->slot_val))))
+    return fail(GNN_ERR_INVALID_ARG, "%s: boundary backward arrays are NULL", who);
+  return GNN_OK;
+}
+
+extern "C" gnn_status gnn_spmm_workspace(const gnn_csr* csr, int32_t F, size_t* ws_bytes) {
+  gnn_status st = check_csr(csr, "gnn_spmm_workspace");
+  if (st != GNN_OK) return st;
+  GNN_REQUIRE(F >= 1 && ws_bytes, "gnn_spmm_workspace: bad arguments");
+  *ws_bytes = spmm_workspace_bytes(*csr, F);
+  return GNN_OK;
+}
+
+extern "C" gnn_status gnn_spmm_fwd(const gnn_csr* csr, const gnn_boundary* bnd, const float* H,
+                                   int64_t ldh, int32_t F, const uint8_t* packed,
+                                   const float* meta, float* M, int64_t ldm, uint16_t* Mb,
+                                   int64_t ldmb, void* ws, size_t ws_bytes, gnn_stream_t stream) {
+  gnn_status st = check_csr(csr, "gnn_spmm_fwd");
+  if (st != GNN_OK) return st;
+  GNN_REQUIRE(F >= 1, "gnn_spmm_fwd: F must be >= 1");
+  if (F > kMaxF) return fail(GNN_ERR_UNSUPPORTED, "gnn_spmm_fwd: F=%d > %d", F, kMaxF);
+  if ((st = check_bnd(csr, bnd, F, false, "gnn_spmm_fwd")) != GNN_OK) return st;
+  if ((st = check_ws(csr, F, ws, ws_bytes, "gnn_spmm_fwd")) != GNN_OK) return st;
+  if (csr->n == 0) return GNN_OK;
+  GNN_REQUIRE(H && (M || Mb), "gnn_spmm_fwd: H is NULL or no output given");
+  GNN_REQUIRE(ldh >= F && ldh % 4 == 0 && ((uintptr_t)H & 15) == 0,
+              "gnn_spmm_fwd: ldh must be >= F, a multiple of 4, H 16-byte aligned");
+  GNN_REQUIRE(!M || (ldm >= F && ldm % 4 == 0 && ((uintptr_t)M & 15) == 0),
+              "gnn_spmm_fwd: ldm must be >= F, a multiple of 4, M 16-byte aligned");
+  GNN_REQUIRE(!Mb || (ldmb >= (F + 15) / 16 * 16 && ldmb % 8 == 0 && ((uintptr_t)Mb & 15) == 0),
+              "gnn_spmm_fwd: ldmb must be >= round_up(F,16), a multiple of 8, Mb 16-byte aligned");
+  GNN_REQUIRE(!bnd || bnd->n_slots == 0 || (packed && meta),
+              "gnn_spmm_fwd: packed/meta required with a boundary");
+  return launch_spmm_fwd(*csr, bnd, H, ldh, F, packed, reinterpret_cast<const float2*>(meta), M,
+                         ldm, Mb, ldmb, static_cast<float*>(ws), as_stream(stream));
+}
+
+extern "C" gnn_status gnn_spmm_bwd(const gnn_csr* csr, const gnn_boundary* bnd, const float* G,
+                                   int64_t ldg, int32_t F, uint32_t seed, uint8_t* packed_ws,
+                                   float* meta_ws, float* dH, int64_t ldh, void* ws,
+                                   size_t ws_bytes, gnn_stream_t stream) {
+  gnn_status st = check_csr(csr, "gnn_spmm_bwd");
+  if (st != GNN_OK) return st;
+  GNN_REQUIRE(F >= 1, "gnn_spmm_bwd: F must be >= 1");
+  if (F > kMaxF) return fail(GNN_ERR_UNSUPPORTED, "gnn_spmm_bwd: F=%d > %d", F, kMaxF);
+  if (!csr->symmetric)
+    return fail(GNN_ERR_UNSUPPORTED, "gnn_spmm_bwd: needs a symmetric CSR (A^T = A)");
+  if ((st = check_bnd(csr, bnd, F, true, "gnn_spmm_bwd")) != GNN_OK) return st;
+  if ((st = check_ws(csr, F, ws, ws_bytes, "gnn_spmm_bwd")) != GNN_OK) return st;
+  if (csr->n == 0) return GNN_OK;
+  GNN_REQUIRE(G && dH, "gnn_spmm_bwd: NULL G or dH");
+  GNN_REQUIRE(ldg >= F && ldg % 4 == 0 && ((uintptr_t)G & 15) == 0,
+              "gnn_spmm_bwd: ldg must be >= F, a multiple of 4, G 16-byte aligned");
+  GNN_REQUIRE(ldh >= F && ldh % 4 == 0 && ((uintptr_t)dH & 15) == 0,
+              "gnn_spmm_bwd: ldh must be >= F, a multiple of 4, dH 16-byte aligned");
+  GNN_REQUIRE(!bnd || bnd->n_slots == 0 ||
+                  (packed_ws && meta_ws && ((uintptr_t)packed_ws & 15) == 0 && ((uintptr_t)meta_ws & 7) == 0),
+              "gnn_spmm_bwd: packed_ws (16-byte aligned) and meta_ws required with a boundary");
+  return launch_spmm_bwd(*csr, bnd, G, ldg, F, seed, packed_ws,
+                         reinterpret_cast<float2*>(meta_ws), dH, ldh, static_cast<float*>(ws),
+                         as_stream(stream));
+}
