@@ -251,6 +251,57 @@ gnn_status gnn_spmm_bwd(const gnn_csr* csr, const gnn_boundary* bnd,
                         int64_t ldh, void* ws, size_t ws_bytes,
                         gnn_stream_t stream);
 
+/* ------------------------------------------------------------------------ */
+/* Dense transform (tcgen05 tensor cores) and whole layers.                   */
+/* ------------------------------------------------------------------------ */
+/* bf16 operands are raw bf16 bit patterns (uint16).  W is [F_in][F_out]
+ * row-major.  F_out must be a multiple of 16, at most 256.  Products
+ * accumulate in fp32. */
+
+/* Workspace bytes for gnn_dense_fwd / gnn_dense_bwd with n rows. */
+gnn_status gnn_dense_workspace(int64_t n, int32_t F_in, int32_t F_out, size_t* ws_bytes);
+
+/* The transform of the GCN layer, SYLVIE guide section 2 (z = W h after
+ * aggregation, h' = sigma(z)): H_out = act(Mb W), Mb [n][ldmb] bf16 with
+ * columns F_in..round_up(F_in,16)-1 zero, act = ReLU if relu else identity.
+ * H_out is fp32 [n][ldo], ldo >= F_out. */
+gnn_status gnn_dense_fwd(const uint16_t* Mb, int64_t ldmb, int64_t n, int32_t F_in,
+                         const uint16_t* W, int32_t F_out, int32_t relu, float* H_out,
+                         int64_t ldo, void* ws, size_t ws_bytes, gnn_stream_t stream);
+
+/* Backward of the transform: dZ = dH_out * 1[H_out > 0] (relu) or dH_out,
+ * rounded to bf16; dM = dZ W^T (fp32 [n][ldm], may be NULL) and the weight
+ * gradient of section 7, dW = Mb^T dZ (fp32 [F_in][F_out]), accumulated over
+ * row blocks and added in a fixed order (deterministic). */
+gnn_status gnn_dense_bwd(const uint16_t* Mb, int64_t ldmb, int64_t n, int32_t F_in,
+                         const uint16_t* W, int32_t F_out, const float* dH_out, int64_t ldg,
+                         const float* H_out, int64_t ldo, int32_t relu, float* dM, int64_t ldm,
+                         float* dW, void* ws, size_t ws_bytes, gnn_stream_t stream);
+
+/* Workspace bytes for gnn_layer_fwd / gnn_layer_bwd on this CSR. */
+gnn_status gnn_layer_workspace(const gnn_csr* csr, int32_t F_in, int32_t F_out, size_t* ws_bytes);
+
+/* One forward GCN layer as in the SYLVIE guide, section 11: quantise and pack
+ * the boundary rows of H_in (gnn_quant_pack with bnd's slots, widths and
+ * offsets, which must be for F_in), aggregate with dequantised remote rows
+ * (gnn_spmm_fwd) into Mb (bf16, kept for the backward), then
+ * H_out = act(Mb W).  bnd NULL: plain A H. */
+gnn_status gnn_layer_fwd(const gnn_csr* csr, const gnn_boundary* bnd, const float* H_in,
+                         int64_t ldh, int32_t F_in, const uint16_t* W, int32_t F_out,
+                         int32_t relu, uint32_t seed, uint8_t* packed_ws, float* meta_ws,
+                         uint16_t* Mb, int64_t ldmb, float* H_out, int64_t ldo, void* ws,
+                         size_t ws_bytes, gnn_stream_t stream);
+
+/* One backward GCN layer: gnn_dense_bwd (dW and dM), then, unless dH_in is
+ * NULL (the first layer), the boundary-quantised gnn_spmm_bwd of dM with
+ * `seed` into dH_in [n][ldh]. */
+gnn_status gnn_layer_bwd(const gnn_csr* csr, const gnn_boundary* bnd, const float* dH_out,
+                         int64_t ldg, const float* H_out, int64_t ldo, int32_t relu,
+                         const uint16_t* Mb, int64_t ldmb, const uint16_t* W, int32_t F_in,
+                         int32_t F_out, uint32_t seed, uint8_t* packed_ws, float* meta_ws,
+                         float* dW, float* dH_in, int64_t ldh, void* ws, size_t ws_bytes,
+                         gnn_stream_t stream);
+
 /* Synchronise `stream` and report device-side failures (GNN_ERR_CUDA for a
  * CUDA error, GNN_ERR_DEVICE_CHECK / GNN_ERR_TIMEOUT for flags the kernels
  * raised).  Clears the flags. */

@@ -17,7 +17,8 @@ __all__ = [
     "Csr", "Boundary", "BitRule", "GnnError", "load", "build",
     "gnn_csr_build", "gnn_csr_split", "gnn_spmm_workspace", "spmm_ws", "gnn_boundary_index", "gnn_boundary_set_bits", "gnn_slot_offsets",
     "gnn_quant_pack", "gnn_dequant_unpack", "gnn_spmm_fwd", "gnn_spmm_bwd", "gnn_sync_check",
-    "rowbytes", "ld_for", "ldb_for",
+    "rowbytes", "ld_for", "ldb_for", "gnn_dense_workspace", "gnn_dense_fwd", "gnn_dense_bwd",
+    "gnn_layer_workspace", "gnn_layer_fwd", "gnn_layer_bwd",
 ]
 
 
@@ -284,3 +285,63 @@ def gnn_spmm_bwd(csr: Csr, bnd: Optional[Boundary], G, F: int, seed: int, packed
 
 def gnn_sync_check(stream=None) -> None:
     call("gnn_sync_check", _stream(stream))
+
+
+# ---------------------------------------------------------------- dense transform and layers
+def gnn_dense_workspace(n: int, F_in: int, F_out: int) -> int:
+    nb = ctypes.c_size_t()
+    call("gnn_dense_workspace", n, F_in, F_out, ctypes.byref(nb))
+    return nb.value
+
+
+def gnn_dense_fwd(Mb, n: int, F_in: int, W, F_out: int, relu: bool, H_out, ws=None,
+                  stream=None) -> None:
+    """H_out = act(Mb W) on tcgen05 (Mb, W bf16 tensors; H_out fp32)."""
+    if ws is None:
+        ws = _workspace(gnn_dense_workspace(n, F_in, F_out), Mb.device)
+    call("gnn_dense_fwd", _ptr(Mb), Mb.stride(0), n, F_in, _ptr(W), F_out, int(relu), _ptr(H_out),
+         H_out.stride(0), _ptr(ws), ws.numel(), _stream(stream))
+
+
+def gnn_dense_bwd(Mb, n: int, F_in: int, W, F_out: int, dH_out, H_out, relu: bool, dM, dW,
+                  ws=None, stream=None) -> None:
+    if ws is None:
+        ws = _workspace(gnn_dense_workspace(n, F_in, F_out), Mb.device)
+    call("gnn_dense_bwd", _ptr(Mb), Mb.stride(0), n, F_in, _ptr(W), F_out, _ptr(dH_out),
+         dH_out.stride(0), _ptr(H_out), H_out.stride(0) if H_out is not None else 0, int(relu),
+         _ptr(dM), dM.stride(0) if dM is not None else 0, _ptr(dW), _ptr(ws), ws.numel(),
+         _stream(stream))
+
+
+def gnn_layer_workspace(csr: Csr, F_in: int, F_out: int) -> int:
+    nb = ctypes.c_size_t()
+    c = csr.c()
+    call("gnn_layer_workspace", ctypes.byref(c), F_in, F_out, ctypes.byref(nb))
+    return nb.value
+
+
+def gnn_layer_fwd(csr: Csr, bnd: Optional[Boundary], H_in, F_in: int, W, F_out: int, relu: bool,
+                  seed: int, packed_ws, meta_ws, Mb, H_out, slot_off=None, ws=None,
+                  stream=None) -> None:
+    c = csr.c()
+    cb = bnd.c(slot_off, F_in if slot_off is not None else None) if bnd is not None else None
+    if ws is None:
+        ws = _workspace(gnn_layer_workspace(csr, F_in, F_out), H_in.device)
+    call("gnn_layer_fwd", ctypes.byref(c), ctypes.byref(cb) if cb is not None else None, _ptr(H_in),
+         H_in.stride(0), F_in, _ptr(W), F_out, int(relu), seed & 0xFFFFFFFF, _ptr(packed_ws),
+         _ptr(meta_ws), _ptr(Mb), Mb.stride(0), _ptr(H_out), H_out.stride(0), _ptr(ws), ws.numel(),
+         _stream(stream))
+
+
+def gnn_layer_bwd(csr: Csr, bnd: Optional[Boundary], dH_out, H_out, relu: bool, Mb, W, F_in: int,
+                  F_out: int, seed: int, packed_ws, meta_ws, dW, dH_in=None, slot_off=None,
+                  ws=None, stream=None) -> None:
+    c = csr.c()
+    cb = bnd.c(slot_off, F_in if slot_off is not None else None) if bnd is not None else None
+    if ws is None:
+        ws = _workspace(gnn_layer_workspace(csr, F_in, F_out), dH_out.device)
+    call("gnn_layer_bwd", ctypes.byref(c), ctypes.byref(cb) if cb is not None else None,
+         _ptr(dH_out), dH_out.stride(0), _ptr(H_out), H_out.stride(0) if H_out is not None else 0,
+         int(relu), _ptr(Mb), Mb.stride(0), _ptr(W), F_in, F_out, seed & 0xFFFFFFFF, _ptr(packed_ws),
+         _ptr(meta_ws), _ptr(dW), _ptr(dH_in), dH_in.stride(0) if dH_in is not None else 0,
+         _ptr(ws), ws.numel(), _stream(stream))

@@ -64,6 +64,17 @@ PROTOTYPES = {
                                     c_vp, c_size, c_vp]),
     "gnn_spmm_bwd": (ctypes.c_int, [P_csr, P_bnd, c_vp, c_i64, c_i32, c_u32, c_vp, c_vp, c_vp, c_i64,
                                     c_vp, c_size, c_vp]),
+    "gnn_dense_workspace": (ctypes.c_int, [c_i64, c_i32, c_i32, P_size]),
+    "gnn_dense_fwd": (ctypes.c_int, [c_vp, c_i64, c_i64, c_i32, c_vp, c_i32, c_i32, c_vp, c_i64, c_vp,
+                                     c_size, c_vp]),
+    "gnn_dense_bwd": (ctypes.c_int, [c_vp, c_i64, c_i64, c_i32, c_vp, c_i32, c_vp, c_i64, c_vp, c_i64,
+                                     c_i32, c_vp, c_i64, c_vp, c_vp, c_size, c_vp]),
+    "gnn_layer_workspace": (ctypes.c_int, [P_csr, c_i32, c_i32, P_size]),
+    "gnn_layer_fwd": (ctypes.c_int, [P_csr, P_bnd, c_vp, c_i64, c_i32, c_vp, c_i32, c_i32, c_u32, c_vp,
+                                     c_vp, c_vp, c_i64, c_vp, c_i64, c_vp, c_size, c_vp]),
+    "gnn_layer_bwd": (ctypes.c_int, [P_csr, P_bnd, c_vp, c_i64, c_vp, c_i64, c_i32, c_vp, c_i64, c_vp,
+                                     c_i32, c_i32, c_u32, c_vp, c_vp, c_vp, c_vp, c_i64, c_vp, c_size,
+                                     c_vp]),
     "gnn_sync_check": (ctypes.c_int, [c_vp]),
 }
 

@@ -1,0 +1,217 @@
+// Dense transform and whole-layer entry points: one GCN layer of the SYLVIE
+// guide's section 11 data path on one stream -- quantise the boundary rows,
+// aggregate with dequantised remote rows, transform with W (tcgen05) and
+// activate; the backward mirrors it with the embedding gradients.
+#include <cuda_runtime.h>
+
+#include "gemm.h"
+#include "internal.h"
+#include "kernels.h"
+
+namespace gnn {
+
+static int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+struct DenseWs {
+  uint16_t* wt;    // W^T [F_out x ldb] (forward)
+  uint16_t* dz;    // dZ bf16 [n x ldz] (backward)
+  float* part;     // split-k partials of dW
+  size_t bytes;
+};
+
+static DenseWs dense_ws_layout(void* base, size_t cap, int64_t n, int F_in, int F_out,
+                               bool* ok) {
+  Arena ar(base, cap);
+  DenseWs w{};
+  const int64_t ldb = round_up(F_in, 16), ldz = round_up(F_out, 64);
+  w.wt = ar.take<uint16_t>((size_t)F_out * ldb);
+  w.dz = ar.take<uint16_t>((size_t)n * ldz);
+  w.part = reinterpret_cast<float*>(ar.take_bytes(gemm_mn_workspace_bytes(F_in, F_out, (int)n)));
+  w.bytes = ar.used;
+  *ok = ar.ok();
+  return w;
+}
+
+static gnn_status check_dims(int64_t n, int F_in, int F_out, const char* who) {
+  if (n < 0 || n > (int64_t)0x7fffffff) return fail(GNN_ERR_INVALID_ARG, "%s: bad row count", who);
+  if (F_in < 1 || F_out < 1) return fail(GNN_ERR_INVALID_ARG, "%s: F_in/F_out must be >= 1", who);
+  if (F_in > kMaxF) return fail(GNN_ERR_UNSUPPORTED, "%s: F_in=%d > %d", who, F_in, kMaxF);
+  if (F_out % 16 != 0 || F_out > 256)
+    return fail(GNN_ERR_UNSUPPORTED, "%s: F_out must be a multiple of 16 and <= 256", who);
+  return GNN_OK;
+}
+
+static gnn_status dense_fwd_impl(const uint16_t* Mb, int64_t ldmb, int64_t n, int F_in,
+                                 const uint16_t* W, int F_out, int relu, float* H_out,
+                                 int64_t ldo, const DenseWs& w, cudaStream_t st) {
+  const int64_t K = round_up(F_in, 16);
+  gnn_status s = launch_transpose_w(W, F_in, F_out, (int)K, w.wt, st);
+  if (s != GNN_OK) return s;
+  return launch_gemm_tn(Mb, ldmb, w.wt, K, (int)n, F_out, (int)K, H_out, ldo, F_out, relu, st);
+}
+
+static gnn_status dense_bwd_impl(const uint16_t* Mb, int64_t ldmb, int64_t n, int F_in,
+                                 const uint16_t* W, int F_out, const float* dH_out, int64_t ldg,
+                                 const float* H_out, int64_t ldo, int relu, float* dM,
+                                 int64_t ldm, float* dW, const DenseWs& w, cudaStream_t st) {
+  const int64_t ldz = round_up(F_out, 64);
+  gnn_status s = launch_relu_mask_bf16(n, F_out, dH_out, ldg, H_out, ldo, relu, w.dz, ldz, st);
+  if (s != GNN_OK) return s;
+  if (dM) {
+    // dM = dZ W^T: A = dZ [n x F_out], B = W [F_in x F_out], both K-major
+    s = launch_gemm_tn(w.dz, ldz, W, F_out, (int)n, F_in, F_out, dM, ldm, (int)round_up(F_in, 4),
+                       0, st);
+    if (s != GNN_OK) return s;
+  }
+  if (dW) {
+    // dW = Mb^T dZ: reduction over the n rows of both (MN-major operands)
+    s = launch_gemm_mn(Mb, ldmb, w.dz, ldz, F_in, F_out, (int)n, dW, F_out, w.part, st);
+    if (s != GNN_OK) return s;
+  }
+  return GNN_OK;
+}
+
+}  // namespace gnn
+
+using namespace gnn;
+
+extern "C" gnn_status gnn_dense_workspace(int64_t n, int32_t F_in, int32_t F_out, size_t* ws_bytes) {
+  gnn_status s = check_dims(n, F_in, F_out, "gnn_dense_workspace");
+  if (s != GNN_OK) return s;
+  GNN_REQUIRE(ws_bytes, "gnn_dense_workspace: NULL ws_bytes");
+  bool ok;
+  *ws_bytes = dense_ws_layout(nullptr, 0, n, F_in, F_out, &ok).bytes;
+  return GNN_OK;
+}
+
+static gnn_status check_mb(const uint16_t* Mb, int64_t ldmb, int F_in, const char* who) {
+  if (!Mb || ldmb < (F_in + 15) / 16 * 16 || ldmb % 8 || ((uintptr_t)Mb & 15))
+    return fail(GNN_ERR_INVALID_ARG, "%s: Mb needs ldmb >= round_up(F_in,16), a multiple of 8, "
+                "16-byte alignment", who);
+  return GNN_OK;
+}
+
+extern "C" gnn_status gnn_dense_fwd(const uint16_t* Mb, int64_t ldmb, int64_t n, int32_t F_in,
+                                    const uint16_t* W, int32_t F_out, int32_t relu, float* H_out,
+                                    int64_t ldo, void* ws, size_t ws_bytes, gnn_stream_t stream) {
+  gnn_status s = check_dims(n, F_in, F_out, "gnn_dense_fwd");
+  if (s != GNN_OK) return s;
+  if (n == 0) return GNN_OK;
+  if ((s = check_mb(Mb, ldmb, F_in, "gnn_dense_fwd")) != GNN_OK) return s;
+  GNN_REQUIRE(W && H_out && ldo >= F_out && ldo % 4 == 0 && ((uintptr_t)H_out & 15) == 0,
+              "gnn_dense_fwd: bad W or H_out");
+  bool ok;
+  DenseWs w = dense_ws_layout(ws, ws_bytes, n, F_in, F_out, &ok);
+  GNN_REQUIRE(ws && ok, "gnn_dense_fwd: workspace too small (%zu < %zu)", ws_bytes, w.bytes);
+  return dense_fwd_impl(Mb, ldmb, n, F_in, W, F_out, relu, H_out, ldo, w, as_stream(stream));
+}
+
+extern "C" gnn_status gnn_dense_bwd(const uint16_t* Mb, int64_t ldmb, int64_t n, int32_t F_in,
+                                    const uint16_t* W, int32_t F_out, const float* dH_out,
+                                    int64_t ldg, const float* H_out, int64_t ldo, int32_t relu,
+                                    float* dM, int64_t ldm, float* dW, void* ws, size_t ws_bytes,
+                                    gnn_stream_t stream) {
+  gnn_status s = check_dims(n, F_in, F_out, "gnn_dense_bwd");
+  if (s != GNN_OK) return s;
+  if ((s = check_mb(Mb, ldmb, F_in, "gnn_dense_bwd")) != GNN_OK) return s;
+  GNN_REQUIRE(W && dH_out && ldg >= F_out && ldg % 4 == 0 && ((uintptr_t)dH_out & 15) == 0,
+              "gnn_dense_bwd: bad W or dH_out");
+  GNN_REQUIRE(!relu || (H_out && ldo >= F_out && ldo % 4 == 0 && ((uintptr_t)H_out & 15) == 0),
+              "gnn_dense_bwd: relu needs H_out");
+  GNN_REQUIRE(!dM || (ldm >= (F_in + 3) / 4 * 4 && ldm % 4 == 0 && ((uintptr_t)dM & 15) == 0),
+              "gnn_dense_bwd: dM needs ldm >= round_up(F_in,4), a multiple of 4");
+  bool ok;
+  DenseWs w = dense_ws_layout(ws, ws_bytes, n, F_in, F_out, &ok);
+  GNN_REQUIRE(ws && ok, "gnn_dense_bwd: workspace too small (%zu < %zu)", ws_bytes, w.bytes);
+  return dense_bwd_impl(Mb, ldmb, n, F_in, W, F_out, dH_out, ldg, H_out, ldo, relu, dM, ldm, dW,
+                        w, as_stream(stream));
+}
+
+// ------------------------------------------------------------------ layers
+struct LayerWs {
+  DenseWs dense;
+  float* dM;
+  float* spmm;
+  size_t bytes;
+};
+
+static LayerWs layer_ws_layout(void* base, size_t cap, const gnn_csr& csr, int F_in, int F_out,
+                               bool* ok) {
+  LayerWs w{};
+  bool ok1;
+  DenseWs probe = dense_ws_layout(nullptr, 0, csr.n, F_in, F_out, &ok1);
+  Arena ar(base, cap);
+  void* dbase = ar.take_bytes(probe.bytes);
+  w.dense = dense_ws_layout(dbase, probe.bytes, csr.n, F_in, F_out, &ok1);
+  w.dM = ar.take<float>((size_t)csr.n * (size_t)round_up(F_in, 4));
+  const size_t sp = spmm_workspace_bytes(csr, F_in);
+  w.spmm = sp ? reinterpret_cast<float*>(ar.take_bytes(sp)) : nullptr;
+  w.bytes = ar.used;
+  *ok = ar.ok();
+  return w;
+}
+
+extern "C" gnn_status gnn_layer_workspace(const gnn_csr* csr, int32_t F_in, int32_t F_out,
+                                          size_t* ws_bytes) {
+  GNN_REQUIRE(csr && ws_bytes, "gnn_layer_workspace: NULL argument");
+  gnn_status s = check_dims(csr->n, F_in, F_out, "gnn_layer_workspace");
+  if (s != GNN_OK) return s;
+  bool ok;
+  *ws_bytes = layer_ws_layout(nullptr, 0, *csr, F_in, F_out, &ok).bytes;
+  return GNN_OK;
+}
+
+extern "C" gnn_status gnn_layer_fwd(const gnn_csr* csr, const gnn_boundary* bnd, const float* H_in,
+                                    int64_t ldh, int32_t F_in, const uint16_t* W, int32_t F_out,
+                                    int32_t relu, uint32_t seed, uint8_t* packed_ws,
+                                    float* meta_ws, uint16_t* Mb, int64_t ldmb, float* H_out,
+                                    int64_t ldo, void* ws, size_t ws_bytes, gnn_stream_t stream) {
+  GNN_REQUIRE(csr, "gnn_layer_fwd: csr is NULL");
+  gnn_status s = check_dims(csr->n, F_in, F_out, "gnn_layer_fwd");
+  if (s != GNN_OK) return s;
+  if (csr->n == 0) return GNN_OK;
+  if ((s = check_mb(Mb, ldmb, F_in, "gnn_layer_fwd")) != GNN_OK) return s;
+  GNN_REQUIRE(W && H_out && ldo >= F_out && ldo % 4 == 0 && ((uintptr_t)H_out & 15) == 0,
+              "gnn_layer_fwd: bad W or H_out");
+  bool ok;
+  LayerWs w = layer_ws_layout(ws, ws_bytes, *csr, F_in, F_out, &ok);
+  GNN_REQUIRE(ws && ok, "gnn_layer_fwd: workspace too small (%zu < %zu)", ws_bytes, w.bytes);
+  cudaStream_t st = as_stream(stream);
+  if (bnd && bnd->n_slots > 0) {
+    GNN_REQUIRE(bnd->slot_node && bnd->slot_bits && bnd->slot_off && bnd->F == F_in,
+                "gnn_layer_fwd: boundary offsets must be for F_in");
+    GNN_REQUIRE(packed_ws && meta_ws && ((uintptr_t)packed_ws & 15) == 0 && ((uintptr_t)meta_ws & 7) == 0,
+                "gnn_layer_fwd: packed_ws/meta_ws required with a boundary");
+    GNN_REQUIRE(ldh >= F_in && ldh % 4 == 0 && ((uintptr_t)H_in & 15) == 0, "gnn_layer_fwd: bad H_in");
+    s = launch_quant_pack(H_in, ldh, F_in, bnd->slot_node, bnd->n_slots, bnd->slot_bits,
+                          bnd->slot_off, seed, packed_ws, reinterpret_cast<float2*>(meta_ws), st);
+    if (s != GNN_OK) return s;
+  }
+  s = gnn_spmm_fwd(csr, bnd, H_in, ldh, F_in, packed_ws, meta_ws, nullptr, 0, Mb, ldmb, w.spmm,
+                   spmm_workspace_bytes(*csr, F_in), stream);
+  if (s != GNN_OK) return s;
+  return dense_fwd_impl(Mb, ldmb, csr->n, F_in, W, F_out, relu, H_out, ldo, w.dense, st);
+}
+
+extern "C" gnn_status gnn_layer_bwd(const gnn_csr* csr, const gnn_boundary* bnd,
+                                    const float* dH_out, int64_t ldg, const float* H_out,
+                                    int64_t ldo, int32_t relu, const uint16_t* Mb, int64_t ldmb,
+                                    const uint16_t* W, int32_t F_in, int32_t F_out, uint32_t seed,
+                                    uint8_t* packed_ws, float* meta_ws, float* dW, float* dH_in,
+                                    int64_t ldh, void* ws, size_t ws_bytes, gnn_stream_t stream) {
+  GNN_REQUIRE(csr, "gnn_layer_bwd: csr is NULL");
+  gnn_status s = check_dims(csr->n, F_in, F_out, "gnn_layer_bwd");
+  if (s != GNN_OK) return s;
+  if (csr->n == 0) return GNN_OK;
+  bool ok;
+  LayerWs w = layer_ws_layout(ws, ws_bytes, *csr, F_in, F_out, &ok);
+  GNN_REQUIRE(ws && ok, "gnn_layer_bwd: workspace too small (%zu < %zu)", ws_bytes, w.bytes);
+  GNN_REQUIRE(dW, "gnn_layer_bwd: dW is NULL");
+  const int64_t ldm = round_up(F_in, 4);
+  s = gnn_dense_bwd(Mb, ldmb, csr->n, F_in, W, F_out, dH_out, ldg, H_out, ldo, relu,
+                    dH_in ? w.dM : nullptr, ldm, dW, w.dense.wt, w.dense.bytes, stream);
+  if (s != GNN_OK) return s;
+  if (!dH_in) return GNN_OK;
+  return gnn_spmm_bwd(csr, bnd, w.dM, ldm, F_in, seed, packed_ws, meta_ws, dH_in, ldh, w.spmm,
+                      spmm_workspace_bytes(*csr, F_in), stream);
+}
