@@ -1,0 +1,524 @@
+"""Throughput of the boundary-quantised GCN aggregation hot path on GB300.
+
+One step = one full forward + backward pass of a GCN over a synthetic graph
+with P virtual partitions (contiguous node blocks): per layer, quantise and
+pack the boundary rows, aggregate with dequantised remote rows (bf16 output),
+transform on tcgen05 with ReLU; backward, mask and transform, weight gradient,
+halo partials quantised and packed, local transpose aggregation plus owner
+dequant-add (skipped for the first layer).
+
+Metric: algorithmic bytes of every kernel of the step (the per-call byte
+counts documented in the design notes) divided by the step time, in GB/s;
+the JSON line also carries per-kernel GB/s, GFLOP/s and TFLOP/s.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload yelp]
+  python bench.py --impl reference ...   (the oracle on host cores)
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "SpMM fwd+bwd GB/s & GFLOP/s, quant-pack GB/s; % of GB300 HBM roofline"
+UNIT = "GB/s"
+
+WORKLOAD_TEXT = {
+    "tiny": "4,096-node planted partition (4 communities, avg degree 8), F=16, 2-layer GCN hidden 16, P=4, top-10% 8 bits else 2",
+    "yelp": "Yelp-shaped DC-SBM: 716,847 nodes, 6.975M undirected edges (14.67M CSR entries), power-law degrees over 64 communities, F=300, 3-layer GCN hidden 256, P=8, top-20% 8 bits else 4",
+    "reddit": "Reddit-shaped DC-SBM: 232,965 nodes, 57.3M undirected edges, heavy tail capped at 20k, 50 communities, F=602, 2-layer GCN hidden 128, P=8, top-10% 8 bits else 2",
+    "products": "ogbn-products-shaped DC-SBM: 2,449,029 nodes, 30,929,570 undirected edges, 128 communities, F=100, 4-layer GCN hidden 256, P=8, width quartiles {1,2,4,8}",
+    "scale": "R-MAT scale 24 (16.8M nodes, 128M edge draws), BFS-ordered into 16 blocks, F=256, 3-layer GCN hidden 256, P=16, top-5% 8 bits else base 1",
+}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def rowbytes(b, F):
+    b = np.asarray(b, np.int64)
+    return np.where(b == 32, 16 * ((4 * F + 15) // 16), 16 * ((F * b + 127) // 128))
+
+
+# --------------------------------------------------------------- byte models
+def kernel_bytes(n, nnz, nnz_cut, S, F, slot_bits, slot_cut, out_bytes_per_row):
+    """Algorithmic bytes of the aggregation calls and the quantiser at width F.
+    slot_cut[s] = cut entries of slot s (forward remote reads per slot)."""
+    rb = rowbytes(slot_bits, F)
+    Q = int(rb.sum())
+    remote = int((slot_cut * (rb + 8)).sum())
+    fwd = 8 * (n + 1) + 8 * nnz + (nnz - nnz_cut) * 4 * F + remote + out_bytes_per_row * n
+    qp = 4 * S + 4 * F * S + Q + 8 * S + 1 * S + 8 * S
+    bwd = (8 * (S + 1) + 8 * nnz_cut + nnz_cut * 4 * F + Q + 8 * S          # halo partials + pack
+           + 8 * (n + 1) + 8 * nnz + (nnz - nnz_cut) * 4 * F + Q + 8 * S + 4 * F * n)  # local + owned
+    return dict(fwd=fwd, quant=qp, bwd=bwd, Q=Q)
+
+
+def gemm_bytes(n, F_in, F_out):
+    ldb = (F_in + 15) // 16 * 16
+    ldz = (F_out + 63) // 64 * 64
+    fwd = 2 * n * ldb + 2 * F_in * F_out + 4 * n * F_out
+    mask = 4 * n * F_out * 2 + 2 * n * ldz
+    dM = 2 * n * ldz + 2 * F_in * F_out + 4 * n * ((F_in + 3) // 4 * 4)
+    dW = 2 * n * ldb + 2 * n * ldz + 4 * F_in * F_out
+    return dict(fwd=fwd, mask=mask, dM=dM, dW=dW)
+
+
+# --------------------------------------------------------------- clocks
+class ClockSampler:
+    def __init__(self, index=0):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.index), "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------- GPU arm
+def run_gpu(args, rank, world, local_rank):
+    import torch
+
+    import sparse_aggregation_message_gb300 as G
+    from synth import make_workload
+    from synth.graphs import make_weight_bf16
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    G.load()
+    wl = make_workload(args.workload)
+    n, P, dims, L = wl.n, wl.P, wl.dims, wl.layers
+    base = wl.base_bits[0]
+    csr = G.gnn_csr_build(n, torch.from_numpy(wl.src).to(dev), torch.from_numpy(wl.dst).to(dev))
+    csr = G.gnn_csr_split(csr, args.split_len)
+    rule = G.BitRule(wl.rule_pct, wl.rule_bits)
+    F0 = dims[0]
+    bnd = G.gnn_boundary_index(csr, P, rule, base, F0)
+    S = bnd.n_slots
+    widths = sorted(set(dims[:-1]))
+    offs = {F: (bnd.slot_off if F == F0 else G.gnn_slot_offsets(bnd.slot_bits, S, F)) for F in widths}
+    Qmax = max(int(offs[F][-1].item()) for F in widths)
+    packed = torch.zeros(max(Qmax, 16), dtype=torch.uint8, device=dev)
+    meta = torch.zeros((max(S, 1), 2), device=dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(wl.seed + 1 + rank)
+    ld = [G.ld_for(F) for F in dims]
+    ldb = [G.ldb_for(F) for F in dims]
+    H = [torch.zeros((n, ld[0]), device=dev)]
+    H[0][:, :F0] = torch.randn((n, F0), generator=g, device=dev)
+    for l in range(1, L + 1):
+        H.append(torch.empty((n, ld[l]), device=dev))
+    Mb = [torch.empty((n, ldb[l]), dtype=torch.bfloat16, device=dev) for l in range(L)]
+    W = [torch.from_numpy(make_weight_bf16(dims[l], dims[l + 1], wl.seed, l).view(np.int16)).to(dev)
+         for l in range(L)]
+    dW = [torch.empty((dims[l], dims[l + 1]), device=dev) for l in range(L)]
+    dH = [torch.empty((n, ld[l]), device=dev) for l in range(L + 1)]
+    dH[L].copy_(torch.randn((n, ld[L]), generator=g, device=dev))
+    # workspaces sized for the largest layer
+    ws_layer = max(G.gnn_layer_workspace(csr, dims[l], dims[l + 1]) for l in range(L))
+    ws = torch.empty(ws_layer, dtype=torch.uint8, device=dev)
+    dense_ws = max(G.gnn_dense_workspace(n, dims[l], dims[l + 1]) for l in range(L))
+    wsd = torch.empty(dense_ws, dtype=torch.uint8, device=dev)
+    spmm_ws = max(G.gnn_spmm_workspace(csr, F) for F in widths)
+    wss = torch.empty(max(spmm_ws, 16), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    # per-slot cut counts for the byte model
+    slot_cut = (bnd.slot_rowptr[1:] - bnd.slot_rowptr[:-1]).cpu().numpy()
+    slot_bits = bnd.slot_bits.cpu().numpy()
+
+    kinds = ["quant", "spmm_fwd", "gemm_fwd", "mask_dM_dW", "spmm_bwd"]
+    ev = {}
+
+    def rec(key):
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(stream)
+        ev.setdefault(key, []).append(e)
+
+    # backward aggregation inputs: one dM per row stride
+    dM_by_ld = {}
+    for l in range(1, L):
+        if ld[l] not in dM_by_ld:
+            dM_by_ld[ld[l]] = torch.empty((n, ld[l]), device=dev)
+
+    def run_step(timed):
+        for l in range(L):
+            F, Fo = dims[l], dims[l + 1]
+            so = offs[F]
+            if timed:
+                rec(("quant", l, 0))
+            G.gnn_quant_pack(H[l], F, bnd.slot_node, S, bnd.slot_bits, so, 2 * l, packed, meta)
+            if timed:
+                rec(("quant", l, 1))
+            G.gnn_spmm_fwd(csr, bnd, H[l], F, packed, meta, Mb=Mb[l], slot_off=so, ws=wss)
+            if timed:
+                rec(("spmm_fwd", l, 1))
+            G.gnn_dense_fwd(Mb[l], n, F, W[l], Fo, l < L - 1, H[l + 1], ws=wsd)
+            if timed:
+                rec(("gemm_fwd", l, 1))
+        for l in reversed(range(L)):
+            F, Fo = dims[l], dims[l + 1]
+            so = offs[F]
+            dMl = dM_by_ld.get(ld[l])
+            if timed:
+                rec(("mask_dM_dW", l, 0))
+            G.gnn_dense_bwd(Mb[l], n, F, W[l], Fo, dH[l + 1], H[l + 1], l < L - 1,
+                            dMl if l > 0 else None, dW[l], ws=wsd)
+            if timed:
+                rec(("mask_dM_dW", l, 1))
+            if l > 0:
+                G.gnn_spmm_bwd(csr, bnd, dMl, F, 2 * l + 1, packed, meta, dH[l], slot_off=so, ws=wss)
+                if timed:
+                    rec(("spmm_bwd", l, 1))
+
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        run_step(False)
+    G.gnn_sync_check()
+    torch.cuda.synchronize(dev)
+
+    launches0 = G.gnn_kernel_launches()
+    barrier()
+    torch.cuda.synchronize(dev)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clk:
+        time.sleep(1.5)  # nvidia-smi needs about a second before its first sample
+        for _ in range(2):
+            run_step(False)
+        torch.cuda.synchronize(dev)
+        t_start.record(stream)
+        for _ in range(args.steps):
+            run_step(True)
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier()
+    launches = G.gnn_kernel_launches() - launches0
+    G.gnn_sync_check()
+    ms = t_start.elapsed_time(t_end) / args.steps
+
+    # per-kernel times (ms per step)
+    per = {k: 0.0 for k in kinds}
+    per_layer = {}
+    for key, lst in ev.items():
+        kind, l, which = key
+        if which != 1:
+            continue
+        start_key = {"quant": ("quant", l, 0), "spmm_fwd": ("quant", l, 1), "gemm_fwd": ("spmm_fwd", l, 1),
+                     "mask_dM_dW": ("mask_dM_dW", l, 0), "spmm_bwd": ("mask_dM_dW", l, 1)}[kind]
+        starts = ev[start_key]
+        tot = sum(a.elapsed_time(b) for a, b in zip(starts, lst)) / args.steps
+        per[kind] += tot
+        per_layer[f"{kind}_l{l + 1}"] = tot
+
+    # algorithmic bytes per step
+    nnz, nc = csr.nnz, bnd.nnz_cut
+    byt = {k: 0 for k in kinds}
+    flops = {"spmm": 0.0, "gemm": 0.0}
+    spmm_fwd_bytes_l = {}
+    for l in range(L):
+        F, Fo = dims[l], dims[l + 1]
+        kb = kernel_bytes(n, nnz, nc, S, F, slot_bits, slot_cut, 2 * ldb[l])
+        gb = gemm_bytes(n, F, Fo)
+        byt["quant"] += kb["quant"]
+        byt["spmm_fwd"] += kb["fwd"]
+        spmm_fwd_bytes_l[l] = kb["fwd"]
+        byt["gemm_fwd"] += gb["fwd"]
+        byt["mask_dM_dW"] += gb["mask"] + gb["dW"] + (gb["dM"] if l > 0 else 0)
+        flops["spmm"] += 2.0 * nnz * F
+        flops["gemm"] += 2.0 * n * F * Fo * (3 if l > 0 else 2)
+        if l > 0:
+            kb4 = kernel_bytes(n, nnz, nc, S, F, slot_bits, slot_cut, 4 * F)
+            byt["spmm_bwd"] += kb4["bwd"]
+            flops["spmm"] += 2.0 * nnz * F
+    total_bytes = sum(byt.values())
+
+    # e2e through the layer API with host buffers: H2D of the step's inputs
+    # (layer-1 features, upstream gradient), D2H of the weight gradients
+    e2e = None
+    if args.e2e_steps > 0:
+        h_in = torch.empty((n, ld[0]), dtype=torch.float32, pin_memory=True)
+        h_in.copy_(H[0].cpu())
+        g_in = torch.empty((n, ld[L]), dtype=torch.float32, pin_memory=True)
+        g_in.copy_(dH[L].cpu())
+        dW_host = [torch.empty(dW[l].shape, dtype=torch.float32, pin_memory=True) for l in range(L)]
+        H0d = torch.empty_like(H[0])
+        dHLd = torch.empty_like(dH[L])
+
+        def e2e_step():
+            H0d.copy_(h_in, non_blocking=True)
+            dHLd.copy_(g_in, non_blocking=True)
+            Hs = [H0d] + H[1:]
+            for l in range(L):
+                F, Fo = dims[l], dims[l + 1]
+                G.gnn_layer_fwd(csr, bnd, Hs[l], F, W[l], Fo, l < L - 1, 2 * l, packed, meta, Mb[l],
+                                Hs[l + 1], slot_off=offs[F], ws=ws)
+            dHs = dH[:L] + [dHLd]
+            for l in reversed(range(L)):
+                F, Fo = dims[l], dims[l + 1]
+                G.gnn_layer_bwd(csr, bnd, dHs[l + 1], Hs[l + 1], l < L - 1, Mb[l], W[l], F, Fo,
+                                2 * l + 1, packed, meta, dW[l], dHs[l] if l > 0 else None,
+                                slot_off=offs[F], ws=ws)
+            for l in range(L):
+                dW_host[l].copy_(dW[l], non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = a.elapsed_time(b) / args.e2e_steps
+        G.gnn_sync_check()
+        h2d = h_in.numel() * 4 + g_in.numel() * 4
+        d2h = sum(x.numel() * 4 for x in dW_host)
+        e2e = dict(ms=e2e_ms, h2d=h2d, d2h=d2h)
+
+    return dict(ms=ms, per=per, per_layer=per_layer, byt=byt, flops=flops, total_bytes=total_bytes,
+                launches=launches, clocks=clk.summary(), e2e=e2e, S=S, nnz=nnz, nnz_cut=nc, n=n,
+                Q=int(offs[F0][-1].item()), spmm_fwd_bytes_l=spmm_fwd_bytes_l, n_long=csr.n_long,
+                n_pieces=csr.n_pieces, dims=dims, P=P)
+
+
+# --------------------------------------------------------------- oracle (CPU) arm
+class OracleBaseline:
+    """The oracle, as it stands, on bounded samples of the workload's rows:
+    forward aggregation (with quantisation of the remote rows it reads) and
+    backward aggregation (halo partials, quantisation, owner adds) at the
+    first layer width.  Rates use the same algorithmic byte model as the GPU
+    arm, scaled by the fraction of rows processed."""
+
+    def __init__(self, workload):
+        import oracle as O
+        from synth import make_workload
+
+        self.O = O
+        wl = make_workload(workload)
+        self.n = n = wl.n
+        self.rp, self.col, self.val = O.csr_build(n, wl.src, wl.dst)
+        self.b = O.boundary_index(n, self.rp, self.col, self.val, wl.P)
+        nb = O.node_bits(n, self.rp, self.b, wl.rule_pct, wl.rule_bits, wl.base_bits[0])
+        self.sb = nb[self.b["slot_node"]]
+        self.F = F = wl.dims[0]
+        rng = np.random.default_rng(wl.seed + 1)
+        self.H = rng.standard_normal((n, F)).astype(np.float32)
+        self.Gm = rng.standard_normal((n, F)).astype(np.float32)
+        slot_cut = np.diff(self.b["slot_rowptr"])
+        kb = kernel_bytes(n, len(self.col), self.b["nnz_cut"], self.b["n_slots"], F, self.sb, slot_cut, 4 * F)
+        self.per_row_bytes = (kb["fwd"] + kb["quant"] + kb["bwd"]) / n
+        self.order = rng.permutation(n)
+        self.pos = 0
+
+    def sample(self, budget_s):
+        O, n = self.O, self.n
+        rows_done, t_used, chunk = 0, 0.0, 256
+        t0 = time.perf_counter()
+        while t_used < budget_s and rows_done < n:
+            if self.pos >= n:
+                self.pos = 0
+            rows = np.sort(self.order[self.pos:self.pos + chunk])
+            self.pos += rows.size
+            O.spmm_fwd(n, self.rp, self.col, self.val, self.H, self.F, self.b, self.sb, seed=0, rows=rows)
+            O.spmm_bwd(n, self.rp, self.col, self.val, self.Gm, self.F, self.b, self.sb, seed=1, rows=rows)
+            rows_done += rows.size
+            t_used = time.perf_counter() - t0
+            chunk = min(chunk * 2, 1 << 14)
+        gbs = self.per_row_bytes * rows_done / t_used / 1e9
+        return dict(value=gbs, unit=UNIT, cores=1, kind="oracle",  # numpy/scipy run on one thread here
+                    sample=f"{rows_done} of {n} rows (forward + backward aggregation with quantised "
+                           f"boundary rows, F={self.F}), {t_used:.1f} s",
+                    seconds=t_used, rows=rows_done)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="yelp", choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
+    ap.add_argument("--split-len", type=int, default=256)
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if args.impl == "gpu" else "gloo")
+        if args.impl == "gpu":
+            import torch
+            torch.cuda.set_device(local_rank)
+
+    config = {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload,
+              "timing": "inputs larger than L2 (no flush); CUDA events on the launching stream",
+              "parallelism": f"replicas x{world}"}
+
+    if args.impl == "reference":
+        if rank == 0:
+            ob = OracleBaseline(args.workload)
+            per_step = max(1.0, args.cpu_budget / max(1, args.steps))
+            for _ in range(args.warmup):
+                ob.sample(0.2)
+            steps = []
+            cb = None
+            for _ in range(args.steps):
+                cb = ob.sample(per_step)
+                steps.append(cb["value"])
+            val = float(statistics.median(steps))
+            line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": world,
+                    "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+                    "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                    "config": config,
+                    "cpu_baseline": {"value": val, "unit": UNIT, "cores": cb["cores"], "kind": "oracle",
+                                     "sample": cb["sample"]},
+                    "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            print(json.dumps(line), flush=True)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    r = run_gpu(args, rank, world, local_rank)
+    ms = r["ms"]
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    hbm, bf16, bf16_sus, peak_src = load_peaks()
+    gbs = r["total_bytes"] * world / (ms * 1e-3) / 1e9
+    per = r["per"]
+
+    def rate(k):
+        return r["byt"][k] / (per[k] * 1e-3) / 1e9 if per[k] > 0 else None
+
+    spmm_ms = per["spmm_fwd"] + per["spmm_bwd"]
+    gemm_ms = per["gemm_fwd"] + per["mask_dM_dW"]
+    # dominant kernel: the forward aggregation of the first layer
+    L0 = 0
+    t_dom = r["per_layer"].get("spmm_fwd_l1")
+    dom_bytes = r["spmm_fwd_bytes_l"][L0]
+    achieved = dom_bytes / (t_dom * 1e-3) / 1e9 if t_dom else None
+    traffic = None
+    tfile = os.path.join(ROOT, "profiles", "spmm_fwd_yelp_traffic.json")
+    if args.workload == "yelp" and os.path.exists(tfile):
+        with open(tfile) as f:
+            traffic = json.load(f).get("dram_bytes_per_launch")
+    line = {
+        "metric": METRIC, "value": gbs, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp32 aggregation, bf16 transform, 1-8 bit messages",
+        "data": "synthetic (seeded generator; no dataset)",
+        "config": config,
+        "kernels": {
+            "spmm_fwd_GBs": rate("spmm_fwd"), "spmm_bwd_GBs": rate("spmm_bwd"),
+            "quant_pack_GBs": rate("quant"),
+            "spmm_GFLOPs": r["flops"]["spmm"] / (spmm_ms * 1e-3) / 1e9 if spmm_ms else None,
+            "gemm_TFLOPs": r["flops"]["gemm"] / (gemm_ms * 1e-3) / 1e12 if gemm_ms else None,
+            "ms": per, "ms_per_layer": r["per_layer"],
+            "hbm_frac": {k: (rate(k) / hbm if rate(k) else None) for k in ["spmm_fwd", "spmm_bwd", "quant"]},
+        },
+        "graph": {"n": r["n"], "nnz": r["nnz"], "nnz_cut": r["nnz_cut"], "slots": r["S"],
+                  "packed_bytes_layer1": r["Q"], "long_rows": r["n_long"], "pieces": r["n_pieces"],
+                  "dims": r["dims"], "P": r["P"]},
+        "roofline": {"kernel": "gnn_spmm_fwd, layer 1 (aggregation with in-gather dequantisation)",
+                     "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": (achieved / hbm) if achieved else None, "traffic": traffic,
+                     "peak_source": peak_src},
+        "gpu_launches": r["launches"],
+        "clocks": r["clocks"],
+    }
+    if r["e2e"]:
+        e = r["e2e"]
+        line["e2e"] = {"value": r["total_bytes"] * world / (e["ms"] * 1e-3) / 1e9, "unit": UNIT,
+                       "ms_per_step": e["ms"], "h2d_bytes_per_step": e["h2d"],
+                       "d2h_bytes_per_step": e["d2h"]}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cb = OracleBaseline(args.workload).sample(args.cpu_budget)
+        line["cpu_baseline"] = {k: cb[k] for k in ["value", "unit", "cores", "kind", "sample"]}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
