@@ -53,6 +53,8 @@ typedef void* gnn_stream_t; /* cudaStream_t */
 const char* gnn_last_error(void);
 /* Library version, major*10000 + minor*100 + patch. */
 int gnn_version(void);
+/* Kernels this process has launched through the library so far. */
+unsigned long long gnn_kernel_launches(void);
 
 /* ------------------------------------------------------------------------ */
 /* CSR adjacency with GCN normalisation.                                    */

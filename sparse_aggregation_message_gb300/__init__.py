@@ -16,7 +16,7 @@ from ._abi import (CSR_DEDUP, CSR_GCN, CSR_SELF_LOOPS, CSR_SYMMETRIZE, GnnBitRul
 __all__ = [
     "Csr", "Boundary", "BitRule", "GnnError", "load", "build",
     "gnn_csr_build", "gnn_csr_split", "gnn_spmm_workspace", "spmm_ws", "gnn_boundary_index", "gnn_boundary_set_bits", "gnn_slot_offsets",
-    "gnn_quant_pack", "gnn_dequant_unpack", "gnn_spmm_fwd", "gnn_spmm_bwd", "gnn_sync_check",
+    "gnn_quant_pack", "gnn_dequant_unpack", "gnn_spmm_fwd", "gnn_spmm_bwd", "gnn_sync_check", "gnn_kernel_launches",
     "rowbytes", "ld_for", "ldb_for", "gnn_dense_workspace", "gnn_dense_fwd", "gnn_dense_bwd",
     "gnn_layer_workspace", "gnn_layer_fwd", "gnn_layer_bwd",
 ]
@@ -281,6 +281,11 @@ def gnn_spmm_bwd(csr: Csr, bnd: Optional[Boundary], G, F: int, seed: int, packed
     call("gnn_spmm_bwd", ctypes.byref(c), ctypes.byref(cb) if cb is not None else None, _ptr(G),
          G.stride(0), F, seed & 0xFFFFFFFF, _ptr(packed_ws), _ptr(meta_ws), _ptr(dH), dH.stride(0),
          wp, wn, _stream(stream))
+
+
+def gnn_kernel_launches() -> int:
+    """Kernels launched through the library by this process so far."""
+    return int(load().gnn_kernel_launches())
 
 
 def gnn_sync_check(stream=None) -> None:

@@ -46,6 +46,7 @@ P_rule = ctypes.POINTER(GnnBitRule)
 PROTOTYPES = {
     "gnn_last_error": (c_char_p, []),
     "gnn_version": (ctypes.c_int, []),
+    "gnn_kernel_launches": (ctypes.c_ulonglong, []),
     "gnn_csr_build_workspace": (ctypes.c_int, [c_i32, c_i64, c_u32, P_size]),
     "gnn_csr_build": (ctypes.c_int, [c_i32, c_i64, c_vp, c_vp, c_u32, c_i64, P_csr, c_vp, c_size, c_vp]),
     "gnn_csr_split_workspace": (ctypes.c_int, [P_csr, P_size]),

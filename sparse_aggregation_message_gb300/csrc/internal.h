@@ -25,7 +25,14 @@ inline cudaStream_t as_stream(gnn_stream_t s) { return reinterpret_cast<cudaStre
                          cudaGetErrorString(e_), __FILE__, __LINE__);               \
   } while (0)
 
-#define GNN_CHECK_LAUNCH() GNN_CUDA(cudaGetLastError())
+// Counts library kernel launches (reported by gnn_kernel_launches).
+void count_launch();
+
+#define GNN_CHECK_LAUNCH()        \
+  do {                            \
+    ::gnn::count_launch();        \
+    GNN_CUDA(cudaGetLastError()); \
+  } while (0)
 
 #define GNN_REQUIRE(cond, ...)                                                      \
   do {                                                                              \

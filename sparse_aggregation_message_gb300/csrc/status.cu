@@ -3,6 +3,8 @@
 #include <stdarg.h>
 #include <stdio.h>
 
+#include <atomic>
+
 #include "internal.h"
 
 namespace gnn {
@@ -16,6 +18,10 @@ gnn_status fail(gnn_status code, const char* fmt, ...) {
   va_end(ap);
   return code;
 }
+
+static std::atomic<unsigned long long> g_launches{0};
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 // Bit 0: a kernel found bad data; bit 1: a bounded wait gave up.
 __device__ unsigned g_device_flags = 0;
@@ -31,6 +37,10 @@ unsigned* device_flags() {
 extern "C" const char* gnn_last_error(void) { return gnn::g_last_error; }
 
 extern "C" int gnn_version(void) { return 1 * 10000 + 0 * 100 + 0; }
+
+extern "C" unsigned long long gnn_kernel_launches(void) {
+  return gnn::g_launches.load(std::memory_order_relaxed);
+}
 
 extern "C" gnn_status gnn_sync_check(gnn_stream_t stream) {
   GNN_CUDA(cudaStreamSynchronize(gnn::as_stream(stream)));
