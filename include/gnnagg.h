@@ -238,6 +238,24 @@ gnn_status gnn_spmm_fwd(const gnn_csr* csr, const gnn_boundary* bnd,
  * feature width F: n_pieces * round_up(F, 4) * 4 (0 without a plan). */
 gnn_status gnn_spmm_workspace(const gnn_csr* csr, int32_t F, size_t* ws_bytes);
 
+/* gnn_spmm_fwd without a workspace, for callers that cannot allocate device
+ * memory while they run (a serving loop whose memory is all reserved at
+ * start-up, or a plugin that its host framework gives only input and output
+ * pointers).  The pages this library follows have no counterpart: it is an
+ * interface convenience.  The split plan's partial rows go to a fixed 32 MiB
+ * device array inside the library (n_pieces * round_up(F,4) * 4 bytes must fit,
+ * else GNN_ERR_UNSUPPORTED with no launch); every GPU that loads the library
+ * holds that array until the process exits.  The first call on a device looks
+ * up the array's device address with that device current, so make it before
+ * any stream capture.  All calls share the array: calls that overlap on the
+ * GPU (other streams, other threads) race.  Arguments and results are as for
+ * gnn_spmm_fwd. */
+gnn_status gnn_spmm_fwd_noalloc(const gnn_csr* csr, const gnn_boundary* bnd,
+                                const float* H, int64_t ldh, int32_t F,
+                                const uint8_t* packed, const float* meta, float* M,
+                                int64_t ldm, uint16_t* Mb, int64_t ldmb,
+                                gnn_stream_t stream);
+
 /* Backward aggregation dH = A^T G for symmetric A (section 3: embedding
  * gradients travel back along the same cross-partition dependencies).  With
  * bnd: each slot s = (q, u) first forms the halo partial

@@ -15,7 +15,7 @@ from ._abi import (CSR_DEDUP, CSR_GCN, CSR_SELF_LOOPS, CSR_SYMMETRIZE, GnnBitRul
 
 __all__ = [
     "Csr", "Boundary", "BitRule", "GnnError", "load", "build",
-    "gnn_csr_build", "gnn_csr_split", "gnn_spmm_workspace", "spmm_ws", "gnn_boundary_index", "gnn_boundary_set_bits", "gnn_slot_offsets",
+    "gnn_csr_build", "gnn_csr_split", "gnn_spmm_workspace", "spmm_ws", "gnn_spmm_fwd_noalloc", "gnn_boundary_index", "gnn_boundary_set_bits", "gnn_slot_offsets",
     "gnn_quant_pack", "gnn_dequant_unpack", "gnn_spmm_fwd", "gnn_spmm_bwd", "gnn_sync_check", "gnn_kernel_launches",
     "rowbytes", "ld_for", "ldb_for", "gnn_dense_workspace", "gnn_dense_fwd", "gnn_dense_bwd",
     "gnn_layer_workspace", "gnn_layer_fwd", "gnn_layer_bwd",
@@ -255,6 +255,18 @@ def gnn_dequant_unpack(packed, meta, row_off, row_bits, n_rows: int, F: int, out
                        stream=None) -> None:
     call("gnn_dequant_unpack", _ptr(packed), _ptr(meta), _ptr(row_off), _ptr(row_bits), n_rows, F,
          _ptr(out), out.stride(0), _stream(stream))
+
+
+def gnn_spmm_fwd_noalloc(csr: Csr, bnd: Optional[Boundary], H, F: int, packed=None, meta=None,
+                         M=None, Mb=None, slot_off=None, stream=None) -> None:
+    """gnn_spmm_fwd for callers that cannot allocate: scratch comes from a
+    fixed device array inside the library (see the C header)."""
+    c = csr.c()
+    cb = bnd.c(slot_off, F if slot_off is not None else None) if bnd is not None else None
+    call("gnn_spmm_fwd_noalloc", ctypes.byref(c), ctypes.byref(cb) if cb is not None else None,
+         _ptr(H), H.stride(0), F, _ptr(packed), _ptr(meta), _ptr(M),
+         M.stride(0) if M is not None else 0, _ptr(Mb), Mb.stride(0) if Mb is not None else 0,
+         _stream(stream))
 
 
 def _ws_args(csr: Csr, F: int, ws, device):

@@ -63,6 +63,8 @@ PROTOTYPES = {
     "gnn_spmm_workspace": (ctypes.c_int, [P_csr, c_i32, P_size]),
     "gnn_spmm_fwd": (ctypes.c_int, [P_csr, P_bnd, c_vp, c_i64, c_i32, c_vp, c_vp, c_vp, c_i64, c_vp, c_i64,
                                     c_vp, c_size, c_vp]),
+    "gnn_spmm_fwd_noalloc": (ctypes.c_int, [P_csr, P_bnd, c_vp, c_i64, c_i32, c_vp, c_vp, c_vp, c_i64,
+                                            c_vp, c_i64, c_vp]),
     "gnn_spmm_bwd": (ctypes.c_int, [P_csr, P_bnd, c_vp, c_i64, c_i32, c_u32, c_vp, c_vp, c_vp, c_i64,
                                     c_vp, c_size, c_vp]),
     "gnn_dense_workspace": (ctypes.c_int, [c_i64, c_i32, c_i32, P_size]),

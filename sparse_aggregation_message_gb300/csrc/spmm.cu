@@ -18,6 +18,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "device.cuh"
 #include "internal.h"
 #include "kernels.h"
@@ -530,4 +532,70 @@ extern "C" gnn_status gnn_spmm_bwd(const gnn_csr* csr, const gnn_boundary* bnd, 
   return launch_spmm_bwd(*csr, bnd, G, ldg, F, seed, packed_ws,
                          reinterpret_cast<float2*>(meta_ws), dH, ldh, static_cast<float*>(ws),
                          as_stream(stream));
+}
+
+// ---------------------------------------------------------------- no-allocation forward
+// Some callers cannot call cudaMalloc once they are running: a serving loop
+// whose device memory is fully reserved at start-up, or a plugin that a host
+// framework hands only input and output pointers while keeping every
+// allocation to itself.  gnn_spmm_fwd_noalloc serves them: the partial rows of
+// the split plan live in the fixed device array below instead of a caller
+// workspace.  Every GPU that loads this library holds the array until the
+// process exits.
+namespace {
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;  // 32 MiB
+constexpr int kNoAllocMaxDevices = 64;
+static __device__ __align__(256) float g_noalloc_partials[kNoAllocScratchBytes / sizeof(float)];
+std::mutex g_noalloc_mu;
+float* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+}  // namespace
+
+// Device address of the array on the current device.  Host code only knows a
+// host-side stand-in for the symbol, so the address is looked up once per
+// device (with that device current) and cached.
+static gnn_status noalloc_scratch(float** out) {
+  int dev = 0;
+  GNN_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kNoAllocMaxDevices)
+    return fail(GNN_ERR_UNSUPPORTED, "gnn_spmm_fwd_noalloc: device %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    GNN_CUDA(cudaGetSymbolAddress(&p, g_noalloc_partials));
+    g_noalloc_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return GNN_OK;
+}
+
+extern "C" gnn_status gnn_spmm_fwd_noalloc(const gnn_csr* csr, const gnn_boundary* bnd,
+                                           const float* H, int64_t ldh, int32_t F,
+                                           const uint8_t* packed, const float* meta, float* M,
+                                           int64_t ldm, uint16_t* Mb, int64_t ldmb,
+                                           gnn_stream_t stream) {
+  gnn_status st = check_csr(csr, "gnn_spmm_fwd_noalloc");
+  if (st != GNN_OK) return st;
+  GNN_REQUIRE(F >= 1, "gnn_spmm_fwd_noalloc: F must be >= 1");
+  if (F > kMaxF) return fail(GNN_ERR_UNSUPPORTED, "gnn_spmm_fwd_noalloc: F=%d > %d", F, kMaxF);
+  const size_t need = spmm_workspace_bytes(*csr, F);
+  if (need > kNoAllocScratchBytes)
+    return fail(GNN_ERR_UNSUPPORTED,
+                "gnn_spmm_fwd_noalloc: the split plan needs %zu bytes of scratch at F=%d; the "
+                "static buffer holds %zu (use gnn_spmm_fwd with a workspace)",
+                need, F, kNoAllocScratchBytes);
+  if ((st = check_bnd(csr, bnd, F, false, "gnn_spmm_fwd_noalloc")) != GNN_OK) return st;
+  if (csr->n == 0) return GNN_OK;
+  GNN_REQUIRE(H && (M || Mb), "gnn_spmm_fwd_noalloc: H is NULL or no output given");
+  GNN_REQUIRE(ldh >= F && ldh % 4 == 0 && ((uintptr_t)H & 15) == 0,
+              "gnn_spmm_fwd_noalloc: ldh must be >= F, a multiple of 4, H 16-byte aligned");
+  GNN_REQUIRE(!M || (ldm >= F && ldm % 4 == 0 && ((uintptr_t)M & 15) == 0),
+              "gnn_spmm_fwd_noalloc: ldm must be >= F, a multiple of 4, M 16-byte aligned");
+  GNN_REQUIRE(!Mb || (ldmb >= (F + 15) / 16 * 16 && ldmb % 8 == 0 && ((uintptr_t)Mb & 15) == 0),
+              "gnn_spmm_fwd_noalloc: ldmb must be >= round_up(F,16), a multiple of 8, Mb 16-byte aligned");
+  GNN_REQUIRE(!bnd || bnd->n_slots == 0 || (packed && meta),
+              "gnn_spmm_fwd_noalloc: packed/meta required with a boundary");
+  float* scratch = nullptr;
+  if ((st = noalloc_scratch(&scratch)) != GNN_OK) return st;
+  return launch_spmm_fwd(*csr, bnd, H, ldh, F, packed, reinterpret_cast<const float2*>(meta), M,
+                         ldm, Mb, ldmb, scratch, as_stream(stream));
 }
