@@ -87,13 +87,21 @@ def csr_build(n, src, dst, flags=FLAGS_GCN):
         rows = np.concatenate([rows[keep], ids])
         cols = np.concatenate([cols[keep], ids])
     key = rows * n + cols
-    key = np.unique(key) if flags & FLAG_DEDUP else np.sort(key)
+    key = _distinct_sorted(key) if flags & FLAG_DEDUP else np.sort(key)
     rows, cols = key // n, key % n
     rowptr = np.zeros(n + 1, np.int64)
     rowptr[1:] = np.cumsum(np.bincount(rows, minlength=n))
     deg = np.diff(rowptr).astype(np.float64)
     val = (1.0 / np.sqrt(deg[rows] * deg[cols])).astype(F32)
     return rowptr, cols.astype(np.int32), val
+
+
+def _distinct_sorted(a):
+    """Sorted distinct values of an integer array (sort, drop repeats)."""
+    a = np.sort(np.asarray(a))
+    if a.size < 2:
+        return a
+    return a[np.concatenate([[True], a[1:] != a[:-1]])]
 
 
 def csr_rows(rowptr):
@@ -122,7 +130,7 @@ def boundary_index(n, rowptr, col, val, P):
     pv = part_of(rows, starts)
     pu = part_of(col64, starts)
     cut = pv != pu
-    slot_keys = np.unique(pv[cut] * n + col64[cut])
+    slot_keys = _distinct_sorted(pv[cut] * n + col64[cut])
     S = slot_keys.size
     slot_q = slot_keys // n
     slot_node = (slot_keys % n).astype(np.int32)

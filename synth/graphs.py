@@ -57,13 +57,6 @@ def _rng(*key) -> np.random.Generator:
     return np.random.default_rng([int(k) & 0xFFFFFFFF for k in key])
 
 
-def _unique_pairs_in_draw_order(keys: np.ndarray) -> np.ndarray:
-    """Distinct values of ``keys`` in order of first appearance."""
-    _, first = np.unique(keys, return_index=True)
-    first.sort()
-    return keys[first]
-
-
 def _keys(u: np.ndarray, v: np.ndarray, n: int) -> np.ndarray:
     lo = np.minimum(u, v).astype(np.int64)
     hi = np.maximum(u, v).astype(np.int64)
@@ -74,19 +67,32 @@ def _split_keys(keys: np.ndarray, n: int):
     return (keys // n).astype(np.int32), (keys % n).astype(np.int32)
 
 
+def _sorted_distinct(a: np.ndarray) -> np.ndarray:
+    a.sort()
+    if a.size < 2:
+        return a
+    keep = np.empty(a.size, bool)
+    keep[0] = True
+    np.not_equal(a[1:], a[:-1], out=keep[1:])
+    return a[keep]
+
+
 def _draw_until(n: int, m_target: int, draw, rng) -> tuple[np.ndarray, np.ndarray]:
-    """Call ``draw(rng, k) -> (u, v)`` until ``m_target`` distinct non-loop
-    unordered pairs exist; keep the first ``m_target`` in draw order."""
+    """Call ``draw(rng, k) -> (u, v)`` until at least ``m_target`` distinct
+    non-loop unordered pairs have been drawn, then keep a seeded uniform
+    subset of exactly ``m_target`` of them."""
     have = np.empty(0, np.int64)
     factor = 1.08
     while have.size < m_target:
         k = int((m_target - have.size) * factor) + 1024
         u, v = draw(rng, k)
         keep = u != v
-        new = _keys(u[keep], v[keep], n)
-        have = _unique_pairs_in_draw_order(np.concatenate([have, new]))
+        have = _sorted_distinct(np.concatenate([have, _keys(u[keep], v[keep], n)]))
         factor = min(4.0, factor * 1.5)
-    return _split_keys(have[:m_target], n)
+    if have.size > m_target:
+        pick = np.sort(rng.choice(have.size, m_target, replace=False))
+        have = have[pick]
+    return _split_keys(have, n)
 
 
 def community_starts(n: int, c: int) -> np.ndarray:
@@ -196,9 +202,9 @@ def rmat_edges(scale: int, draws: int, abcd, seed: int, blocks: int = 16):
             s |= sbit.astype(np.int64) << sh
             d |= dbit.astype(np.int64) << sh
         keep = s != d
-        keys.append(np.unique(_keys(s[keep], d[keep], n)))
+        keys.append(_sorted_distinct(_keys(s[keep], d[keep], n)))
         done += k
-    keys = np.unique(np.concatenate(keys))
+    keys = _sorted_distinct(np.concatenate(keys))
     u, v = _split_keys(keys, n)
     perm = rng.permutation(n).astype(np.int32)
     u, v = perm[u], perm[v]
@@ -232,7 +238,7 @@ def circulant_edges(n: int, d: int):
         vs.append(h + n // 2)
     u = np.concatenate(us)
     v = np.concatenate(vs)
-    keys = np.unique(_keys(u, v, n))
+    keys = _sorted_distinct(_keys(u, v, n))
     return _split_keys(keys, n)
 
 
