@@ -81,6 +81,27 @@ def gemm_bytes(n, F_in, F_out):
     return dict(fwd=fwd, mask=mask, dM=dM, dW=dW)
 
 
+def committed_traffic():
+    """DRAM bytes per launch of the layer-1 forward aggregation from the
+    committed ncu summary, or None when the kernel source has changed since
+    those counters were taken (the summary records a hash of the source)."""
+    import hashlib
+    import re
+
+    path = os.path.join(ROOT, "profiles", "kernels_yelp_fullset.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_b = re.search(r"^traffic_bytes_per_launch:\s*(\d+)", text, re.M)
+    m_h = re.search(r"^traffic_source_sha256_16:\s*([0-9a-f]+)", text, re.M)
+    if not (m_b and m_h):
+        return None
+    csrc = os.path.join(ROOT, "sparse_aggregation_message_gb300", "csrc")
+    h = hashlib.sha256(open(os.path.join(csrc, "spmm.cu"), "rb").read() +
+                       open(os.path.join(csrc, "device.cuh"), "rb").read()).hexdigest()[:16]
+    return int(m_b.group(1)) if h == m_h.group(1) else None
+
+
 # --------------------------------------------------------------- clocks
 class ClockSampler:
     def __init__(self, index=0):
@@ -476,11 +497,7 @@ def main():
     t_dom = r["per_layer"].get("spmm_fwd_l1")
     dom_bytes = r["spmm_fwd_bytes_l"][L0]
     achieved = dom_bytes / (t_dom * 1e-3) / 1e9 if t_dom else None
-    traffic = None
-    tfile = os.path.join(ROOT, "profiles", "spmm_fwd_yelp_traffic.json")
-    if args.workload == "yelp" and os.path.exists(tfile):
-        with open(tfile) as f:
-            traffic = json.load(f).get("dram_bytes_per_launch")
+    traffic = committed_traffic() if args.workload == "yelp" else None
     line = {
         "metric": METRIC, "value": gbs, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
