@@ -176,6 +176,7 @@ def run_gpu(args, rank, world, local_rank):
     rule = G.BitRule(wl.rule_pct, wl.rule_bits)
     F0 = dims[0]
     bnd = G.gnn_boundary_index(csr, P, rule, base, F0)
+    G.gnn_boundary_long_slots(csr, bnd, args.long_slot_len)
     S = bnd.n_slots
     widths = sorted(set(dims[:-1]))
     offs = {F: (bnd.slot_off if F == F0 else G.gnn_slot_offsets(bnd.slot_bits, S, F)) for F in widths}
@@ -429,7 +430,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="yelp", choices=sorted(WORKLOAD_TEXT))
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
-    ap.add_argument("--split-len", type=int, default=256)
+    ap.add_argument("--split-len", type=int, default=128)
+    ap.add_argument("--long-slot-len", type=int, default=128)
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -154,6 +154,12 @@ typedef struct gnn_boundary {
   uint8_t* node_bits;   /* [n]                                                 */
   uint8_t* slot_bits;   /* [S] = node_bits[slot_node[s]]                       */
   int64_t* slot_off;    /* [S+1] byte offset of slot s in a message buffer     */
+  /* Optional list of slots with more than long_slot_len backward entries
+   * (gnn_boundary_long_slots; zero/NULL = none).  Their halo partials are
+   * summed by a whole thread block each, in the same fixed order.          */
+  int32_t long_slot_len;
+  int32_t n_long_slots;
+  int32_t* long_slots;  /* [n_long_slots] ascending                          */
 } gnn_boundary;
 
 /* Workspace bytes for gnn_boundary_count / _index / _set_bits on this CSR. */
@@ -179,6 +185,16 @@ gnn_status gnn_boundary_index(const gnn_csr* csr, const gnn_bit_rule* rule,
 gnn_status gnn_boundary_set_bits(const gnn_csr* csr, const gnn_bit_rule* rule,
                                  uint8_t base_bits, int32_t F, gnn_boundary* bnd,
                                  void* ws, size_t ws_bytes, gnn_stream_t stream);
+
+/* Long-slot list for load balance of the backward halo partials: the count
+ * of slots with more than long_slot_len (>= 32) entries (synchronises), then,
+ * with bnd->long_slots allocated and long_slot_len / n_long_slots set, the
+ * list itself.  Workspace: gnn_boundary_workspace bytes. */
+gnn_status gnn_boundary_long_slots_count(const gnn_boundary* bnd, int32_t long_slot_len,
+                                         int32_t* n_long_slots, void* ws, size_t ws_bytes,
+                                         gnn_stream_t stream);
+gnn_status gnn_boundary_long_slots(gnn_boundary* bnd, void* ws, size_t ws_bytes,
+                                   gnn_stream_t stream);
 
 /* slot_off[s] = sum_{t<s} rowbytes(slot_bits[t], F), slot_off[S] = total,
  * rowbytes(b,F) = 16*ceil(F*b/128) (b=32: 16*ceil(4F/16)).  Every row starts

@@ -15,7 +15,7 @@ from ._abi import (CSR_DEDUP, CSR_GCN, CSR_SELF_LOOPS, CSR_SYMMETRIZE, GnnBitRul
 
 __all__ = [
     "Csr", "Boundary", "BitRule", "GnnError", "load", "build",
-    "gnn_csr_build", "gnn_csr_split", "gnn_spmm_workspace", "spmm_ws", "gnn_spmm_fwd_noalloc", "gnn_boundary_index", "gnn_boundary_set_bits", "gnn_slot_offsets",
+    "gnn_csr_build", "gnn_csr_split", "gnn_spmm_workspace", "spmm_ws", "gnn_spmm_fwd_noalloc", "gnn_boundary_index", "gnn_boundary_long_slots", "gnn_boundary_set_bits", "gnn_slot_offsets",
     "gnn_quant_pack", "gnn_dequant_unpack", "gnn_spmm_fwd", "gnn_spmm_bwd", "gnn_sync_check", "gnn_kernel_launches",
     "rowbytes", "ld_for", "ldb_for", "gnn_dense_workspace", "gnn_dense_fwd", "gnn_dense_bwd",
     "gnn_layer_workspace", "gnn_layer_fwd", "gnn_layer_bwd",
@@ -105,6 +105,8 @@ class Boundary:
     nnz_cut: int
     F: int
     arrays: dict = field(default_factory=dict)
+    long_slot_len: int = 0
+    n_long_slots: int = 0
 
     def __getattr__(self, k):
         arrays = self.__dict__.get("arrays", {})
@@ -121,6 +123,8 @@ class Boundary:
                   "slot_val", "own_ptr", "own_slot", "node_bits", "slot_bits"):
             setattr(b, k, _ptr(a[k]))
         b.slot_off = _ptr(a["slot_off"] if slot_off is None else slot_off)
+        b.long_slot_len, b.n_long_slots = self.long_slot_len, self.n_long_slots
+        b.long_slots = _ptr(a.get("long_slots"))
         return b
 
 
@@ -217,6 +221,26 @@ def gnn_boundary_index(csr: Csr, P: int, rule: BitRule, base_bits: int, F: int,
                  node_bits=n, slot_bits=S, slot_off=S + 1)
     b.arrays = {k: v[:sizes[k]] for k, v in a.items()}
     return b
+
+
+def gnn_boundary_long_slots(csr: Csr, bnd: Boundary, long_slot_len: int = 128, stream=None) -> None:
+    """Attach the list of slots with more than long_slot_len backward entries
+    (their halo partials are then summed by a whole thread block each)."""
+    torch = _torch()
+    dev = csr.rowptr.device
+    c = csr.c()
+    ws_bytes = ctypes.c_size_t()
+    call("gnn_boundary_workspace", ctypes.byref(c), bnd.P, ctypes.byref(ws_bytes))
+    ws = _workspace(ws_bytes.value, dev)
+    cb = bnd.c()
+    nl = ctypes.c_int32()
+    st = _stream(stream)
+    call("gnn_boundary_long_slots_count", ctypes.byref(cb), long_slot_len, ctypes.byref(nl), _ptr(ws),
+         ws.numel(), st)
+    bnd.arrays["long_slots"] = torch.empty(max(nl.value, 1), dtype=torch.int32, device=dev)
+    bnd.long_slot_len, bnd.n_long_slots = long_slot_len, nl.value
+    cb = bnd.c()
+    call("gnn_boundary_long_slots", ctypes.byref(cb), _ptr(ws), ws.numel(), st)
 
 
 def gnn_boundary_set_bits(csr: Csr, bnd: Boundary, rule: BitRule, base_bits: int, F: int,

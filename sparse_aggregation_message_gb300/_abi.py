@@ -35,7 +35,8 @@ class GnnBoundary(ctypes.Structure):
                 ("reserved", c_i32), ("part_start", c_vp), ("send_start", c_vp),
                 ("slot_node", c_vp), ("col_remap", c_vp), ("slot_rowptr", c_vp),
                 ("slot_col", c_vp), ("slot_val", c_vp), ("own_ptr", c_vp), ("own_slot", c_vp),
-                ("node_bits", c_vp), ("slot_bits", c_vp), ("slot_off", c_vp)]
+                ("node_bits", c_vp), ("slot_bits", c_vp), ("slot_off", c_vp),
+                ("long_slot_len", c_i32), ("n_long_slots", c_i32), ("long_slots", c_vp)]
 
 
 P_csr = ctypes.POINTER(GnnCsr)
@@ -56,6 +57,8 @@ PROTOTYPES = {
     "gnn_boundary_count": (ctypes.c_int, [P_csr, c_i32, P_i64, P_i64, c_vp, c_size, c_vp]),
     "gnn_boundary_index": (ctypes.c_int, [P_csr, P_rule, c_u8, c_i32, P_bnd, c_vp, c_size, c_vp]),
     "gnn_boundary_set_bits": (ctypes.c_int, [P_csr, P_rule, c_u8, c_i32, P_bnd, c_vp, c_size, c_vp]),
+    "gnn_boundary_long_slots_count": (ctypes.c_int, [P_bnd, c_i32, ctypes.POINTER(c_i32), c_vp, c_size, c_vp]),
+    "gnn_boundary_long_slots": (ctypes.c_int, [P_bnd, c_vp, c_size, c_vp]),
     "gnn_slot_offsets_workspace": (ctypes.c_int, [c_i64, P_size]),
     "gnn_slot_offsets": (ctypes.c_int, [c_vp, c_i64, c_i32, c_vp, c_vp, c_size, c_vp]),
     "gnn_quant_pack": (ctypes.c_int, [c_vp, c_i64, c_i32, c_vp, c_i64, c_vp, c_vp, c_u32, c_vp, c_vp, c_vp]),

@@ -89,26 +89,30 @@ __device__ __forceinline__ void quantize_pack_row(const float4 (&v)[CPL], int F,
   }
   if (__float_as_uint(mn) == 0x80000000u) mn = 0.f;  // a zero min/max is stored as +0
   if (__float_as_uint(mx) == 0x80000000u) mx = 0.f;
-  const float top = static_cast<float>((1u << b) - 1u);
+  const float top = static_cast<float>((1u << b) - 1u);  // exact: 2^b - 1 < 2^24
   const bool flat = !(mx > mn);
   const float scale = flat ? 0.f : __fdiv_rn(__fsub_rn(mx, mn), top);
   // chunk slots covered by the padded row: rowbytes*2/b chunks
   const int slots = (int)(rowbytes_dev(b, F) * 2u) / b;
   const int per_word = 8 / b;  // chunks per 32-bit word
   uint32_t* words = reinterpret_cast<uint32_t*>(out);
+  const uint32_t topi = (1u << b) - 1u;
 #pragma unroll
   for (int i = 0; i < CPL; ++i) {
     const int c = gl + i * G;
     uint32_t part = 0;
     if (c < nch && !flat) {
+      // floor(t + u) >= 0 and below 2^24, so rounding down while converting
+      // to an integer gives the same code as floorf followed by a conversion
+      const bool full = 4 * c + 3 < F;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int j = 4 * c + k;
-        if (j < F) {
+        if (full || j < F) {
           const float t = __fdiv_rn(__fsub_rn(elem(v[i], k), mn), scale);
           const float u = sr_offset(key, (uint32_t)j);
-          const float q = fminf(floorf(__fadd_rn(t, u)), top);
-          part |= static_cast<uint32_t>(q) << (k * b);
+          const uint32_t q = min(__float2uint_rd(__fadd_rn(t, u)), topi);
+          part |= q << (k * b);
         }
       }
     }

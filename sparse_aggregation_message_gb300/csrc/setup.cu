@@ -724,3 +724,65 @@ extern "C" gnn_status gnn_csr_split(gnn_csr* csr, void* ws, size_t ws_bytes, gnn
   GNN_CUDA(cudaStreamSynchronize(st));
   return GNN_OK;
 }
+
+// ------------------------------------------------------------------ long slots
+__global__ void long_flag_kernel(int64_t S, const int64_t* __restrict__ srp, int T,
+                                 int32_t* __restrict__ flag) {
+  const int64_t s = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (s > S) return;
+  flag[s] = (s < S && srp[s + 1] - srp[s] > T) ? 1 : 0;
+}
+
+__global__ void long_fill_kernel(int64_t S, const int32_t* __restrict__ flag,
+                                 const int32_t* __restrict__ pos, int32_t* __restrict__ out) {
+  const int64_t s = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (s < S && flag[s]) out[pos[s]] = (int32_t)s;
+}
+
+static gnn_status long_slots_scan(const gnn_boundary& b, int T, void* ws, size_t ws_bytes,
+                                  int32_t** flag, int32_t** pos, int32_t* count, cudaStream_t st) {
+  const int64_t S = b.n_slots;
+  size_t t = 0;
+  GNN_CUDA(cub::DeviceScan::ExclusiveSum(nullptr, t, (int32_t*)nullptr, (int32_t*)nullptr, S + 1));
+  Arena ar(ws, ws_bytes);
+  *flag = ar.take<int32_t>((size_t)S + 1);
+  *pos = ar.take<int32_t>((size_t)S + 1);
+  void* temp = ar.take_bytes(t);
+  if (!ar.ok()) return fail(GNN_ERR_INVALID_ARG, "long slots: workspace too small");
+  long_flag_kernel<<<GRID1(S + 1), 0, st>>>(S, b.slot_rowptr, T, *flag);
+  GNN_CHECK_LAUNCH();
+  GNN_CUDA(cub::DeviceScan::ExclusiveSum(temp, t, *flag, *pos, S + 1, st));
+  GNN_CUDA(cudaMemcpyAsync(count, *pos + S, sizeof(int32_t), cudaMemcpyDeviceToHost, st));
+  GNN_CUDA(cudaStreamSynchronize(st));
+  return GNN_OK;
+}
+
+extern "C" gnn_status gnn_boundary_long_slots_count(const gnn_boundary* bnd, int32_t long_slot_len,
+                                                    int32_t* n_long_slots, void* ws,
+                                                    size_t ws_bytes, gnn_stream_t stream) {
+  GNN_REQUIRE(bnd && n_long_slots && ws && long_slot_len >= 32 && bnd->slot_rowptr,
+              "gnn_boundary_long_slots_count: bad arguments");
+  int32_t *flag, *pos;
+  return long_slots_scan(*bnd, long_slot_len, ws, ws_bytes, &flag, &pos, n_long_slots,
+                         as_stream(stream));
+}
+
+extern "C" gnn_status gnn_boundary_long_slots(gnn_boundary* bnd, void* ws, size_t ws_bytes,
+                                              gnn_stream_t stream) {
+  GNN_REQUIRE(bnd && ws && bnd->long_slot_len >= 32 && bnd->slot_rowptr &&
+                  (bnd->n_long_slots == 0 || bnd->long_slots),
+              "gnn_boundary_long_slots: bad arguments");
+  cudaStream_t st = as_stream(stream);
+  int32_t *flag, *pos, count = 0;
+  gnn_status s = long_slots_scan(*bnd, bnd->long_slot_len, ws, ws_bytes, &flag, &pos, &count, st);
+  if (s != GNN_OK) return s;
+  if (count != bnd->n_long_slots)
+    return fail(GNN_ERR_INVALID_ARG, "gnn_boundary_long_slots: n_long_slots %d does not match %d",
+                bnd->n_long_slots, count);
+  if (bnd->n_slots > 0) {
+    long_fill_kernel<<<GRID1(bnd->n_slots), 0, st>>>(bnd->n_slots, flag, pos, bnd->long_slots);
+    GNN_CHECK_LAUNCH();
+  }
+  GNN_CUDA(cudaStreamSynchronize(st));
+  return GNN_OK;
+}

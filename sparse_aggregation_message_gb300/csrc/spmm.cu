@@ -47,20 +47,19 @@ struct RowSplit {
 
 // acc += sum over entries [beg, end) of val * x, x = H[col] or the remote
 // slot's dequantised message (kFwdRemote); remote entries are skipped in the
-// backward (their contribution arrives as the owner's message).
+// backward (their contribution arrives as the owner's message).  The group
+// covers chunks c0 + gl + i*G (i < CPL) below c_end.  One accumulator per
+// chunk; U entries are gathered before they are added, so U*CPL 16-byte loads
+// per lane are in flight.
 template <int G, int CPL, int MODE, int U>
-__device__ __forceinline__ void gather_range(int64_t beg, int64_t end, int64_t self_row,
-                                             const int32_t* __restrict__ col,
+__device__ __forceinline__ void gather_range(int64_t beg, int64_t end, const int32_t* __restrict__ col,
                                              const float* __restrict__ val,
-                                             const float4* __restrict__ H4, int64_t ldh4, int nch,
-                                             const SlotMsgs& msg, int gl, uint32_t gmask,
+                                             const float4* __restrict__ H4, int64_t ldh4, int c0,
+                                             int c_end, const SlotMsgs& msg, int gl, uint32_t gmask,
                                              float4 (&acc)[CPL]) {
-  float4 acc1[CPL];
-#pragma unroll
-  for (int i = 0; i < CPL; ++i) acc1[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int64_t base = beg; base < end; base += G) {
     const int64_t e = base + gl;
-    int cc = (int)self_row;
+    int cc = 0;
     float w = 0.f;
     int sb = 0;
     uint32_t so16 = 0;
@@ -74,10 +73,6 @@ __device__ __forceinline__ void gather_range(int64_t beg, int64_t end, int64_t s
         so16 = (uint32_t)(__ldg(msg.off + s) >> 4);
         sm = __ldg(msg.meta + s);
       }
-      if (MODE == kBwdOwned && cc < 0) {
-        cc = (int)self_row;
-        w = 0.f;
-      }
     }
     const int cnt = (int)min((int64_t)G, end - base);
     for (int k = 0; k < cnt; k += U) {
@@ -85,10 +80,10 @@ __device__ __forceinline__ void gather_range(int64_t beg, int64_t end, int64_t s
       float wk[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const int src = (k + u < cnt) ? k + u : k;
+        const bool valid = k + u < cnt;
+        const int src = valid ? k + u : k;
         const int ck = __shfl_sync(gmask, cc, src, G);
-        wk[u] = __shfl_sync(gmask, w, src, G);
-        if (k + u >= cnt) wk[u] = 0.f;
+        wk[u] = valid ? __shfl_sync(gmask, w, src, G) : 0.f;
         if (MODE == kFwdRemote) {
           const int bk = __shfl_sync(gmask, sb, src, G);
           const uint32_t ok = __shfl_sync(gmask, so16, src, G);
@@ -96,40 +91,36 @@ __device__ __forceinline__ void gather_range(int64_t beg, int64_t end, int64_t s
           const float sck = __shfl_sync(gmask, sm.y, src, G);
 #pragma unroll
           for (int i = 0; i < CPL; ++i) {
-            const int c = gl + i * G;
-            if (c < nch)
+            const int c = c0 + gl + i * G;
+            x[u][i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (valid && c < c_end)
               x[u][i] = ck >= 0 ? __ldg(H4 + (int64_t)ck * ldh4 + c)
                                 : dequant_chunk(msg.packed + ((size_t)ok << 4), bk, mnk, sck, c);
           }
         } else {
+          const bool load = valid && (MODE != kBwdOwned || ck >= 0);
 #pragma unroll
           for (int i = 0; i < CPL; ++i) {
-            const int c = gl + i * G;
-            if (c < nch) x[u][i] = __ldg(H4 + (int64_t)ck * ldh4 + c);
+            const int c = c0 + gl + i * G;
+            x[u][i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (load && c < c_end) x[u][i] = __ldg(H4 + (int64_t)ck * ldh4 + c);
           }
         }
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
 #pragma unroll
-        for (int i = 0; i < CPL; ++i) {
-          if (gl + i * G < nch) {
-            if (u & 1) fma4(acc1[i], wk[u], x[u][i]);
-            else fma4(acc[i], wk[u], x[u][i]);
-          }
-        }
+        for (int i = 0; i < CPL; ++i) fma4(acc[i], wk[u], x[u][i]);
       }
     }
   }
-#pragma unroll
-  for (int i = 0; i < CPL; ++i) add4(acc[i], acc1[i]);
 }
 
 // acc += dequantised messages of the slots row r owns (backward).
 template <int G, int CPL>
 __device__ __forceinline__ void add_owned(int64_t r, const int64_t* __restrict__ own_ptr,
                                           const int32_t* __restrict__ own_slot,
-                                          const SlotMsgs& msg, int nch, int gl,
+                                          const SlotMsgs& msg, int c0, int c_end, int gl,
                                           float4 (&acc)[CPL]) {
   const int64_t ob = __ldg(own_ptr + r), oe = __ldg(own_ptr + r + 1);
   for (int64_t o = ob; o < oe; ++o) {
@@ -139,41 +130,53 @@ __device__ __forceinline__ void add_owned(int64_t r, const int64_t* __restrict__
     const uint8_t* row = msg.packed + __ldg(msg.off + s);
 #pragma unroll
     for (int i = 0; i < CPL; ++i) {
-      const int c = gl + i * G;
-      if (c < nch) add4(acc[i], dequant_chunk(row, b, m.x, m.y, c));
+      const int c = c0 + gl + i * G;
+      if (c < c_end) add4(acc[i], dequant_chunk(row, b, m.x, m.y, c));
     }
   }
 }
 
+// Writes the group's chunks of row r: fp32 chunks below nch, bf16 chunks
+// below nch_b (zeros past F), both limited to the group's slice [c0, c1).
 template <int G, int CPL>
 __device__ __forceinline__ void store_row(int64_t r, const float4 (&acc)[CPL], int F, int nch,
-                                          int nch_b, int gl, float* __restrict__ M, int64_t ldm,
+                                          int nch_b, int c0, int c1, int gl,
+                                          float* __restrict__ M, int64_t ldm,
                                           __nv_bfloat16* __restrict__ Mb, int64_t ldmb) {
   if (M) {
     float* mrow = M + r * ldm;
 #pragma unroll
     for (int i = 0; i < CPL; ++i) {
-      const int c = gl + i * G;
-      if (c < nch) store_chunk_f32(mrow, c, F, acc[i]);
+      const int c = c0 + gl + i * G;
+      if (c < c1 && c < nch) store_chunk_f32(mrow, c, F, acc[i]);
     }
   }
   if (Mb) {
     __nv_bfloat16* brow = Mb + r * ldmb;
 #pragma unroll
     for (int i = 0; i < CPL; ++i) {
-      const int c = gl + i * G;
-      if (c < nch_b)
+      const int c = c0 + gl + i * G;
+      if (c < c1 && c < nch_b)
         store_chunk_bf16(brow, c, F, c < nch ? acc[i] : make_float4(0.f, 0.f, 0.f, 0.f));
     }
   }
 }
 
+// Feature slices: wide rows are cut into ns slices of cs chunks, each owned
+// by its own group (the slices re-read the row's (col, val) pairs).
+struct Slices {
+  int ns;
+  int cs;
+};
+
+// 4 blocks of 256 per SM (64 registers); the 3-chunk forward with remote rows
+// needs up to 80 and runs 3 blocks.
 template <int G, int CPL, int MODE, int U>
-__global__ void __launch_bounds__(256) spmm_rows_kernel(
+__global__ void __launch_bounds__(256, (MODE == 1 && CPL == 3) ? 3 : 4) spmm_rows_kernel(
     int n, const int64_t* __restrict__ rowptr, const int32_t* __restrict__ col,
     const float* __restrict__ val, const float* __restrict__ H, int64_t ldh, int F,
     SlotMsgs msg, const int64_t* __restrict__ own_ptr, const int32_t* __restrict__ own_slot,
-    RowSplit sp, float* __restrict__ partial, float* __restrict__ M, int64_t ldm,
+    RowSplit sp, Slices sl, float* __restrict__ partial, float* __restrict__ M, int64_t ldm,
     __nv_bfloat16* __restrict__ Mb, int64_t ldmb, int nch_b) {
   const int lane = threadIdx.x & 31;
   const int gl = lane & (G - 1);
@@ -182,43 +185,50 @@ __global__ void __launch_bounds__(256) spmm_rows_kernel(
   const int nch = (F + 3) >> 2;
   const float4* H4 = reinterpret_cast<const float4*>(H);
   const int64_t ldh4 = ldh >> 2;
+  const int slice = (int)(g % sl.ns);
+  const int64_t unit = g / sl.ns;
+  const int c0 = slice * sl.cs, c1 = c0 + sl.cs;
   float4 acc[CPL];
 #pragma unroll
   for (int i = 0; i < CPL; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 
-  if (g < sp.n_pieces) {  // a piece of a long row -> partial row g
-    const int64_t row = __ldg(sp.piece_row + g);
-    const int64_t beg = __ldg(sp.piece_beg + g);
+  if (unit < sp.n_pieces) {  // a piece of a long row -> partial row `unit`
+    const int64_t row = __ldg(sp.piece_row + unit);
+    const int64_t beg = __ldg(sp.piece_beg + unit);
     const int64_t end = min(beg + (int64_t)sp.T, __ldg(rowptr + row + 1));
-    gather_range<G, CPL, MODE, U>(beg, end, row, col, val, H4, ldh4, nch, msg, gl, gmask, acc);
-    float4* prow = reinterpret_cast<float4*>(partial) + g * nch;
+    gather_range<G, CPL, MODE, U>(beg, end, col, val, H4, ldh4, c0, min(c1, nch), msg, gl, gmask, acc);
+    float4* prow = reinterpret_cast<float4*>(partial) + unit * nch;
 #pragma unroll
     for (int i = 0; i < CPL; ++i) {
-      const int c = gl + i * G;
-      if (c < nch) prow[c] = acc[i];
+      const int c = c0 + gl + i * G;
+      if (c < c1 && c < nch) prow[c] = acc[i];
     }
     return;
   }
-  const int64_t r = g - sp.n_pieces;
+  const int64_t r = unit - sp.n_pieces;
   if (r >= n) return;  // uniform across the group
   const int64_t beg = __ldg(rowptr + r), end = __ldg(rowptr + r + 1);
   if (sp.T > 0 && end - beg > sp.T) return;  // a long row: its pieces cover it
-  gather_range<G, CPL, MODE, U>(beg, end, r, col, val, H4, ldh4, nch, msg, gl, gmask, acc);
-  if (MODE == kBwdOwned) add_owned<G, CPL>(r, own_ptr, own_slot, msg, nch, gl, acc);
-  store_row<G, CPL>(r, acc, F, nch, nch_b, gl, M, ldm, Mb, ldmb);
+  gather_range<G, CPL, MODE, U>(beg, end, col, val, H4, ldh4, c0, min(c1, nch), msg, gl, gmask, acc);
+  if (MODE == kBwdOwned) add_owned<G, CPL>(r, own_ptr, own_slot, msg, c0, min(c1, nch), gl, acc);
+  store_row<G, CPL>(r, acc, F, nch, nch_b, c0, c1, gl, M, ldm, Mb, ldmb);
 }
 
-// Long rows: sum of their pieces' partial rows in piece order.
+// Long rows: sum of their pieces' partial rows, 16 pieces at a time and then
+// the block sums, always in piece order (deterministic, short fp32 chains).
 template <int G, int CPL, int MODE>
 __global__ void __launch_bounds__(256) spmm_fixup_kernel(
-    RowSplit sp, const float* __restrict__ partial, int F, SlotMsgs msg,
+    RowSplit sp, Slices sl, const float* __restrict__ partial, int F, SlotMsgs msg,
     const int64_t* __restrict__ own_ptr, const int32_t* __restrict__ own_slot,
     float* __restrict__ M, int64_t ldm, __nv_bfloat16* __restrict__ Mb, int64_t ldmb,
     int nch_b) {
   const int lane = threadIdx.x & 31;
   const int gl = lane & (G - 1);
-  const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / G;
+  const int64_t g = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / G;
+  const int64_t i = g / sl.ns;
   if (i >= sp.n_long) return;
+  const int slice = (int)(g % sl.ns);
+  const int c0 = slice * sl.cs, c1 = c0 + sl.cs;
   const int nch = (F + 3) >> 2;
   const int64_t row = __ldg(sp.long_rows + i);
   const int64_t pb = __ldg(sp.piece_ptr + i), pe = __ldg(sp.piece_ptr + i + 1);
@@ -226,39 +236,104 @@ __global__ void __launch_bounds__(256) spmm_fixup_kernel(
 #pragma unroll
   for (int k = 0; k < CPL; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
   const float4* P4 = reinterpret_cast<const float4*>(partial);
-  for (int64_t p = pb; p < pe; ++p) {
+  for (int64_t p0 = pb; p0 < pe; p0 += 16) {
+    float4 blk[CPL];
 #pragma unroll
-    for (int k = 0; k < CPL; ++k) {
-      const int c = gl + k * G;
-      if (c < nch) add4(acc[k], __ldg(P4 + p * nch + c));
+    for (int k = 0; k < CPL; ++k) blk[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int64_t p1 = min(pe, p0 + 16);
+    for (int64_t p = p0; p < p1; ++p) {
+#pragma unroll
+      for (int k = 0; k < CPL; ++k) {
+        const int c = c0 + gl + k * G;
+        if (c < c1 && c < nch) add4(blk[k], __ldg(P4 + p * nch + c));
+      }
     }
+#pragma unroll
+    for (int k = 0; k < CPL; ++k) add4(acc[k], blk[k]);
   }
-  if (MODE == kBwdOwned) add_owned<G, CPL>(row, own_ptr, own_slot, msg, nch, gl, acc);
-  store_row<G, CPL>(row, acc, F, nch, nch_b, gl, M, ldm, Mb, ldmb);
+  if (MODE == kBwdOwned) add_owned<G, CPL>(row, own_ptr, own_slot, msg, c0, min(c1, nch), gl, acc);
+  store_row<G, CPL>(row, acc, F, nch, nch_b, c0, c1, gl, M, ldm, Mb, ldmb);
 }
 
 // Backward messages: halo partial of slot s over its entries in ascending v,
 // every product and sum rounded to fp32 (start +0), then quantised and packed
-// in registers with row key s.  U entries are loaded ahead of their adds; the
-// adds stay in entry order.
+// in registers with row key s.
+//
+// Blocks [0, n_long) each take one long slot: the block's threads load E
+// entry rows at a time into shared memory (all loads in flight together),
+// then thread t adds chunk t of those rows in entry order.  The remaining
+// blocks give every ordinary slot a group of G lanes that loads U entries
+// ahead of their adds.  Both keep each element's additions in entry order,
+// so the result is the same as one sequential loop.
 template <int G, int CPL, int U>
 __global__ void __launch_bounds__(256) halo_quant_pack_kernel(
     int64_t S, const int64_t* __restrict__ srp, const int32_t* __restrict__ scol,
     const float* __restrict__ sval, const float* __restrict__ Gm, int64_t ldg, int F,
     const uint8_t* __restrict__ slot_bits, const int64_t* __restrict__ slot_off, uint32_t seed,
-    uint8_t* __restrict__ packed, float2* __restrict__ meta) {
+    uint8_t* __restrict__ packed, float2* __restrict__ meta, int n_long,
+    const int32_t* __restrict__ long_slots, int long_len, int E) {
+  constexpr int CPLQ = (G * CPL + 31) / 32;  // chunks per lane when one warp quantises
+  extern __shared__ float4 tile[];
   const int lane = threadIdx.x & 31;
-  const int gl = lane & (G - 1);
-  const int64_t s = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / G;
-  if (s >= S) return;
-  const uint32_t gmask = group_mask(G, lane);
   const int nch = (F + 3) >> 2;
   const float4* G4 = reinterpret_cast<const float4*>(Gm);
   const int64_t ldg4 = ldg >> 2;
+
+  if ((int)blockIdx.x < n_long) {
+    __shared__ int sv[32];
+    __shared__ float sw[32];
+    const int64_t s = __ldg(long_slots + blockIdx.x);
+    const int64_t beg = __ldg(srp + s), end = __ldg(srp + s + 1);
+    const int t = threadIdx.x;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int64_t base = beg; base < end; base += E) {
+      const int cnt = (int)min((int64_t)E, end - base);
+      if (t < cnt) {
+        sv[t] = __ldg(scol + base + t);
+        sw[t] = __ldg(sval + base + t);
+      }
+      __syncthreads();
+      for (int idx = t; idx < cnt * nch; idx += blockDim.x) {
+        const int e = idx / nch, c = idx - e * nch;
+        tile[idx] = __ldg(G4 + (int64_t)sv[e] * ldg4 + c);
+      }
+      __syncthreads();
+      if (t < nch) {
+        for (int e = 0; e < cnt; ++e) {
+          const float4 x = tile[e * nch + t];
+          const float w = sw[e];
+          acc.x = __fadd_rn(acc.x, __fmul_rn(w, x.x));
+          acc.y = __fadd_rn(acc.y, __fmul_rn(w, x.y));
+          acc.z = __fadd_rn(acc.z, __fmul_rn(w, x.z));
+          acc.w = __fadd_rn(acc.w, __fmul_rn(w, x.w));
+        }
+      }
+      __syncthreads();
+    }
+    if (t < nch) tile[t] = acc;
+    __syncthreads();
+    if (t < 32) {
+      float4 v[CPLQ];
+#pragma unroll
+      for (int i = 0; i < CPLQ; ++i) {
+        const int c = lane + 32 * i;
+        v[i] = c < nch ? tile[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      quantize_pack_row<32, CPLQ>(v, F, __ldg(slot_bits + s), row_key(seed, (uint32_t)s),
+                                  packed + __ldg(slot_off + s), meta + s, lane, 0xffffffffu);
+    }
+    return;
+  }
+
+  const int gl = lane & (G - 1);
+  const int64_t s = ((int64_t)(blockIdx.x - n_long) * blockDim.x + threadIdx.x) / G;
+  if (s >= S) return;
+  const int64_t beg = __ldg(srp + s), end = __ldg(srp + s + 1);
+  if (long_len > 0 && end - beg > long_len) return;  // summed by a long-slot block
+  const uint32_t gmask = group_mask(G, lane);
   float4 acc[CPL];
 #pragma unroll
   for (int i = 0; i < CPL; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-  const int64_t beg = __ldg(srp + s), end = __ldg(srp + s + 1);
   for (int64_t base = beg; base < end; base += G) {
     const int64_t e = base + gl;
     int v = 0;
@@ -326,38 +401,40 @@ static gnn_status dispatch_rows(const gnn_csr& csr, const int32_t* colv, const f
   const int nch_b = Mb ? ((F + 15) / 16) * 4 : nch;
   const int need = nch_b > nch ? nch_b : nch;
   const RowSplit sp = row_split_of(csr);
+  // slices of at most 96 chunks (3 per lane) keep every lane's registers low
+  Slices sl{1, need};
+  if (need > 96) {
+    sl.ns = (need + 95) / 96;
+    sl.cs = (need + sl.ns - 1) / sl.ns;
+  }
+  const int cpl = (sl.cs + 31) / 32;
   const int block = 256;
 #define GNN_ROWS(G_, CPL_, U_)                                                                 \
   do {                                                                                         \
-    const int64_t groups = (int64_t)csr.n + sp.n_pieces;                                       \
+    const int64_t groups = ((int64_t)csr.n + sp.n_pieces) * sl.ns;                             \
     const int64_t grid = (groups * G_ + block - 1) / block;                                    \
     spmm_rows_kernel<G_, CPL_, MODE, U_><<<(unsigned)grid, block, 0, st>>>(                    \
-        csr.n, csr.rowptr, colv, csr.val, H, ldh, F, msg, own_ptr, own_slot, sp, partial, M,   \
-        ldm, Mb, ldmb, nch_b);                                                                 \
+        csr.n, csr.rowptr, colv, csr.val, H, ldh, F, msg, own_ptr, own_slot, sp, sl, partial,  \
+        M, ldm, Mb, ldmb, nch_b);                                                              \
     GNN_CHECK_LAUNCH();                                                                        \
     if (sp.n_long > 0) {                                                                       \
-      const int64_t g2 = ((int64_t)sp.n_long * G_ + block - 1) / block;                        \
+      const int64_t g2 = ((int64_t)sp.n_long * sl.ns * G_ + block - 1) / block;                \
       spmm_fixup_kernel<G_, CPL_, MODE><<<(unsigned)g2, block, 0, st>>>(                       \
-          sp, partial, F, msg, own_ptr, own_slot, M, ldm, Mb, ldmb, nch_b);                    \
+          sp, sl, partial, F, msg, own_ptr, own_slot, M, ldm, Mb, ldmb, nch_b);                \
       GNN_CHECK_LAUNCH();                                                                      \
     }                                                                                          \
   } while (0)
-  if (need <= 4) GNN_ROWS(4, 1, 4);
-  else if (need <= 8) GNN_ROWS(8, 1, 4);
-  else if (need <= 16) GNN_ROWS(16, 1, 4);
-  else {
-    switch ((need + 31) / 32) {
-      case 1: GNN_ROWS(32, 1, 4); break;
-      case 2: GNN_ROWS(32, 2, 4); break;
-      case 3: GNN_ROWS(32, 3, 2); break;
-      case 4: GNN_ROWS(32, 4, 2); break;
-      case 5: GNN_ROWS(32, 5, 2); break;
-      case 6: GNN_ROWS(32, 6, 2); break;
-      case 7: GNN_ROWS(32, 7, 2); break;
-      case 8: GNN_ROWS(32, 8, 2); break;
-      default: return fail(GNN_ERR_UNSUPPORTED, "spmm: F=%d exceeds %d", F, kMaxF);
-    }
-  }
+  // entries gathered per round: about 8 float4 loads in flight per lane; the
+  // forward with remote rows carries 4 more values per entry, so it gathers
+  // half as many to stay within 64 registers
+  constexpr int W = MODE == kFwdRemote ? 2 : 1;
+  if (sl.cs <= 4) GNN_ROWS(4, 1, 8 / W);
+  else if (sl.cs <= 8) GNN_ROWS(8, 1, 8 / W);
+  else if (sl.cs <= 16) GNN_ROWS(16, 1, 8 / W);
+  else if (cpl == 1) GNN_ROWS(32, 1, 8 / W);
+  else if (cpl == 2) GNN_ROWS(32, 2, 4 / W);
+  else if (cpl == 3) GNN_ROWS(32, 3, 2);
+  else return fail(GNN_ERR_UNSUPPORTED, "spmm: F=%d exceeds %d", F, kMaxF);
 #undef GNN_ROWS
   return GNN_OK;
 }
@@ -387,13 +464,24 @@ gnn_status launch_halo_quant_pack(const gnn_boundary& b, const float* Gm, int64_
   const int64_t S = b.n_slots;
   if (S == 0) return GNN_OK;
   const int slots = quant_chunk_slots(F);
+  const int nch = (F + 3) / 4;
   const int block = 256;
+  const bool use_long = b.long_slot_len > 0 && b.n_long_slots > 0 && b.long_slots;
+  const int n_long = use_long ? b.n_long_slots : 0;
+  const int long_len = use_long ? b.long_slot_len : 0;
+  // entries staged per round by a long-slot block: at most 32 and 48 KB
+  int E = 3072 / nch;
+  if (E > 32) E = 32;
+  if (E < 1) E = 1;
+  const size_t smem = use_long ? (size_t)E * nch * sizeof(float4) : 0;
+  const size_t smem_q = (size_t)nch * sizeof(float4);
+  const size_t dyn = smem > smem_q ? smem : (use_long ? smem_q : 0);
 #define GNN_HALO(G_, CPL_, U_)                                                                   \
   do {                                                                                           \
-    const int64_t grid = (S * G_ + block - 1) / block;                                           \
-    halo_quant_pack_kernel<G_, CPL_, U_><<<(unsigned)grid, block, 0, st>>>(                      \
+    const int64_t grid = n_long + (S * G_ + block - 1) / block;                                  \
+    halo_quant_pack_kernel<G_, CPL_, U_><<<(unsigned)grid, block, dyn, st>>>(                    \
         S, b.slot_rowptr, b.slot_col, b.slot_val, Gm, ldg, F, b.slot_bits, b.slot_off, seed,     \
-        packed_ws, meta_ws);                                                                     \
+        packed_ws, meta_ws, n_long, b.long_slots, long_len, E);                                  \
   } while (0)
   if (slots <= 32) GNN_HALO(8, 4, 2);
   else {
@@ -473,6 +561,9 @@ static gnn_status check_bnd(const gnn_csr* csr, const gnn_boundary* b, int F, bo
   if (bwd && (!b->own_ptr || (b->n_slots > 0 && (!b->slot_rowptr || !b->own_slot)) ||
               (b->nnz_cut > 0 && (!b->slot_col || !b->slot_val))))
     return fail(GNN_ERR_INVALID_ARG, "%s: boundary backward arrays are NULL", who);
+  if (bwd && b->long_slot_len > 0 &&
+      (b->long_slot_len < 32 || b->n_long_slots < 0 || (b->n_long_slots > 0 && !b->long_slots)))
+    return fail(GNN_ERR_INVALID_ARG, "%s: incomplete long-slot list", who);
   return GNN_OK;
 }
 

@@ -94,6 +94,21 @@ def test_csr_split_plan(built, name, split):
         assert np.array_equal(host(csr.split["piece_beg"])[: len(pieces)], [p[1] for p in pieces])
 
 
+@pytest.mark.parametrize("name,P,T", [("star", 3, 32), ("star", 5, 100), ("planted", 4, 32),
+                                      ("er300", 3, 32)])
+def test_boundary_long_slot_list(built, name, P, T):
+    n, src, dst = GRAPHS[name]
+    csr = gpu_graph(n, src, dst)
+    b = G.gnn_boundary_index(csr, P, G.BitRule([50], [2, 8]), 1, 8)
+    G.gnn_boundary_long_slots(csr, b, T)
+    rp, col, val = O.csr_build(n, src, dst)
+    ob = O.boundary_index(n, rp, col, val, P)
+    want = np.nonzero(np.diff(ob["slot_rowptr"]) > T)[0]
+    assert b.n_long_slots == want.size
+    if want.size:
+        assert np.array_equal(host(b.arrays["long_slots"])[: want.size], want)
+
+
 # ------------------------------------------------------------------ a2: boundary
 BND_CASES = [("er64", 4, [90], [2, 8], 1, 16), ("er300", 7, [25, 50, 75], [1, 2, 4, 8], 1, 37),
              ("planted", 4, [90], [2, 8], 1, 16), ("star", 3, [80], [4, 8], 2, 5),
@@ -211,10 +226,12 @@ def test_spmm_fwd_plain(built, name, F, split):
     assert np.all(mb[:, F:] == 0)
 
 
-def _partitioned_setup(name, P, pct, bits, base, F, seed, split=0):
+def _partitioned_setup(name, P, pct, bits, base, F, seed, split=0, long_slots=0):
     n, src, dst = GRAPHS[name]
     csr = gpu_graph(n, src, dst, split=split)
     b = G.gnn_boundary_index(csr, P, G.BitRule(pct, bits), base, F)
+    if long_slots:
+        G.gnn_boundary_long_slots(csr, b, long_slots)
     rp, col, val = O.csr_build(n, src, dst)
     ob = oracle_boundary(n, rp, col, val, P, pct, bits, base, F)
     return n, csr, b, rp, col, val, ob
@@ -313,8 +330,11 @@ def test_spmm_bwd_plain(built, name, F, split):
 
 @pytest.mark.parametrize("name,P,pct,bits,base,F,split", PART_CASES)
 def test_spmm_bwd_partitioned(built, name, P, pct, bits, base, F, split):
+    """With a split plan the long slots (more than 32 entries) are also summed
+    by whole blocks; the messages must not change."""
     t = __import__("torch")
-    n, csr, b, rp, col, val, ob = _partitioned_setup(name, P, pct, bits, base, F, 0, split)
+    n, csr, b, rp, col, val, ob = _partitioned_setup(name, P, pct, bits, base, F, 0, split,
+                                                     long_slots=32 if split else 0)
     Gm = _features(n, F, 31)
     ld = G.ld_for(F)
     Q = int(ob["slot_off"][-1])

@@ -1,5 +1,6 @@
 """The five synthetic workloads at full size, in the launch configuration
-bench.py times (row-split plan of 256 entries, slot offsets per layer width).
+bench.py times (row-split plan of 128 entries, long-slot list of 128
+entries, slot offsets per layer width).
 
 Per workload: CSR, boundary index, widths and offsets bit-exact against the
 oracle in full; quantised messages (forward and backward) bit-exact on a
@@ -21,7 +22,8 @@ pytestmark = pytest.mark.gpu
 
 G = pytest.importorskip("sparse_aggregation_message_gb300")
 
-SPLIT_LEN = 256
+SPLIT_LEN = 128
+LONG_SLOT_LEN = 128
 N_SAMPLE_ROWS = 2048
 N_SAMPLE_SLOTS = 4096
 
@@ -66,6 +68,7 @@ def test_workload_parity(name):
     assert np.array_equal(host(bnd.slot_val).view(np.uint32), ob["slot_val"].view(np.uint32))
     S = bnd.n_slots
     sb = ob["slot_bits"]
+    G.gnn_boundary_long_slots(csr, bnd, LONG_SLOT_LEN)
 
     # sampled rows: random plus the longest rows (those are split into pieces)
     deg = np.diff(rp)
