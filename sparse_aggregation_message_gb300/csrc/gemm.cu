@@ -32,12 +32,16 @@ constexpr int BK = 64;  // one 128-byte swizzle row of bf16
 constexpr int STAGES = 4;
 constexpr int A_STAGE = BM * BK * 2;           // 16 KB
 constexpr int B_STAGE = 256 * BK * 2;          // 32 KB (N tile up to 256)
+constexpr int OUT_SUB = 32 * 32 * 4;           // one epilogue warp's 32 x 32 fp32 sub-tile
+constexpr int OUT_STAGE = 4 * 2 * OUT_SUB;     // 4 warps, double-buffered: 32 KB
 constexpr int SMEM_BYTES = STAGES * (A_STAGE + B_STAGE) + 1024 /*barriers*/ + 1024 /*align*/;
+constexpr int SMEM_TN_BYTES = SMEM_BYTES + OUT_STAGE;
 constexpr int THREADS = 192;
 
 struct Smem {
   uint8_t* a;
   uint8_t* b;
+  uint8_t* out;  // epilogue staging (gemm_tn only), 1024-byte aligned
   uint64_t* full;
   uint64_t* empty;
   uint64_t* tfull;
@@ -58,6 +62,7 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
   s.tempty = bars + 2 * STAGES + 2;
   s.tmem_base = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 4);
   s.abort_flag = reinterpret_cast<volatile int*>(s.tmem_base + 1);
+  s.out = s.b + STAGES * B_STAGE + 1024;
   return s;
 }
 
@@ -112,7 +117,7 @@ struct TnArgs {
 
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   TnArgs g) {
+                   const __grid_constant__ CUtensorMap tmC, TnArgs g) {
   extern __shared__ uint8_t smem_raw[];
   const Smem s = carve(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -166,37 +171,57 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc::mma_commit(&s.tfull[acc]);
     }
   } else if (warp >= 2) {
-    const int q = warp & 3;  // TMEM lane quarter this warp may read
-    int it = 0;
+    // Each epilogue warp owns 32 accumulator rows (its TMEM lane quarter).
+    // Per 32-column chunk: TMEM -> registers (ReLU) -> a 128-byte-swizzled
+    // 32 x 32 fp32 sub-tile in shared memory -> one TMA store (rows and
+    // columns outside the output are clipped by the tensor map).  Two
+    // staging buffers per warp let a store drain while the next fills.
+    const int q = warp & 3;
+    uint8_t* stage0 = s.out + (warp - 2) * 2 * OUT_SUB;
+    int it = 0, nbuf = 0;
     for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++it) {
       const int m0 = (t % num_m) * BM, n0 = (t / num_m) * BN;
       const int acc = it & 1;
       const uint32_t aph = (it >> 1) & 1;
       if (!tc::mbar_wait(&s.tfull[acc], aph, g.flags, s.abort_flag)) goto done;
       tc::fence_after_sync();
-      const int row = m0 + q * 32 + lane;
-      float* orow = g.out + (int64_t)row * g.ldo;
-      for (int c0 = 0; c0 < BN; c0 += 16) {
-        float v[16];
-        tc::tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + acc * BN + c0, v);
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        float v[32];
+        tc::tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + acc * BN + c0, *reinterpret_cast<float(*)[16]>(v));
+        if (c0 + 16 < BN)
+          tc::tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + acc * BN + c0 + 16,
+                        *reinterpret_cast<float(*)[16]>(v + 16));
+        else {
+#pragma unroll
+          for (int j = 16; j < 32; ++j) v[j] = 0.f;
+        }
+        if (c0 + 32 >= BN) {  // accumulator fully read: hand it back to the MMA warp
+          tc::fence_before_sync();
+          tc::mbar_arrive(&s.tempty[acc]);
+        }
         if (g.relu) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = fmaxf(v[j], 0.f);
+          for (int j = 0; j < 32; ++j) v[j] = fmaxf(v[j], 0.f);
         }
-        if (row < g.M) {
+        uint8_t* stage = stage0 + nbuf * OUT_SUB;
+        if (lane == 0) tc::bulk_wait_read<1>();  // this buffer's previous store has read it
+        __syncwarp();
 #pragma unroll
-          for (int j = 0; j < 16; j += 4) {
-            const int col = n0 + c0 + j;
-            if (col < g.n_store)
-              *reinterpret_cast<float4*>(orow + col) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-          }
+        for (int k = 0; k < 8; ++k)
+          *reinterpret_cast<float4*>(stage + lane * 128 + ((k ^ (lane & 7)) << 4)) =
+              make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+        tc::fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tc::tma_store_2d(&tmC, stage, n0 + c0, m0 + q * 32);
+          tc::bulk_commit();
         }
+        nbuf ^= 1;
       }
-      tc::fence_before_sync();
-      tc::mbar_arrive(&s.tempty[acc]);
     }
   }
 done:
+  if (warp >= 2 && lane == 0) tc::bulk_wait_all();  // stores finish before the block exits
   teardown(s, BN, tmem);
 }
 
@@ -390,6 +415,24 @@ static gnn_status make_tmap(CUtensorMap* map, const void* base, uint64_t inner, 
   return GNN_OK;
 }
 
+// fp32 output map for the epilogue's TMA stores (128-byte swizzle, 32 x 32 box).
+static gnn_status make_tmap_f32(CUtensorMap* map, void* base, uint64_t inner, uint64_t outer,
+                                uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  if (((uintptr_t)base & 15) || (row_bytes & 15))
+    return fail(GNN_ERR_INVALID_ARG, "dense transform: output needs 16-byte aligned rows");
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (!encode) return fail(GNN_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, es,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(GNN_ERR_CUDA, "cuTensorMapEncodeTiled (output) failed (%d)", (int)r);
+  return GNN_OK;
+}
+
 static int sm_count() {
   static int n = 0;
   if (n == 0) {
@@ -404,7 +447,7 @@ static int sm_count() {
 static gnn_status ensure_smem_attr() {
   static bool done = false;
   if (!done) {
-    GNN_CUDA(cudaFuncSetAttribute(gemm_tn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES));
+    GNN_CUDA(cudaFuncSetAttribute(gemm_tn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_TN_BYTES));
     GNN_CUDA(cudaFuncSetAttribute(gemm_mn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES));
     done = true;
   }
@@ -418,17 +461,21 @@ gnn_status launch_gemm_tn(const uint16_t* A, int64_t lda, const uint16_t* B, int
   if (N < 1 || K < 1) return fail(GNN_ERR_INVALID_ARG, "dense transform: empty N or K");
   gnn_status s = ensure_smem_attr();
   if (s != GNN_OK) return s;
+  // N tile: a multiple of 16 (MMA shape); with several tiles a multiple of 32,
+  // so the epilogue's 32-column stores never reach into the next tile
   const int num_n = (N + 255) / 256;
-  const int BN = ((N + num_n - 1) / num_n + 15) / 16 * 16;
-  CUtensorMap ta, tb;
+  const int BN = num_n == 1 ? (N + 15) / 16 * 16 : ((N + num_n - 1) / num_n + 31) / 32 * 32;
+  CUtensorMap ta, tb, tcm;
   if ((s = make_tmap(&ta, A, (uint64_t)lda, (uint64_t)M, (uint64_t)lda * 2, BK, BM)) != GNN_OK) return s;
   if ((s = make_tmap(&tb, B, (uint64_t)ldb, (uint64_t)N, (uint64_t)ldb * 2, BK, (uint32_t)BN)) != GNN_OK) return s;
+  if ((s = make_tmap_f32(&tcm, out, (uint64_t)n_store, (uint64_t)M, (uint64_t)ldo * 4, 32, 32)) != GNN_OK)
+    return s;
   unsigned* flags = device_flags();
   if (!flags) return fail(GNN_ERR_CUDA, "device flag word unavailable");
   TnArgs g{M, N, K, BN, n_store, out, ldo, relu, flags};
   const int tiles = ((M + BM - 1) / BM) * num_n;
   const int grid = tiles < sm_count() ? tiles : sm_count();
-  gemm_tn_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(ta, tb, g);
+  gemm_tn_kernel<<<grid, THREADS, SMEM_TN_BYTES, st>>>(ta, tb, tcm, g);
   GNN_CHECK_LAUNCH();
   return GNN_OK;
 }

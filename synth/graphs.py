@@ -192,17 +192,18 @@ def rmat_edges(scale: int, draws: int, abcd, seed: int, blocks: int = 16):
     done = 0
     while done < draws:
         k = min(chunk, draws - done)
-        s = np.zeros(k, np.int64)
-        d = np.zeros(k, np.int64)
-        for level in range(scale):
+        s = np.zeros(k, np.uint32)
+        d = np.zeros(k, np.uint32)
+        for _ in range(scale):
+            # quadrant 0..3 = a, b, c, d: source bit q >> 1, destination bit q & 1
             r = np.frombuffer(rng.bytes(2 * k), dtype=np.uint16)
-            sbit = r >= tab
-            dbit = ((r >= ta) & (r < tab)) | (r >= tabc)
-            sh = scale - 1 - level
-            s |= sbit.astype(np.int64) << sh
-            d |= dbit.astype(np.int64) << sh
+            q = (r >= ta).view(np.uint8) + (r >= tab).view(np.uint8) + (r >= tabc).view(np.uint8)
+            s <<= 1
+            d <<= 1
+            s |= q >> 1
+            d |= q & 1
         keep = s != d
-        keys.append(_sorted_distinct(_keys(s[keep], d[keep], n)))
+        keys.append(_sorted_distinct(_keys(s[keep].astype(np.int64), d[keep].astype(np.int64), n)))
         done += k
     keys = _sorted_distinct(np.concatenate(keys))
     u, v = _split_keys(keys, n)
