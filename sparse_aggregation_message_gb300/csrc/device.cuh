@@ -27,11 +27,6 @@ __device__ __forceinline__ uint32_t row_key(uint32_t seed, uint32_t r) {
   return fmix32(seed ^ fmix32(r));
 }
 
-// Stochastic-rounding offset u = (hash32 >> 8) * 2^-24, exact in fp32.
-__device__ __forceinline__ float sr_offset(uint32_t key, uint32_t j) {
-  return __fmul_rn(static_cast<float>(fmix32(key ^ j) >> 8), 5.9604644775390625e-08f);
-}
-
 __device__ __forceinline__ uint32_t group_mask(int G, int lane) {
   return G == 32 ? 0xffffffffu : (((1u << G) - 1u) << (lane & ~(G - 1)));
 }
@@ -44,9 +39,50 @@ __device__ __forceinline__ uint32_t rowbytes_dev(int b, int F) {
   return b == 32 ? 16u * ((4u * F + 15u) / 16u) : 16u * ((uint32_t)(F * b + 127) / 128u);
 }
 
+// Codes of one quantised row at compile-time width B, packed into 32-bit
+// words: the 8/B chunks of a word sit on consecutive lanes of the group and
+// are OR-ed together with shuffles; zero words pad the row to rowbytes(B, F).
+// u_j * 2^24 is an integer below 2^24, so RN(t + u) is formed by one fused
+// multiply-add of that integer by 2^-24 (exact) and t.
+template <int G, int CPL, int B>
+__device__ __forceinline__ void pack_codes(const float4 (&v)[CPL], int F, float mn, float scale,
+                                           bool flat, uint32_t key, uint32_t* __restrict__ words,
+                                           int gl, uint32_t gmask) {
+  constexpr uint32_t TOP = (1u << B) - 1u;
+  constexpr int PER_WORD = 8 / B;  // chunks per 32-bit word
+  const int nch = (F + 3) >> 2;
+  const int slots = (int)(rowbytes_dev(B, F) * 2u) / B;  // chunk slots of the padded row
+#pragma unroll
+  for (int i = 0; i < CPL; ++i) {
+    const int c = gl + i * G;
+    uint32_t part = 0;
+    if (c < nch && !flat) {
+      const bool full = 4 * c + 3 < F;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int j = 4 * c + k;
+        if (full || j < F) {
+          const float t = __fdiv_rn(__fsub_rn(elem(v[i], k), mn), scale);
+          const float m = static_cast<float>(fmix32(key ^ (uint32_t)j) >> 8);
+          // floor(t + u) >= 0 and below 2^24: round down while converting
+          const uint32_t q = min(__float2uint_rd(__fmaf_rn(m, 5.9604644775390625e-08f, t)), TOP);
+          part |= q << (k * B);
+        }
+      }
+    }
+    if (PER_WORD > 1) {
+      part <<= (c % PER_WORD) * 4 * B;
+#pragma unroll
+      for (int o = 1; o < PER_WORD; o <<= 1) part |= __shfl_xor_sync(gmask, part, o);
+    }
+    if (c < slots && (c % PER_WORD) == 0) words[(c * B) >> 3] = part;
+  }
+}
+
 // Quantises the group's row held in v[] (elements >= F ignored) with width b
 // and row key `key`, writes the packed row at `out` (16-byte aligned) and
-// (mn, scale) at meta (lane 0 of the group).  All lanes of the group must call.
+// (mn, scale) at meta (lane 0 of the group).  All lanes of the group must
+// call.  Groups of at least 8 lanes (one 1-bit word spans 8 chunks).
 template <int G, int CPL>
 __device__ __forceinline__ void quantize_pack_row(const float4 (&v)[CPL], int F, int b,
                                                   uint32_t key, uint8_t* __restrict__ out,
@@ -92,34 +128,12 @@ __device__ __forceinline__ void quantize_pack_row(const float4 (&v)[CPL], int F,
   const float top = static_cast<float>((1u << b) - 1u);  // exact: 2^b - 1 < 2^24
   const bool flat = !(mx > mn);
   const float scale = flat ? 0.f : __fdiv_rn(__fsub_rn(mx, mn), top);
-  // chunk slots covered by the padded row: rowbytes*2/b chunks
-  const int slots = (int)(rowbytes_dev(b, F) * 2u) / b;
-  const int per_word = 8 / b;  // chunks per 32-bit word
   uint32_t* words = reinterpret_cast<uint32_t*>(out);
-  const uint32_t topi = (1u << b) - 1u;
-#pragma unroll
-  for (int i = 0; i < CPL; ++i) {
-    const int c = gl + i * G;
-    uint32_t part = 0;
-    if (c < nch && !flat) {
-      // floor(t + u) >= 0 and below 2^24, so rounding down while converting
-      // to an integer gives the same code as floorf followed by a conversion
-      const bool full = 4 * c + 3 < F;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int j = 4 * c + k;
-        if (full || j < F) {
-          const float t = __fdiv_rn(__fsub_rn(elem(v[i], k), mn), scale);
-          const float u = sr_offset(key, (uint32_t)j);
-          const uint32_t q = min(__float2uint_rd(__fadd_rn(t, u)), topi);
-          part |= q << (k * b);
-        }
-      }
-    }
-    // the per_word chunks of one word sit on consecutive lanes of the group
-    part <<= (c % per_word) * 4 * b;
-    for (int o = 1; o < per_word; o <<= 1) part |= __shfl_xor_sync(gmask, part, o);
-    if (c < slots && (c % per_word) == 0) words[(c * b) >> 3] = part;
+  switch (b) {
+    case 1: pack_codes<G, CPL, 1>(v, F, mn, scale, flat, key, words, gl, gmask); break;
+    case 2: pack_codes<G, CPL, 2>(v, F, mn, scale, flat, key, words, gl, gmask); break;
+    case 4: pack_codes<G, CPL, 4>(v, F, mn, scale, flat, key, words, gl, gmask); break;
+    default: pack_codes<G, CPL, 8>(v, F, mn, scale, flat, key, words, gl, gmask); break;
   }
   if (gl == 0) *meta = make_float2(mn, scale);
 }
