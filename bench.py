@@ -102,6 +102,23 @@ def committed_traffic():
     return int(m_b.group(1)) if h == m_h.group(1) else None
 
 
+def max_over_ranks(value, world, device="cpu"):
+    """The slowest rank's value (every rank gets it); identity for one rank."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(bytes_per_rank, world, ms):
+    """GB/s of the whole job: every replica moves bytes_per_rank in ms."""
+    return bytes_per_rank * world / (ms * 1e-3) / 1e9
+
+
 # --------------------------------------------------------------- clocks
 class ClockSampler:
     def __init__(self, index=0):
@@ -195,7 +212,8 @@ def run_gpu(args, rank, world, local_rank):
     W = [torch.from_numpy(make_weight_bf16(dims[l], dims[l + 1], wl.seed, l).view(np.int16)).to(dev)
          for l in range(L)]
     dW = [torch.empty((dims[l], dims[l + 1]), device=dev) for l in range(L)]
-    dH = [torch.empty((n, ld[l]), device=dev) for l in range(L + 1)]
+    # gradients w.r.t. each layer's input; the first layer's is never formed
+    dH = [None] + [torch.empty((n, ld[l]), device=dev) for l in range(1, L + 1)]
     dH[L].copy_(torch.randn((n, ld[L]), generator=g, device=dev))
     # workspaces sized for the largest layer
     ws_layer = max(G.gnn_layer_workspace(csr, dims[l], dims[l + 1]) for l in range(L))
@@ -502,15 +520,9 @@ def main():
         return
 
     r = run_gpu(args, rank, world, local_rank)
-    ms = r["ms"]
-    if world > 1:
-        import torch
-        import torch.distributed as dist
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(r["ms"], world, "cuda")
     hbm, bf16, bf16_sus, peak_src = load_peaks()
-    gbs = r["total_bytes"] * world / (ms * 1e-3) / 1e9
+    gbs = whole_job_rate(r["total_bytes"], world, ms)
     per = r["per"]
 
     def rate(k):
@@ -550,8 +562,9 @@ def main():
     }
     if r["e2e"]:
         e = r["e2e"]
-        line["e2e"] = {"value": r["total_bytes"] * world / (e["ms"] * 1e-3) / 1e9, "unit": UNIT,
-                       "ms_per_step": e["ms"], "h2d_bytes_per_step": e["h2d"],
+        e_ms = max_over_ranks(e["ms"], world, "cuda")
+        line["e2e"] = {"value": whole_job_rate(r["total_bytes"], world, e_ms), "unit": UNIT,
+                       "ms_per_step": e_ms, "h2d_bytes_per_step": e["h2d"],
                        "d2h_bytes_per_step": e["d2h"]}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cb = OracleBaseline(args.workload).sample(args.cpu_budget)
