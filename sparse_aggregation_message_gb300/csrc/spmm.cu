@@ -169,10 +169,22 @@ struct Slices {
   int cs;
 };
 
-// 4 blocks of 256 per SM (64 registers); the 3-chunk forward with remote rows
-// needs up to 80 and runs 3 blocks.
+// Threads per block of the rows kernel.  Small blocks free their slot as soon
+// as their few rows finish, which keeps more warps resident when row lengths
+// vary.
+#ifndef GNN_ROWS_BLOCK
+#define GNN_ROWS_BLOCK 64
+#endif
+// Widest feature slice a group covers (in 16-byte chunks).
+#ifndef GNN_SLICE_CHUNKS
+#define GNN_SLICE_CHUNKS 96
+#endif
+
+// 1024 resident threads per SM (64 registers each); the 3-chunk forward with
+// remote rows needs up to 80 and keeps 768.
 template <int G, int CPL, int MODE, int U>
-__global__ void __launch_bounds__(256, (MODE == 1 && CPL == 3) ? 3 : 4) spmm_rows_kernel(
+__global__ void __launch_bounds__(GNN_ROWS_BLOCK, ((MODE == 1 && CPL == 3) ? 768 : 1024) / GNN_ROWS_BLOCK)
+    spmm_rows_kernel(
     int n, const int64_t* __restrict__ rowptr, const int32_t* __restrict__ col,
     const float* __restrict__ val, const float* __restrict__ H, int64_t ldh, int F,
     SlotMsgs msg, const int64_t* __restrict__ own_ptr, const int32_t* __restrict__ own_slot,
@@ -401,14 +413,14 @@ static gnn_status dispatch_rows(const gnn_csr& csr, const int32_t* colv, const f
   const int nch_b = Mb ? ((F + 15) / 16) * 4 : nch;
   const int need = nch_b > nch ? nch_b : nch;
   const RowSplit sp = row_split_of(csr);
-  // slices of at most 96 chunks (3 per lane) keep every lane's registers low
+  // feature slices of at most 96 chunks (3 per lane) keep every lane's registers low
   Slices sl{1, need};
-  if (need > 96) {
-    sl.ns = (need + 95) / 96;
+  if (need > GNN_SLICE_CHUNKS) {
+    sl.ns = (need + GNN_SLICE_CHUNKS - 1) / GNN_SLICE_CHUNKS;
     sl.cs = (need + sl.ns - 1) / sl.ns;
   }
   const int cpl = (sl.cs + 31) / 32;
-  const int block = 256;
+  const int block = GNN_ROWS_BLOCK;
 #define GNN_ROWS(G_, CPL_, U_)                                                                 \
   do {                                                                                         \
     const int64_t groups = ((int64_t)csr.n + sp.n_pieces) * sl.ns;                             \
