@@ -145,7 +145,11 @@ typedef struct gnn_boundary {
   int64_t* part_start;  /* [P+1]                                               */
   int64_t* send_start;  /* [P+1] first slot received by partition q            */
   int32_t* slot_node;   /* [S] u of slot s                                     */
-  int32_t* col_remap;   /* [nnz] col[e] if local, else ~s of (part(row), col)  */
+  int32_t* col_remap;   /* [nnz] each row's entries, local sources first (their
+                         * ids, in CSR order), then remote ones as ~s of the
+                         * slot (part(row), col), in CSR order                 */
+  float* val_remap;     /* [nnz] the GCN weights in the same order             */
+  int32_t* local_cnt;   /* [n] local entries at the start of each row          */
   int64_t* slot_rowptr; /* [S+1] backward entries of slot s ...                */
   int32_t* slot_col;    /* [nnz_cut] ... the rows v of q that aggregate u,     */
   float* slot_val;      /* [nnz_cut] ... ascending, with their weights A_vu    */

@@ -123,7 +123,9 @@ def part_of(x, starts):
 
 def boundary_index(n, rowptr, col, val, P):
     """Slots are the pairs (q, u) where a node of partition q aggregates u and
-    u is not in q; ordered by q then u.  Returns a dict of the index arrays."""
+    u is not in q; ordered by q then u.  Each row's entries are listed with
+    local sources first (their ids) and remote ones after (~slot), both in CSR
+    order, with the weights in the same order.  Returns a dict of the arrays."""
     starts = partition_starts(n, P)
     rows = csr_rows(rowptr)
     col64 = col.astype(np.int64)
@@ -136,8 +138,14 @@ def boundary_index(n, rowptr, col, val, P):
     slot_node = (slot_keys % n).astype(np.int32)
     send_start = np.searchsorted(slot_q, np.arange(P + 1), side="left").astype(np.int64)
     s_of_edge = np.searchsorted(slot_keys, pv[cut] * n + col64[cut])
-    col_remap = col.astype(np.int32).copy()
-    col_remap[cut] = ~s_of_edge.astype(np.int32)
+    remap_csr = col.astype(np.int32).copy()
+    remap_csr[cut] = ~s_of_edge.astype(np.int32)
+    # each row's entries: local sources first, then remote slots, each group
+    # in CSR order (a stable partition of the row)
+    order = np.lexsort((np.arange(rows.size), cut, rows))
+    col_remap = remap_csr[order]
+    val_remap = val[order]
+    local_cnt = np.bincount(rows[~cut], minlength=n).astype(np.int32)
     ev = rows[cut]
     order = np.lexsort((ev, s_of_edge))
     slot_col = ev[order].astype(np.int32)
@@ -149,6 +157,7 @@ def boundary_index(n, rowptr, col, val, P):
     own_ptr[1:] = np.cumsum(np.bincount(slot_node, minlength=n))
     return dict(P=P, n=n, n_slots=S, nnz_cut=int(cut.sum()), part_start=starts,
                 send_start=send_start, slot_node=slot_node, col_remap=col_remap,
+                val_remap=val_remap, local_cnt=local_cnt,
                 slot_rowptr=slot_rowptr, slot_col=slot_col, slot_val=slot_val,
                 own_ptr=own_ptr, own_slot=own_slot)
 
@@ -328,7 +337,7 @@ def spmm_fwd(n, rowptr, col, val, H, F, bnd=None, slot_bits=None, seed=0, rows=N
     lens = rowptr[rows + 1] - rowptr[rows]
     e = _expand_ranges(rowptr[rows], lens)
     out_row = np.repeat(np.arange(rows.size), lens)
-    w = val[e].astype(np.float64)
+    w = (val if bnd is None else bnd["val_remap"])[e].astype(np.float64)
     if bnd is None:
         src_id = col[e].astype(np.int64)
         uniq, inv = np.unique(src_id, return_inverse=True)
@@ -399,7 +408,7 @@ def spmm_bwd(n, rowptr, col, val, G, F, bnd=None, slot_bits=None, seed=0, rows=N
     loc = cr >= 0
     src = cr[loc].astype(np.int64)
     uniq, inv = np.unique(src, return_inverse=True)
-    A = sp.csr_matrix((val[e][loc].astype(np.float64), (out_row[loc], inv)),
+    A = sp.csr_matrix((bnd["val_remap"][e][loc].astype(np.float64), (out_row[loc], inv)),
                       shape=(rows.size, uniq.size))
     Xl = np.asarray(G)[uniq, :F].astype(np.float64)
     dH = A @ Xl

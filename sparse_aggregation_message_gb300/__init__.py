@@ -119,8 +119,9 @@ class Boundary:
         b = GnnBoundary()
         b.P, b.n, b.n_slots, b.nnz_cut = self.P, self.n, self.n_slots, self.nnz_cut
         b.F = self.F if F is None else F
-        for k in ("part_start", "send_start", "slot_node", "col_remap", "slot_rowptr", "slot_col",
-                  "slot_val", "own_ptr", "own_slot", "node_bits", "slot_bits"):
+        for k in ("part_start", "send_start", "slot_node", "col_remap", "val_remap", "local_cnt",
+                  "slot_rowptr", "slot_col", "slot_val", "own_ptr", "own_slot", "node_bits",
+                  "slot_bits"):
             setattr(b, k, _ptr(a[k]))
         b.slot_off = _ptr(a["slot_off"] if slot_off is None else slot_off)
         b.long_slot_len, b.n_long_slots = self.long_slot_len, self.n_long_slots
@@ -209,7 +210,8 @@ def gnn_boundary_index(csr: Csr, P: int, rule: BitRule, base_bits: int, F: int,
         return torch.empty(max(k, 1), dtype=dt, device=dev)
 
     a = dict(part_start=e(P + 1, i64), send_start=e(P + 1, i64), slot_node=e(S, i32),
-             col_remap=e(csr.nnz, i32), slot_rowptr=e(S + 1, i64), slot_col=e(nc, i32),
+             col_remap=e(csr.nnz, i32), val_remap=e(csr.nnz, f32), local_cnt=e(n, i32),
+             slot_rowptr=e(S + 1, i64), slot_col=e(nc, i32),
              slot_val=e(nc, f32), own_ptr=e(n + 1, i64), own_slot=e(S, i32), node_bits=e(n, u8),
              slot_bits=e(S, u8), slot_off=e(S + 1, i64))
     b = Boundary(P=P, n=n, n_slots=S, nnz_cut=nc, F=F, arrays=a)
@@ -217,7 +219,7 @@ def gnn_boundary_index(csr: Csr, P: int, rule: BitRule, base_bits: int, F: int,
     call("gnn_boundary_index", ctypes.byref(c), ctypes.byref(rule.to_c()), base_bits, F,
          ctypes.byref(cb), _ptr(ws), ws.numel(), st)
     sizes = dict(part_start=P + 1, send_start=P + 1, slot_node=S, col_remap=csr.nnz,
-                 slot_rowptr=S + 1, slot_col=nc, slot_val=nc, own_ptr=n + 1, own_slot=S,
+                 val_remap=csr.nnz, local_cnt=n, slot_rowptr=S + 1, slot_col=nc, slot_val=nc, own_ptr=n + 1, own_slot=S,
                  node_bits=n, slot_bits=S, slot_off=S + 1)
     b.arrays = {k: v[:sizes[k]] for k, v in a.items()}
     return b

@@ -33,7 +33,8 @@ class GnnBitRule(ctypes.Structure):
 class GnnBoundary(ctypes.Structure):
     _fields_ = [("P", c_i32), ("n", c_i32), ("n_slots", c_i64), ("nnz_cut", c_i64), ("F", c_i32),
                 ("reserved", c_i32), ("part_start", c_vp), ("send_start", c_vp),
-                ("slot_node", c_vp), ("col_remap", c_vp), ("slot_rowptr", c_vp),
+                ("slot_node", c_vp), ("col_remap", c_vp), ("val_remap", c_vp), ("local_cnt", c_vp),
+                ("slot_rowptr", c_vp),
                 ("slot_col", c_vp), ("slot_val", c_vp), ("own_ptr", c_vp), ("own_slot", c_vp),
                 ("node_bits", c_vp), ("slot_bits", c_vp), ("slot_off", c_vp),
                 ("long_slot_len", c_i32), ("n_long_slots", c_i32), ("long_slots", c_vp)]

@@ -181,6 +181,28 @@ __global__ void cut_remap_kernel(int n, const int64_t* __restrict__ rowptr,
   v2[i] = val[e];
 }
 
+// Row v's entries reordered: local sources first, then remote slots, each
+// group keeping CSR order; weights follow their entries.
+__global__ void reorder_rows_kernel(int n, const int64_t* __restrict__ rowptr,
+                                    const int32_t* __restrict__ remap_csr,
+                                    const float* __restrict__ val, int32_t* __restrict__ col_remap,
+                                    float* __restrict__ val_remap, int32_t* __restrict__ local_cnt) {
+  const int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (v >= n) return;
+  const int64_t beg = rowptr[v], end = rowptr[v + 1];
+  int64_t cnt = 0;
+  for (int64_t e = beg; e < end; ++e) cnt += remap_csr[e] >= 0;
+  local_cnt[v] = (int32_t)cnt;
+  int64_t li = beg, ri = beg + cnt;
+  for (int64_t e = beg; e < end; ++e) {
+    const int32_t c = remap_csr[e];
+    const float w = val[e];
+    const int64_t at = c >= 0 ? li++ : ri++;
+    col_remap[at] = c;
+    val_remap[at] = w;
+  }
+}
+
 __global__ void slot_csr_kernel(const uint64_t* __restrict__ key2, int64_t nc, int shift,
                                 int32_t* __restrict__ slot_col) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -577,8 +599,9 @@ extern "C" gnn_status gnn_boundary_index(const gnn_csr* csr, const gnn_bit_rule*
   if ((s = check_rule(rule, base_bits)) != GNN_OK) return s;
   GNN_REQUIRE(out && ws && F >= 1, "gnn_boundary_index: bad arguments");
   GNN_REQUIRE(out->P >= 1, "gnn_boundary_index: out->P must be set");
-  GNN_REQUIRE(out->part_start && out->send_start && out->col_remap && out->own_ptr &&
-                  out->node_bits && out->slot_off && out->slot_rowptr,
+  GNN_REQUIRE(out->part_start && out->send_start && out->col_remap && out->val_remap &&
+                  out->local_cnt && out->own_ptr && out->node_bits && out->slot_off &&
+                  out->slot_rowptr,
               "gnn_boundary_index: NULL output array");
   GNN_REQUIRE(out->n_slots == 0 || (out->slot_node && out->own_slot && out->slot_bits),
               "gnn_boundary_index: NULL slot array");
@@ -600,13 +623,15 @@ extern "C" gnn_status gnn_boundary_index(const gnn_csr* csr, const gnn_bit_rule*
   part_start_kernel<<<GRID1(P + 1), 0, st>>>(n, P, out->part_start);
   send_start_kernel<<<GRID1(P + 1), 0, st>>>(w.k2, S, shift, P, out->send_start);
   if (S > 0) slots_decode_kernel<<<GRID1(S), 0, st>>>(w.k2, S, shift, out->slot_node);
-  if (csr->nnz > 0) copy_col_kernel<<<GRID1(csr->nnz), 0, st>>>(csr->col, csr->nnz, out->col_remap);
+  // col_remap in CSR order goes to a temporary first (w.v2 is free here)
+  int32_t* remap_csr = reinterpret_cast<int32_t*>(w.v2);
+  if (csr->nnz > 0) copy_col_kernel<<<GRID1(csr->nnz), 0, st>>>(csr->col, csr->nnz, remap_csr);
   GNN_CHECK_LAUNCH();
   const int shiftS = bits_for((uint64_t)(S > 0 ? S : 1));
   if (nc > 0) {
     // backward entries keyed (s, v): slot s's rows v in ascending order
     cut_remap_kernel<<<GRID1(nc), 0, st>>>(n, csr->rowptr, csr->val, w.k0, w.eidx, nc, w.k2, S,
-                                          shift, out->col_remap, w.k1, w.v1);
+                                          shift, remap_csr, w.k1, w.v1);
     GNN_CHECK_LAUNCH();
     size_t tb = w.temp_bytes;
     GNN_CUDA(cub::DeviceRadixSort::SortPairs(w.temp, tb, w.k1, w.k3, w.v1, out->slot_val, nc, 0,
@@ -615,6 +640,9 @@ extern "C" gnn_status gnn_boundary_index(const gnn_csr* csr, const gnn_bit_rule*
     GNN_CHECK_LAUNCH();
   }
   bound_ptr_kernel<<<GRID1(S + 1), 0, st>>>(w.k3, nc, shift, S, out->slot_rowptr);
+  GNN_CHECK_LAUNCH();
+  reorder_rows_kernel<<<GRID1(n), 0, st>>>(n, csr->rowptr, remap_csr, csr->val, out->col_remap,
+                                           out->val_remap, out->local_cnt);
   GNN_CHECK_LAUNCH();
   // owner lists keyed (u, s)
   if (S > 0) {

@@ -45,13 +45,12 @@ struct RowSplit {
   const int64_t* piece_beg;
 };
 
-// acc += sum over entries [beg, end) of val * x, x = H[col] or the remote
-// slot's dequantised message (kFwdRemote); remote entries are skipped in the
-// backward (their contribution arrives as the owner's message).  The group
-// covers chunks c0 + gl + i*G (i < CPL) below c_end.  One accumulator per
-// chunk; U entries are gathered before they are added, so U*CPL 16-byte loads
-// per lane are in flight.
-template <int G, int CPL, int MODE, int U>
+// acc += sum over entries [beg, end) of val * x.  Local entries gather H[col];
+// with REMOTE, every entry is a remote slot (~s) whose dequantised message is
+// read from the packed buffer.  The group covers chunks c0 + gl + i*G (i <
+// CPL) below c_end.  One accumulator per chunk; U entries are gathered before
+// they are added, so U*CPL 16-byte loads per lane are in flight.
+template <int G, int CPL, bool REMOTE, int U>
 __device__ __forceinline__ void gather_range(int64_t beg, int64_t end, const int32_t* __restrict__ col,
                                              const float* __restrict__ val,
                                              const float4* __restrict__ H4, int64_t ldh4, int c0,
@@ -67,7 +66,7 @@ __device__ __forceinline__ void gather_range(int64_t beg, int64_t end, const int
     if (e < end) {
       cc = __ldg(col + e);
       w = __ldg(val + e);
-      if (MODE == kFwdRemote && cc < 0) {
+      if (REMOTE) {
         const int s = ~cc;
         sb = __ldg(msg.bits + s);
         so16 = (uint32_t)(__ldg(msg.off + s) >> 4);
@@ -82,9 +81,8 @@ __device__ __forceinline__ void gather_range(int64_t beg, int64_t end, const int
       for (int u = 0; u < U; ++u) {
         const bool valid = k + u < cnt;
         const int src = valid ? k + u : k;
-        const int ck = __shfl_sync(gmask, cc, src, G);
         wk[u] = valid ? __shfl_sync(gmask, w, src, G) : 0.f;
-        if (MODE == kFwdRemote) {
+        if (REMOTE) {
           const int bk = __shfl_sync(gmask, sb, src, G);
           const uint32_t ok = __shfl_sync(gmask, so16, src, G);
           const float mnk = __shfl_sync(gmask, sm.x, src, G);
@@ -94,16 +92,15 @@ __device__ __forceinline__ void gather_range(int64_t beg, int64_t end, const int
             const int c = c0 + gl + i * G;
             x[u][i] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (valid && c < c_end)
-              x[u][i] = ck >= 0 ? __ldg(H4 + (int64_t)ck * ldh4 + c)
-                                : dequant_chunk(msg.packed + ((size_t)ok << 4), bk, mnk, sck, c);
+              x[u][i] = dequant_chunk(msg.packed + ((size_t)ok << 4), bk, mnk, sck, c);
           }
         } else {
-          const bool load = valid && (MODE != kBwdOwned || ck >= 0);
+          const int ck = __shfl_sync(gmask, cc, src, G);
 #pragma unroll
           for (int i = 0; i < CPL; ++i) {
             const int c = c0 + gl + i * G;
             x[u][i] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (load && c < c_end) x[u][i] = __ldg(H4 + (int64_t)ck * ldh4 + c);
+            if (valid && c < c_end) x[u][i] = __ldg(H4 + (int64_t)ck * ldh4 + c);
           }
         }
       }
@@ -175,6 +172,27 @@ struct Slices {
 #ifndef GNN_ROWS_BLOCK
 #define GNN_ROWS_BLOCK 64
 #endif
+// Entries gathered per round for lanes holding 1 or 2 chunks: local (U; the
+// forward with remote rows has its own, measured best) and remote (UR)
+// entries; the 3-chunk layout gathers 2 of either.
+#ifndef GNN_U1
+#define GNN_U1 6
+#endif
+#ifndef GNN_U2
+#define GNN_U2 3
+#endif
+#ifndef GNN_U1_FWD
+#define GNN_U1_FWD 8
+#endif
+#ifndef GNN_U2_FWD
+#define GNN_U2_FWD 4
+#endif
+#ifndef GNN_UR1
+#define GNN_UR1 4
+#endif
+#ifndef GNN_UR2
+#define GNN_UR2 2
+#endif
 // Widest feature slice a group covers (in 16-byte chunks).
 #ifndef GNN_SLICE_CHUNKS
 #define GNN_SLICE_CHUNKS 96
@@ -182,11 +200,12 @@ struct Slices {
 
 // 1024 resident threads per SM (64 registers each); the 3-chunk forward with
 // remote rows needs up to 80 and keeps 768.
-template <int G, int CPL, int MODE, int U>
+template <int G, int CPL, int MODE, int U, int UR>
 __global__ void __launch_bounds__(GNN_ROWS_BLOCK, ((MODE == 1 && CPL == 3) ? 768 : 1024) / GNN_ROWS_BLOCK)
     spmm_rows_kernel(
     int n, const int64_t* __restrict__ rowptr, const int32_t* __restrict__ col,
-    const float* __restrict__ val, const float* __restrict__ H, int64_t ldh, int F,
+    const float* __restrict__ val, const int32_t* __restrict__ local_cnt,
+    const float* __restrict__ H, int64_t ldh, int F,
     SlotMsgs msg, const int64_t* __restrict__ own_ptr, const int32_t* __restrict__ own_slot,
     RowSplit sp, Slices sl, float* __restrict__ partial, float* __restrict__ M, int64_t ldm,
     __nv_bfloat16* __restrict__ Mb, int64_t ldmb, int nch_b) {
@@ -204,11 +223,31 @@ __global__ void __launch_bounds__(GNN_ROWS_BLOCK, ((MODE == 1 && CPL == 3) ? 768
 #pragma unroll
   for (int i = 0; i < CPL; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 
-  if (unit < sp.n_pieces) {  // a piece of a long row -> partial row `unit`
-    const int64_t row = __ldg(sp.piece_row + unit);
-    const int64_t beg = __ldg(sp.piece_beg + unit);
-    const int64_t end = min(beg + (int64_t)sp.T, __ldg(rowptr + row + 1));
-    gather_range<G, CPL, MODE, U>(beg, end, col, val, H4, ldh4, c0, min(c1, nch), msg, gl, gmask, acc);
+  const bool piece = unit < sp.n_pieces;
+  int64_t row, beg, end;
+  if (piece) {  // a piece of a long row -> partial row `unit`
+    row = __ldg(sp.piece_row + unit);
+    beg = __ldg(sp.piece_beg + unit);
+    end = min(beg + (int64_t)sp.T, __ldg(rowptr + row + 1));
+  } else {
+    row = unit - sp.n_pieces;
+    if (row >= n) return;  // uniform across the group
+    beg = __ldg(rowptr + row);
+    end = __ldg(rowptr + row + 1);
+    if (sp.T > 0 && end - beg > sp.T) return;  // a long row: its pieces cover it
+  }
+  if (MODE == kPlain) {
+    gather_range<G, CPL, false, U>(beg, end, col, val, H4, ldh4, c0, min(c1, nch), msg, gl, gmask, acc);
+  } else {
+    // local entries lead each row, remote slots follow
+    const int64_t mid = (piece ? __ldg(rowptr + row) : beg) + __ldg(local_cnt + row);
+    gather_range<G, CPL, false, U>(beg, min(end, mid), col, val, H4, ldh4, c0, min(c1, nch), msg,
+                                   gl, gmask, acc);
+    if (MODE == kFwdRemote)
+      gather_range<G, CPL, true, UR>(max(beg, mid), end, col, val, H4, ldh4, c0, min(c1, nch), msg,
+                                     gl, gmask, acc);
+  }
+  if (piece) {
     float4* prow = reinterpret_cast<float4*>(partial) + unit * nch;
 #pragma unroll
     for (int i = 0; i < CPL; ++i) {
@@ -217,13 +256,8 @@ __global__ void __launch_bounds__(GNN_ROWS_BLOCK, ((MODE == 1 && CPL == 3) ? 768
     }
     return;
   }
-  const int64_t r = unit - sp.n_pieces;
-  if (r >= n) return;  // uniform across the group
-  const int64_t beg = __ldg(rowptr + r), end = __ldg(rowptr + r + 1);
-  if (sp.T > 0 && end - beg > sp.T) return;  // a long row: its pieces cover it
-  gather_range<G, CPL, MODE, U>(beg, end, col, val, H4, ldh4, c0, min(c1, nch), msg, gl, gmask, acc);
-  if (MODE == kBwdOwned) add_owned<G, CPL>(r, own_ptr, own_slot, msg, c0, min(c1, nch), gl, acc);
-  store_row<G, CPL>(r, acc, F, nch, nch_b, c0, c1, gl, M, ldm, Mb, ldmb);
+  if (MODE == kBwdOwned) add_owned<G, CPL>(row, own_ptr, own_slot, msg, c0, min(c1, nch), gl, acc);
+  store_row<G, CPL>(row, acc, F, nch, nch_b, c0, c1, gl, M, ldm, Mb, ldmb);
 }
 
 // Long rows: sum of their pieces' partial rows, 16 pieces at a time and then
@@ -405,15 +439,16 @@ static RowSplit row_split_of(const gnn_csr& csr) {
 }
 
 template <int MODE>
-static gnn_status dispatch_rows(const gnn_csr& csr, const int32_t* colv, const float* H,
-                                int64_t ldh, int F, SlotMsgs msg, const int64_t* own_ptr,
-                                const int32_t* own_slot, float* partial, float* M, int64_t ldm,
-                                __nv_bfloat16* Mb, int64_t ldmb, cudaStream_t st) {
+static gnn_status dispatch_rows(const gnn_csr& csr, const int32_t* colv, const float* valv,
+                                const int32_t* local_cnt, const float* H, int64_t ldh, int F,
+                                SlotMsgs msg, const int64_t* own_ptr, const int32_t* own_slot,
+                                float* partial, float* M, int64_t ldm, __nv_bfloat16* Mb,
+                                int64_t ldmb, cudaStream_t st) {
   const int nch = (F + 3) / 4;
   const int nch_b = Mb ? ((F + 15) / 16) * 4 : nch;
   const int need = nch_b > nch ? nch_b : nch;
   const RowSplit sp = row_split_of(csr);
-  // feature slices of at most 96 chunks (3 per lane) keep every lane's registers low
+  // feature slices of at most GNN_SLICE_CHUNKS chunks keep every lane's registers low
   Slices sl{1, need};
   if (need > GNN_SLICE_CHUNKS) {
     sl.ns = (need + GNN_SLICE_CHUNKS - 1) / GNN_SLICE_CHUNKS;
@@ -421,31 +456,31 @@ static gnn_status dispatch_rows(const gnn_csr& csr, const int32_t* colv, const f
   }
   const int cpl = (sl.cs + 31) / 32;
   const int block = GNN_ROWS_BLOCK;
-#define GNN_ROWS(G_, CPL_, U_)                                                                 \
+#define GNN_ROWS(G_, CPL_, U_, UR_)                                                            \
   do {                                                                                         \
     const int64_t groups = ((int64_t)csr.n + sp.n_pieces) * sl.ns;                             \
     const int64_t grid = (groups * G_ + block - 1) / block;                                    \
-    spmm_rows_kernel<G_, CPL_, MODE, U_><<<(unsigned)grid, block, 0, st>>>(                    \
-        csr.n, csr.rowptr, colv, csr.val, H, ldh, F, msg, own_ptr, own_slot, sp, sl, partial,  \
-        M, ldm, Mb, ldmb, nch_b);                                                              \
+    spmm_rows_kernel<G_, CPL_, MODE, U_, UR_><<<(unsigned)grid, block, 0, st>>>(               \
+        csr.n, csr.rowptr, colv, valv, local_cnt, H, ldh, F, msg, own_ptr, own_slot, sp, sl,   \
+        partial, M, ldm, Mb, ldmb, nch_b);                                                     \
     GNN_CHECK_LAUNCH();                                                                        \
     if (sp.n_long > 0) {                                                                       \
-      const int64_t g2 = ((int64_t)sp.n_long * sl.ns * G_ + block - 1) / block;                \
-      spmm_fixup_kernel<G_, CPL_, MODE><<<(unsigned)g2, block, 0, st>>>(                       \
+      const int64_t g2 = ((int64_t)sp.n_long * sl.ns * G_ + 255) / 256;                        \
+      spmm_fixup_kernel<G_, CPL_, MODE><<<(unsigned)g2, 256, 0, st>>>(                         \
           sp, sl, partial, F, msg, own_ptr, own_slot, M, ldm, Mb, ldmb, nch_b);                \
       GNN_CHECK_LAUNCH();                                                                      \
     }                                                                                          \
   } while (0)
-  // entries gathered per round: about 8 float4 loads in flight per lane; the
-  // forward with remote rows carries 4 more values per entry, so it gathers
-  // half as many to stay within 64 registers
-  constexpr int W = MODE == kFwdRemote ? 2 : 1;
-  if (sl.cs <= 4) GNN_ROWS(4, 1, 8 / W);
-  else if (sl.cs <= 8) GNN_ROWS(8, 1, 8 / W);
-  else if (sl.cs <= 16) GNN_ROWS(16, 1, 8 / W);
-  else if (cpl == 1) GNN_ROWS(32, 1, 8 / W);
-  else if (cpl == 2) GNN_ROWS(32, 2, 4 / W);
-  else if (cpl == 3) GNN_ROWS(32, 3, 2);
+  // entries gathered per round: ~8 float4 loads in flight per lane for local
+  // rows; remote rows carry four more values per entry and gather fewer
+  constexpr int U1 = MODE == kFwdRemote ? GNN_U1_FWD : GNN_U1;
+  constexpr int U2 = MODE == kFwdRemote ? GNN_U2_FWD : GNN_U2;
+  if (sl.cs <= 4) GNN_ROWS(4, 1, U1, GNN_UR1);
+  else if (sl.cs <= 8) GNN_ROWS(8, 1, U1, GNN_UR1);
+  else if (sl.cs <= 16) GNN_ROWS(16, 1, U1, GNN_UR1);
+  else if (cpl == 1) GNN_ROWS(32, 1, U1, GNN_UR1);
+  else if (cpl == 2) GNN_ROWS(32, 2, U2, GNN_UR2);
+  else if (cpl == 3) GNN_ROWS(32, 3, 2, 2);
   else return fail(GNN_ERR_UNSUPPORTED, "spmm: F=%d exceeds %d", F, kMaxF);
 #undef GNN_ROWS
   return GNN_OK;
@@ -458,11 +493,11 @@ gnn_status launch_spmm_fwd(const gnn_csr& csr, const gnn_boundary* bnd, const fl
   if (csr.n == 0) return GNN_OK;
   auto* mb = reinterpret_cast<__nv_bfloat16*>(Mb);
   if (!bnd)
-    return dispatch_rows<kPlain>(csr, csr.col, H, ldh, F, SlotMsgs{}, nullptr, nullptr, partial,
-                                 M, ldm, mb, ldmb, st);
+    return dispatch_rows<kPlain>(csr, csr.col, csr.val, nullptr, H, ldh, F, SlotMsgs{}, nullptr,
+                                 nullptr, partial, M, ldm, mb, ldmb, st);
   SlotMsgs msg{packed, meta, bnd->slot_off, bnd->slot_bits};
-  return dispatch_rows<kFwdRemote>(csr, bnd->col_remap, H, ldh, F, msg, nullptr, nullptr, partial,
-                                   M, ldm, mb, ldmb, st);
+  return dispatch_rows<kFwdRemote>(csr, bnd->col_remap, bnd->val_remap, bnd->local_cnt, H, ldh, F,
+                                   msg, nullptr, nullptr, partial, M, ldm, mb, ldmb, st);
 }
 
 static int quant_chunk_slots(int F) {
@@ -520,13 +555,13 @@ gnn_status launch_spmm_bwd(const gnn_csr& csr, const gnn_boundary* bnd, const fl
                            cudaStream_t st) {
   if (csr.n == 0) return GNN_OK;
   if (!bnd)
-    return dispatch_rows<kPlain>(csr, csr.col, Gm, ldg, F, SlotMsgs{}, nullptr, nullptr, partial,
-                                 dH, ldh, nullptr, 0, st);
+    return dispatch_rows<kPlain>(csr, csr.col, csr.val, nullptr, Gm, ldg, F, SlotMsgs{}, nullptr,
+                                 nullptr, partial, dH, ldh, nullptr, 0, st);
   gnn_status s = launch_halo_quant_pack(*bnd, Gm, ldg, F, seed, packed_ws, meta_ws, st);
   if (s != GNN_OK) return s;
   SlotMsgs msg{packed_ws, meta_ws, bnd->slot_off, bnd->slot_bits};
-  return dispatch_rows<kBwdOwned>(csr, bnd->col_remap, Gm, ldg, F, msg, bnd->own_ptr,
-                                  bnd->own_slot, partial, dH, ldh, nullptr, 0, st);
+  return dispatch_rows<kBwdOwned>(csr, bnd->col_remap, bnd->val_remap, bnd->local_cnt, Gm, ldg, F,
+                                  msg, bnd->own_ptr, bnd->own_slot, partial, dH, ldh, nullptr, 0, st);
 }
 
 size_t spmm_workspace_bytes(const gnn_csr& csr, int F) {
@@ -568,7 +603,8 @@ static gnn_status check_bnd(const gnn_csr* csr, const gnn_boundary* b, int F, bo
   if (b->n != csr->n || b->P < 1) return fail(GNN_ERR_INVALID_ARG, "%s: boundary does not match csr", who);
   if (b->F != F)
     return fail(GNN_ERR_INVALID_ARG, "%s: boundary offsets are for F=%d, call has F=%d", who, b->F, F);
-  if (!b->col_remap || (b->n_slots > 0 && (!b->slot_off || !b->slot_bits)))
+  if (!b->col_remap || !b->val_remap || !b->local_cnt ||
+      (b->n_slots > 0 && (!b->slot_off || !b->slot_bits)))
     return fail(GNN_ERR_INVALID_ARG, "%s: boundary arrays are NULL", who);
   if (bwd && (!b->own_ptr || (b->n_slots > 0 && (!b->slot_rowptr || !b->own_slot)) ||
               (b->nnz_cut > 0 && (!b->slot_col || !b->slot_val))))

@@ -125,12 +125,13 @@ def test_boundary_index_bit_exact(built, name, P, pct, bits, base, F):
     rp, col, val = O.csr_build(n, src, dst)
     ob = oracle_boundary(n, rp, col, val, P, pct, bits, base, F)
     assert (b.n_slots, b.nnz_cut) == (ob["n_slots"], ob["nnz_cut"])
-    for k in ("part_start", "send_start", "slot_node", "col_remap", "slot_rowptr", "slot_col",
-              "own_ptr", "own_slot", "node_bits", "slot_bits", "slot_off"):
+    for k in ("part_start", "send_start", "slot_node", "col_remap", "local_cnt", "slot_rowptr",
+              "slot_col", "own_ptr", "own_slot", "node_bits", "slot_bits", "slot_off"):
         got = host(b.arrays[k])
         want = np.asarray(ob[k])
         assert np.array_equal(got, want.astype(got.dtype)), k
     assert np.array_equal(host(b.slot_val).view(np.uint32), ob["slot_val"].view(np.uint32))
+    assert np.array_equal(host(b.val_remap).view(np.uint32), ob["val_remap"].view(np.uint32))
     # base-width change recomputes widths and offsets only
     G.gnn_boundary_set_bits(csr, b, G.BitRule(pct, bits), 8, F + 3)
     nb8 = O.node_bits(n, rp, ob, pct, bits, 8)
@@ -266,9 +267,10 @@ def test_spmm_fwd_partitioned(built, name, P, pct, bits, base, F, split):
     assert_close_agg(host(M)[:, :F], ref, T, f"spmm_fwd partitioned {name}")
 
 
-def test_spmm_fwd_passthrough_equals_plain_bitwise(built):
+def test_spmm_fwd_passthrough_equals_plain(built):
     """Width 32 sends exact rows, so the partitioned forward reproduces the
-    plain one bit for bit (same summation order)."""
+    plain one up to the order of the fp32 additions (the partitioned layout
+    adds a row's local entries before its remote ones)."""
     t = __import__("torch")
     n, csr, b, rp, col, val, ob = _partitioned_setup("planted", 4, [90], [32, 32], 1, 24, 0)
     H = dev(padded(_features(n, 24, 3), 24, 24))
@@ -280,7 +282,9 @@ def test_spmm_fwd_passthrough_equals_plain_bitwise(built):
     M0 = t.empty((n, 24), device="cuda")
     G.gnn_spmm_fwd(csr, b, H, 24, packed, meta, M=M1)
     G.gnn_spmm_fwd(csr, None, H, 24, M=M0)
-    assert t.equal(M0.view(t.int32), M1.view(t.int32))
+    _, T = O.spmm_fwd(n, rp, col, val, host(H), 24)
+    err = np.abs(host(M1).astype(np.float64) - host(M0))
+    assert np.all(err <= 2e-5 * T + 2e-7)
 
 
 @pytest.mark.parametrize("P", [1, 4])

@@ -61,11 +61,12 @@ def test_workload_parity(name):
     bnd = G.gnn_boundary_index(csr, P, G.BitRule(cfg_pct, cfg_bits), base, F0)
     ob = oracle_boundary(n, rp, col, val, P, cfg_pct, cfg_bits, base, F0)
     assert (bnd.n_slots, bnd.nnz_cut) == (ob["n_slots"], ob["nnz_cut"])
-    for k in ("part_start", "send_start", "slot_node", "col_remap", "slot_rowptr", "slot_col",
-              "own_ptr", "own_slot", "node_bits", "slot_bits", "slot_off"):
+    for k in ("part_start", "send_start", "slot_node", "col_remap", "local_cnt", "slot_rowptr",
+              "slot_col", "own_ptr", "own_slot", "node_bits", "slot_bits", "slot_off"):
         got = host(bnd.arrays[k])
         assert np.array_equal(got, np.asarray(ob[k]).astype(got.dtype)), k
     assert np.array_equal(host(bnd.slot_val).view(np.uint32), ob["slot_val"].view(np.uint32))
+    assert np.array_equal(host(bnd.val_remap).view(np.uint32), ob["val_remap"].view(np.uint32))
     S = bnd.n_slots
     sb = ob["slot_bits"]
     G.gnn_boundary_long_slots(csr, bnd, LONG_SLOT_LEN)

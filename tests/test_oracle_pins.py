@@ -159,10 +159,13 @@ def test_boundary_bruteforce(n, p, P, seed):
         [(int(q), int(u)) for q, u in zip(np.repeat(np.arange(P), np.diff(b["send_start"])), b["slot_node"])]
     index = {sl: s for s, sl in enumerate(slots)}
     for v in range(n):
-        for k in range(rowptr[v], rowptr[v + 1]):
-            u = int(col[k])
-            want = u if part(u) == part(v) else ~index[(part(v), u)]
-            assert b["col_remap"][k] == want
+        ks = range(rowptr[v], rowptr[v + 1])
+        local = [(int(col[k]), val[k]) for k in ks if part(int(col[k])) == part(v)]
+        remote = [(~index[(part(v), int(col[k]))], val[k]) for k in ks if part(int(col[k])) != part(v)]
+        want = local + remote
+        got = list(zip(b["col_remap"][rowptr[v]:rowptr[v + 1]], b["val_remap"][rowptr[v]:rowptr[v + 1]]))
+        assert [(int(c), float(w)) for c, w in got] == [(c, float(w)) for c, w in want]
+        assert b["local_cnt"][v] == len(local)
     for s, (q, u) in enumerate(slots):
         ents = [(v, val[k]) for v in range(n) if part(v) == q
                 for k in range(rowptr[v], rowptr[v + 1]) if col[k] == u]
@@ -358,7 +361,8 @@ def test_fwd_quantised_rows_use_their_slot_message():
             if O.part_of(u, starts) == O.part_of(v, starts):
                 x = H[u].astype(np.float64)
             else:
-                s = int(~b["col_remap"][k])
+                s = int(np.searchsorted(b["slot_node"][b["send_start"][O.part_of(v, starts)]:], u)
+                        + b["send_start"][O.part_of(v, starts)])
                 assert b["slot_node"][s] == u
                 c, m = O.quantize(H[u:u + 1], [bits[s]], [s], seed=8)
                 x = O.dequantize(c, m, [bits[s]])[0].astype(np.float64)
