@@ -187,7 +187,7 @@ def run_gpu(args, rank, world, local_rank):
     G.load()
     wl = make_workload(args.workload)
     n, P, dims, L = wl.n, wl.P, wl.dims, wl.layers
-    base = wl.base_bits[0]
+    base = args.base_bits if args.base_bits else wl.base_bits[0]
     csr = G.gnn_csr_build(n, torch.from_numpy(wl.src).to(dev), torch.from_numpy(wl.dst).to(dev))
     csr = G.gnn_csr_split(csr, args.split_len)
     rule = G.BitRule(wl.rule_pct, wl.rule_bits)
@@ -473,6 +473,8 @@ def main():
     ap.add_argument("--workload", default="yelp", choices=sorted(WORKLOAD_TEXT))
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--split-len", type=int, default=128)
+    ap.add_argument("--base-bits", type=int, default=0,
+                    help="epoch base width (1, 2, 4, 8); default: the workload's first")
     ap.add_argument("--long-slot-len", type=int, default=128)
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
@@ -491,6 +493,7 @@ def main():
             torch.cuda.set_device(local_rank)
 
     config = {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload,
+              "base_bits": args.base_bits or None,
               "timing": "inputs larger than L2 (no flush); CUDA events on the launching stream",
               "parallelism": f"replicas x{world}"}
 
