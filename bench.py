@@ -339,6 +339,54 @@ def run_gpu(args, rank, world, local_rank):
             flops["spmm"] += 2.0 * nnz * F
     total_bytes = sum(byt.values())
 
+    # an asynchronous epoch (SYLVIE guide section 10) through the layer API:
+    # each layer aggregates with the previous step's messages while this
+    # step's are quantised and packed on a second stream.  Same work and byte
+    # model as the synchronous step; per layer and direction two message
+    # buffers alternate between steps.
+    asy = None
+    if args.async_steps > 0:
+        aux = torch.cuda.Stream(dev)
+
+        def msgbufs(F):
+            Qf = max(int(offs[F][-1].item()), 16)
+            return [(torch.zeros(Qf, dtype=torch.uint8, device=dev),
+                     torch.zeros((max(S, 1), 2), device=dev)) for _ in range(2)]
+
+        fwd_msgs = [msgbufs(dims[l]) for l in range(L)]
+        bwd_msgs = [msgbufs(dims[l]) if l > 0 else None for l in range(L)]
+
+        def async_step(i):
+            cur, prev = i % 2, (i + 1) % 2
+            for l in range(L):
+                F, Fo = dims[l], dims[l + 1]
+                (pp, mp), (pn, mn) = fwd_msgs[l][prev], fwd_msgs[l][cur]
+                G.gnn_layer_fwd_async(csr, bnd, H[l], F, W[l], Fo, l < L - 1, 2 * l, pp, mp, pn, mn,
+                                      Mb[l], H[l + 1], aux, slot_off=offs[F], ws=ws)
+            for l in reversed(range(L)):
+                F, Fo = dims[l], dims[l + 1]
+                if l > 0:
+                    (pp, mp), (pn, mn) = bwd_msgs[l][prev], bwd_msgs[l][cur]
+                    G.gnn_layer_bwd_async(csr, bnd, dH[l + 1], H[l + 1], l < L - 1, Mb[l], W[l], F, Fo,
+                                          2 * l + 1, pp, mp, pn, mn, dW[l], dH[l], aux,
+                                          slot_off=offs[F], ws=ws)
+                else:
+                    G.gnn_dense_bwd(Mb[0], n, F, W[0], Fo, dH[1], H[1], L > 1, None, dW[0], ws=wsd)
+
+        for i in range(args.warmup):
+            async_step(i)
+        torch.cuda.synchronize(dev)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(args.async_steps):
+            async_step(i)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        G.gnn_sync_check()
+        asy = dict(ms=a.elapsed_time(b) / args.async_steps)
+        del fwd_msgs, bwd_msgs
+
     # e2e through the layer API with host buffers: every step copies its inputs
     # (layer-1 features, upstream gradient) from pinned host memory and reads
     # the weight gradients back.  The copy of step i+1's inputs runs on a copy
@@ -410,7 +458,7 @@ def run_gpu(args, rank, world, local_rank):
         e2e = dict(ms=e2e_ms, h2d=h2d, d2h=d2h)
 
     return dict(ms=ms, per=per, per_layer=per_layer, byt=byt, flops=flops, total_bytes=total_bytes,
-                launches=launches, clocks=clk.summary(), e2e=e2e, S=S, nnz=nnz, nnz_cut=nc, n=n,
+                launches=launches, clocks=clk.summary(), e2e=e2e, asy=asy, S=S, nnz=nnz, nnz_cut=nc, n=n,
                 Q=int(offs[F0][-1].item()), spmm_fwd_bytes_l=spmm_fwd_bytes_l, n_long=csr.n_long,
                 n_pieces=csr.n_pieces, dims=dims, P=P)
 
@@ -477,6 +525,8 @@ def main():
                     help="epoch base width (1, 2, 4, 8); default: the workload's first")
     ap.add_argument("--long-slot-len", type=int, default=128)
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--async-steps", type=int, default=10,
+                    help="also time asynchronous-epoch steps (0: skip)")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -569,6 +619,12 @@ def main():
         line["e2e"] = {"value": whole_job_rate(r["total_bytes"], world, e_ms), "unit": UNIT,
                        "ms_per_step": e_ms, "h2d_bytes_per_step": e["h2d"],
                        "d2h_bytes_per_step": e["d2h"]}
+    if r["asy"]:
+        a_ms = max_over_ranks(r["asy"]["ms"], world, "cuda")
+        line["async_epoch"] = {"value": whole_job_rate(r["total_bytes"], world, a_ms), "unit": UNIT,
+                               "ms_per_step": a_ms,
+                               "what": "remote sources read the previous step's messages; this "
+                                       "step's are packed on a second stream meanwhile"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cb = OracleBaseline(args.workload).sample(args.cpu_budget)
         line["cpu_baseline"] = {k: cb[k] for k in ["value", "unit", "cores", "kind", "sample"]}

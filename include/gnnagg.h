@@ -342,6 +342,80 @@ gnn_status gnn_layer_bwd(const gnn_csr* csr, const gnn_boundary* bnd, const floa
                          float* dW, float* dH_in, int64_t ldh, void* ws, size_t ws_bytes,
                          gnn_stream_t stream);
 
+/* ------------------------------------------------------------------------ */
+/* Asynchronous epochs (SYLVIE guide, section 10: boundary messages one      */
+/* epoch stale, their quantisation overlapped with local computation).       */
+/* ------------------------------------------------------------------------ */
+/* The two halves of gnn_spmm_bwd, for callers that overlap them:
+ * gnn_halo_quant_pack forms each slot's fixed-order halo partial of G and
+ * quantises/packs it (row key s, `seed`) into packed/meta;
+ * gnn_spmm_bwd_local computes dH[u] = sum over u's local entries of
+ * val * G[v] + the dequantised messages in packed/meta of the slots u owns.
+ * gnn_spmm_bwd(G) equals gnn_halo_quant_pack(G) then gnn_spmm_bwd_local(G)
+ * with the same buffers. */
+gnn_status gnn_halo_quant_pack(const gnn_boundary* bnd, const float* G, int64_t ldg, int32_t F,
+                               uint32_t seed, uint8_t* packed, float* meta, gnn_stream_t stream);
+gnn_status gnn_spmm_bwd_local(const gnn_csr* csr, const gnn_boundary* bnd, const float* G,
+                              int64_t ldg, int32_t F, const uint8_t* packed, const float* meta,
+                              float* dH, int64_t ldh, void* ws, size_t ws_bytes,
+                              gnn_stream_t stream);
+
+/* An asynchronous forward layer: the aggregation uses the messages of the
+ * previous epoch (packed_prev/meta_prev, as gnn_quant_pack wrote them from
+ * that epoch's H_in), while this epoch's H_in is quantised and packed into
+ * packed_next/meta_next on `aux` at the same time.  The call orders `stream`
+ * after that work (the next buffers are complete when later work on `stream`
+ * runs).  Other arguments as gnn_layer_fwd. */
+gnn_status gnn_layer_fwd_async(const gnn_csr* csr, const gnn_boundary* bnd, const float* H_in,
+                               int64_t ldh, int32_t F_in, const uint16_t* W, int32_t F_out,
+                               int32_t relu, uint32_t seed, const uint8_t* packed_prev,
+                               const float* meta_prev, uint8_t* packed_next, float* meta_next,
+                               uint16_t* Mb, int64_t ldmb, float* H_out, int64_t ldo, void* ws,
+                               size_t ws_bytes, gnn_stream_t stream, gnn_stream_t aux);
+
+/* An asynchronous backward layer: dense backward on `stream`; then the
+ * owner-side aggregation into dH_in uses the previous epoch's backward
+ * messages (packed_prev/meta_prev) while this epoch's halo partials of dM are
+ * quantised and packed into packed_next/meta_next on `aux`. */
+gnn_status gnn_layer_bwd_async(const gnn_csr* csr, const gnn_boundary* bnd,
+                               const float* dH_out, int64_t ldg, const float* H_out, int64_t ldo,
+                               int32_t relu, const uint16_t* Mb, int64_t ldmb,
+                               const uint16_t* W, int32_t F_in, int32_t F_out, uint32_t seed,
+                               const uint8_t* packed_prev, const float* meta_prev,
+                               uint8_t* packed_next, float* meta_next, float* dW, float* dH_in,
+                               int64_t ldh, void* ws, size_t ws_bytes, gnn_stream_t stream,
+                               gnn_stream_t aux);
+
+/* ------------------------------------------------------------------------ */
+/* Epoch control (SYLVIE guide, sections 8 and 11).  Host code.              */
+/* ------------------------------------------------------------------------ */
+#define GNN_LDR_MAX_DELTA 64
+/* Coordinator, Quant Orchestrator and Pipeline Adaptor state.  After every
+ * epoch, gnn_ldr_update takes the partitions' losses and the epoch time:
+ * L_t = mean loss, F_t = lambda F_{t-1} + (1 - lambda) L_t (F_0 = L_0),
+ * LDR_t = (F_{t-1} - F_t) / et_t, the descent rate (LDR_0 = 0).  Then, for
+ * the next epoch: after the first epoch base_bits = b_min; when t > delta,
+ * LDR_t < LDR_{t-delta} doubles base_bits (at most b_max) and makes the next
+ * epoch synchronous, otherwise base_bits halves (at least b_min) and the next
+ * epoch is asynchronous; for 0 < t <= delta nothing changes.  The sign reading
+ * (smaller descent rate = worse) follows the pages' prose. */
+typedef struct gnn_ldr_state {
+  double lambda;     /* smoothing coefficient (0.9 recommended)       */
+  int32_t delta;     /* look-back interval in epochs (5, 10, 20)      */
+  int32_t b_min;     /* 1                                             */
+  int32_t b_max;     /* 8                                             */
+  int32_t t;         /* epochs reported so far                        */
+  int32_t base_bits; /* base width for the next epoch                 */
+  int32_t async_next;/* 1: run the next epoch asynchronously          */
+  double F;          /* smoothed loss after the last report           */
+  double ldr[GNN_LDR_MAX_DELTA + 1]; /* last delta+1 LDR values (ring) */
+} gnn_ldr_state;
+
+gnn_status gnn_ldr_init(gnn_ldr_state* st, double lambda, int32_t delta, int32_t b_min,
+                        int32_t b_max);
+gnn_status gnn_ldr_update(gnn_ldr_state* st, const double* partition_loss, int32_t n_parts,
+                          double epoch_seconds);
+
 /* Synchronise `stream` and report device-side failures (GNN_ERR_CUDA for a
  * CUDA error, GNN_ERR_DEVICE_CHECK / GNN_ERR_TIMEOUT for flags the kernels
  * raised).  Clears the flags. */

@@ -328,11 +328,13 @@ def _slot_messages(X, F, slot_node, slots, slot_bits, seed):
     return dequantize(codes, meta, slot_bits[slots])
 
 
-def spmm_fwd(n, rowptr, col, val, H, F, bnd=None, slot_bits=None, seed=0, rows=None):
+def spmm_fwd(n, rowptr, col, val, H, F, bnd=None, slot_bits=None, seed=0, rows=None, H_msg=None):
     """M[v] = sum_e val[e] * x_e, where x_e = H[u] for a local source u and the
     dequantised message of slot (part(v), u) for a remote one.  Accumulates in
     fp64; also returns T[v] = sum_e |val[e] * x_e| (for error bounds).
-    ``rows`` selects output rows (default all)."""
+    ``rows`` selects output rows (default all).  ``H_msg``: the matrix the
+    messages are formed from (default H); in an asynchronous epoch (section
+    10) it is the previous epoch's layer input and ``seed`` that epoch's."""
     rows = np.arange(n, dtype=np.int64) if rows is None else np.asarray(rows, np.int64)
     lens = rowptr[rows + 1] - rowptr[rows]
     e = _expand_ranges(rowptr[rows], lens)
@@ -352,7 +354,8 @@ def spmm_fwd(n, rowptr, col, val, H, F, bnd=None, slot_bits=None, seed=0, rows=N
         X = np.zeros((uniq.size, F), np.float64)
         X[: loc.size] = np.asarray(H)[loc, :F]
         if slots.size:
-            X[loc.size:] = _slot_messages(H, F, bnd["slot_node"], slots, slot_bits, seed)
+            Xm = H if H_msg is None else H_msg
+            X[loc.size:] = _slot_messages(Xm, F, bnd["slot_node"], slots, slot_bits, seed)
     A = sp.csr_matrix((w, (out_row, inv)), shape=(rows.size, uniq.size))
     M = A @ X
     T = abs(A) @ np.abs(X)
@@ -390,11 +393,13 @@ def slot_partials(bnd, G, F, slots=None):
     return acc
 
 
-def spmm_bwd(n, rowptr, col, val, G, F, bnd=None, slot_bits=None, seed=0, rows=None):
+def spmm_bwd(n, rowptr, col, val, G, F, bnd=None, slot_bits=None, seed=0, rows=None, G_msg=None):
     """dH = A^T G (A symmetric).  With partitions: dH[u] = sum of A_vu G[v]
     over local v, plus the dequantised halo partials of every slot u owns
     (each quantised with key s and ``seed``).  fp64 accumulation; returns
-    (dH, T) for ``rows`` (default all)."""
+    (dH, T) for ``rows`` (default all).  ``G_msg``: the matrix the halo
+    partials are formed from (default G; the previous epoch's in an
+    asynchronous epoch, section 10)."""
     rows = np.arange(n, dtype=np.int64) if rows is None else np.asarray(rows, np.int64)
     if bnd is None:
         A = sp.csr_matrix((val.astype(np.float64), col.astype(np.int64), rowptr), shape=(n, n))
@@ -419,7 +424,7 @@ def spmm_bwd(n, rowptr, col, val, G, F, bnd=None, slot_bits=None, seed=0, rows=N
         oi = _expand_ranges(own_ptr[rows], olens)
         slots = own_slot[oi].astype(np.int64)
         orow = np.repeat(np.arange(rows.size), olens)
-        part = slot_partials(bnd, G, F, slots)
+        part = slot_partials(bnd, G if G_msg is None else G_msg, F, slots)
         codes, meta = quantize(part, slot_bits[slots], slots, seed)
         deq = dequantize(codes, meta, slot_bits[slots]).astype(np.float64)
         np.add.at(dH, orow, deq)

@@ -11,7 +11,9 @@ from typing import Optional, Sequence
 
 from . import _abi
 from ._abi import (CSR_DEDUP, CSR_GCN, CSR_SELF_LOOPS, CSR_SYMMETRIZE, GnnBitRule,  # noqa: F401
-                   GnnBoundary, GnnCsr, GnnError, call, load)
+                   GnnBoundary, GnnCsr, GnnError, GnnLdrState, call, load)
+
+LdrState = GnnLdrState
 
 __all__ = [
     "Csr", "Boundary", "BitRule", "GnnError", "load", "build",
@@ -19,6 +21,8 @@ __all__ = [
     "gnn_quant_pack", "gnn_dequant_unpack", "gnn_spmm_fwd", "gnn_spmm_bwd", "gnn_sync_check", "gnn_kernel_launches",
     "rowbytes", "ld_for", "ldb_for", "gnn_dense_workspace", "gnn_dense_fwd", "gnn_dense_bwd",
     "gnn_layer_workspace", "gnn_layer_fwd", "gnn_layer_bwd",
+    "gnn_halo_quant_pack", "gnn_spmm_bwd_local", "gnn_layer_fwd_async", "gnn_layer_bwd_async",
+    "LdrState", "gnn_ldr_init", "gnn_ldr_update",
 ]
 
 
@@ -321,6 +325,26 @@ def gnn_spmm_bwd(csr: Csr, bnd: Optional[Boundary], G, F: int, seed: int, packed
          wp, wn, _stream(stream))
 
 
+def gnn_halo_quant_pack(bnd: Boundary, G, F: int, seed: int, packed, meta, slot_off=None,
+                        stream=None) -> None:
+    """Backward messages only: each slot's halo partial of G, quantised and
+    packed."""
+    cb = bnd.c(slot_off, F if slot_off is not None else None)
+    call("gnn_halo_quant_pack", ctypes.byref(cb), _ptr(G), G.stride(0), F, seed & 0xFFFFFFFF,
+         _ptr(packed), _ptr(meta), _stream(stream))
+
+
+def gnn_spmm_bwd_local(csr: Csr, bnd: Boundary, G, F: int, packed, meta, dH, slot_off=None,
+                       ws=None, stream=None) -> None:
+    """Owner-side backward aggregation: local transpose entries plus the
+    dequantised backward messages in packed/meta."""
+    c = csr.c()
+    cb = bnd.c(slot_off, F if slot_off is not None else None)
+    wp, wn = _ws_args(csr, F, ws, G.device)
+    call("gnn_spmm_bwd_local", ctypes.byref(c), ctypes.byref(cb), _ptr(G), G.stride(0), F,
+         _ptr(packed), _ptr(meta), _ptr(dH), dH.stride(0), wp, wn, _stream(stream))
+
+
 def gnn_kernel_launches() -> int:
     """Kernels launched through the library by this process so far."""
     return int(load().gnn_kernel_launches())
@@ -388,3 +412,48 @@ def gnn_layer_bwd(csr: Csr, bnd: Optional[Boundary], dH_out, H_out, relu: bool, 
          int(relu), _ptr(Mb), Mb.stride(0), _ptr(W), F_in, F_out, seed & 0xFFFFFFFF, _ptr(packed_ws),
          _ptr(meta_ws), _ptr(dW), _ptr(dH_in), dH_in.stride(0) if dH_in is not None else 0,
          _ptr(ws), ws.numel(), _stream(stream))
+
+
+def gnn_layer_fwd_async(csr: Csr, bnd: Boundary, H_in, F_in: int, W, F_out: int, relu: bool,
+                        seed: int, packed_prev, meta_prev, packed_next, meta_next, Mb, H_out,
+                        aux, slot_off=None, ws=None, stream=None) -> None:
+    """Forward layer of an asynchronous epoch: remote sources read the
+    previous epoch's messages; this epoch's are packed on ``aux`` meanwhile."""
+    c = csr.c()
+    cb = bnd.c(slot_off, F_in if slot_off is not None else None)
+    if ws is None:
+        ws = _workspace(gnn_layer_workspace(csr, F_in, F_out), H_in.device)
+    call("gnn_layer_fwd_async", ctypes.byref(c), ctypes.byref(cb), _ptr(H_in), H_in.stride(0), F_in,
+         _ptr(W), F_out, int(relu), seed & 0xFFFFFFFF, _ptr(packed_prev), _ptr(meta_prev),
+         _ptr(packed_next), _ptr(meta_next), _ptr(Mb), Mb.stride(0), _ptr(H_out), H_out.stride(0),
+         _ptr(ws), ws.numel(), _stream(stream), aux.cuda_stream)
+
+
+def gnn_layer_bwd_async(csr: Csr, bnd: Boundary, dH_out, H_out, relu: bool, Mb, W, F_in: int,
+                        F_out: int, seed: int, packed_prev, meta_prev, packed_next, meta_next, dW,
+                        dH_in, aux, slot_off=None, ws=None, stream=None) -> None:
+    c = csr.c()
+    cb = bnd.c(slot_off, F_in if slot_off is not None else None)
+    if ws is None:
+        ws = _workspace(gnn_layer_workspace(csr, F_in, F_out), dH_out.device)
+    call("gnn_layer_bwd_async", ctypes.byref(c), ctypes.byref(cb), _ptr(dH_out), dH_out.stride(0),
+         _ptr(H_out), H_out.stride(0) if H_out is not None else 0, int(relu), _ptr(Mb), Mb.stride(0),
+         _ptr(W), F_in, F_out, seed & 0xFFFFFFFF, _ptr(packed_prev), _ptr(meta_prev),
+         _ptr(packed_next), _ptr(meta_next), _ptr(dW), _ptr(dH_in),
+         dH_in.stride(0) if dH_in is not None else 0, _ptr(ws), ws.numel(), _stream(stream),
+         aux.cuda_stream)
+
+
+# ---------------------------------------------------------------- epoch control (host only)
+def gnn_ldr_init(lam: float = 0.9, delta: int = 5, b_min: int = 1, b_max: int = 8) -> LdrState:
+    st = LdrState()
+    call("gnn_ldr_init", ctypes.byref(st), float(lam), delta, b_min, b_max)
+    return st
+
+
+def gnn_ldr_update(st: LdrState, partition_losses: Sequence[float], epoch_seconds: float):
+    """Reports one epoch; returns (base width, asynchronous?) for the next."""
+    n = len(partition_losses)
+    arr = (ctypes.c_double * max(n, 1))(*[float(x) for x in partition_losses])
+    call("gnn_ldr_update", ctypes.byref(st), arr, n, float(epoch_seconds))
+    return st.base_bits, bool(st.async_next)

@@ -40,6 +40,15 @@ class GnnBoundary(ctypes.Structure):
                 ("long_slot_len", c_i32), ("n_long_slots", c_i32), ("long_slots", c_vp)]
 
 
+GNN_LDR_MAX_DELTA = 64
+
+
+class GnnLdrState(ctypes.Structure):
+    _fields_ = [("lambda_", ctypes.c_double), ("delta", c_i32), ("b_min", c_i32), ("b_max", c_i32),
+                ("t", c_i32), ("base_bits", c_i32), ("async_next", c_i32), ("F", ctypes.c_double),
+                ("ldr", ctypes.c_double * (GNN_LDR_MAX_DELTA + 1))]
+
+
 P_csr = ctypes.POINTER(GnnCsr)
 P_bnd = ctypes.POINTER(GnnBoundary)
 P_rule = ctypes.POINTER(GnnBitRule)
@@ -82,6 +91,18 @@ PROTOTYPES = {
     "gnn_layer_bwd": (ctypes.c_int, [P_csr, P_bnd, c_vp, c_i64, c_vp, c_i64, c_i32, c_vp, c_i64, c_vp,
                                      c_i32, c_i32, c_u32, c_vp, c_vp, c_vp, c_vp, c_i64, c_vp, c_size,
                                      c_vp]),
+    "gnn_halo_quant_pack": (ctypes.c_int, [P_bnd, c_vp, c_i64, c_i32, c_u32, c_vp, c_vp, c_vp]),
+    "gnn_spmm_bwd_local": (ctypes.c_int, [P_csr, P_bnd, c_vp, c_i64, c_i32, c_vp, c_vp, c_vp, c_i64, c_vp,
+                                          c_size, c_vp]),
+    "gnn_layer_fwd_async": (ctypes.c_int, [P_csr, P_bnd, c_vp, c_i64, c_i32, c_vp, c_i32, c_i32, c_u32,
+                                           c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_vp, c_i64, c_vp, c_size,
+                                           c_vp, c_vp]),
+    "gnn_layer_bwd_async": (ctypes.c_int, [P_csr, P_bnd, c_vp, c_i64, c_vp, c_i64, c_i32, c_vp, c_i64,
+                                           c_vp, c_i32, c_i32, c_u32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
+                                           c_i64, c_vp, c_size, c_vp, c_vp]),
+    "gnn_ldr_init": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_double, c_i32, c_i32, c_i32]),
+    "gnn_ldr_update": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_double), c_i32,
+                                      ctypes.c_double]),
     "gnn_sync_check": (ctypes.c_int, [c_vp]),
 }
 

@@ -19,8 +19,10 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libgnnagg.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
-              "-Xptxas", "-warn-spills"]
+# Host code keeps separate multiplies and adds (no contraction into fused
+# multiply-adds), so host arithmetic gives the same bits on x86 and Arm.
+NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-ffp-contract=off",
+              "--expt-relaxed-constexpr", "-Xptxas", "-warn-spills"]
 
 
 def nvcc() -> str:

@@ -31,6 +31,14 @@ gnn_status launch_spmm_bwd(const gnn_csr& csr, const gnn_boundary* bnd, const fl
                            float2* meta_ws, float* dH, int64_t ldh, float* partial,
                            cudaStream_t st);
 
+gnn_status launch_spmm_bwd_local(const gnn_csr& csr, const gnn_boundary& bnd, const float* G,
+                                 int64_t ldg, int F, const uint8_t* packed, const float2* meta,
+                                 float* dH, int64_t ldh, float* partial, cudaStream_t st);
+
+gnn_status launch_halo_quant_pack(const gnn_boundary& b, const float* Gm, int64_t ldg, int F,
+                                  uint32_t seed, uint8_t* packed_ws, float2* meta_ws,
+                                  cudaStream_t st);
+
 size_t spmm_workspace_bytes(const gnn_csr& csr, int F);
 
 }  // namespace gnn

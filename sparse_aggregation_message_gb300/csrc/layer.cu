@@ -215,3 +215,103 @@ extern "C" gnn_status gnn_layer_bwd(const gnn_csr* csr, const gnn_boundary* bnd,
   return gnn_spmm_bwd(csr, bnd, w.dM, ldm, F_in, seed, packed_ws, meta_ws, dH_in, ldh, w.spmm,
                       spmm_workspace_bytes(*csr, F_in), stream);
 }
+
+// ------------------------------------------------------------------ asynchronous epochs
+// `aux` waits for `stream` (the layer's input is ready), runs the quantise
+// and pack of this epoch's messages, and `stream` waits for `aux` before the
+// call returns, so the overlap stays inside the call.
+struct Fork {
+  cudaEvent_t ready = nullptr, done = nullptr;
+  ~Fork() {
+    if (ready) cudaEventDestroy(ready);
+    if (done) cudaEventDestroy(done);
+  }
+};
+
+static gnn_status fork_to(Fork& f, cudaStream_t st, cudaStream_t aux) {
+  GNN_CUDA(cudaEventCreateWithFlags(&f.ready, cudaEventDisableTiming));
+  GNN_CUDA(cudaEventCreateWithFlags(&f.done, cudaEventDisableTiming));
+  GNN_CUDA(cudaEventRecord(f.ready, st));
+  GNN_CUDA(cudaStreamWaitEvent(aux, f.ready, 0));
+  return GNN_OK;
+}
+
+static gnn_status join_from(Fork& f, cudaStream_t st, cudaStream_t aux) {
+  GNN_CUDA(cudaEventRecord(f.done, aux));
+  GNN_CUDA(cudaStreamWaitEvent(st, f.done, 0));
+  return GNN_OK;
+}
+
+extern "C" gnn_status gnn_layer_fwd_async(const gnn_csr* csr, const gnn_boundary* bnd,
+                                          const float* H_in, int64_t ldh, int32_t F_in,
+                                          const uint16_t* W, int32_t F_out, int32_t relu,
+                                          uint32_t seed, const uint8_t* packed_prev,
+                                          const float* meta_prev, uint8_t* packed_next,
+                                          float* meta_next, uint16_t* Mb, int64_t ldmb,
+                                          float* H_out, int64_t ldo, void* ws, size_t ws_bytes,
+                                          gnn_stream_t stream, gnn_stream_t aux) {
+  GNN_REQUIRE(csr && bnd, "gnn_layer_fwd_async: csr and boundary required");
+  gnn_status s = check_dims(csr->n, F_in, F_out, "gnn_layer_fwd_async");
+  if (s != GNN_OK) return s;
+  if (csr->n == 0) return GNN_OK;
+  if ((s = check_mb(Mb, ldmb, F_in, "gnn_layer_fwd_async")) != GNN_OK) return s;
+  GNN_REQUIRE(W && H_out && ldo >= F_out && ldo % 4 == 0 && ((uintptr_t)H_out & 15) == 0,
+              "gnn_layer_fwd_async: bad W or H_out");
+  GNN_REQUIRE(bnd->F == F_in, "gnn_layer_fwd_async: boundary offsets must be for F_in");
+  GNN_REQUIRE(bnd->n_slots == 0 ||
+                  (packed_prev && meta_prev && packed_next && meta_next &&
+                   ((uintptr_t)packed_next & 15) == 0 && ((uintptr_t)meta_next & 7) == 0 &&
+                   bnd->slot_node && bnd->slot_bits && bnd->slot_off),
+              "gnn_layer_fwd_async: message buffers required with a boundary");
+  GNN_REQUIRE(ldh >= F_in && ldh % 4 == 0 && H_in && ((uintptr_t)H_in & 15) == 0,
+              "gnn_layer_fwd_async: bad H_in");
+  bool ok;
+  LayerWs w = layer_ws_layout(ws, ws_bytes, *csr, F_in, F_out, &ok);
+  GNN_REQUIRE(ws && ok, "gnn_layer_fwd_async: workspace too small (%zu < %zu)", ws_bytes, w.bytes);
+  cudaStream_t st = as_stream(stream), ax = as_stream(aux);
+  Fork f;
+  if ((s = fork_to(f, st, ax)) != GNN_OK) return s;
+  if (bnd->n_slots > 0) {
+    s = launch_quant_pack(H_in, ldh, F_in, bnd->slot_node, bnd->n_slots, bnd->slot_bits,
+                          bnd->slot_off, seed, packed_next, reinterpret_cast<float2*>(meta_next), ax);
+    if (s != GNN_OK) return s;
+  }
+  s = gnn_spmm_fwd(csr, bnd, H_in, ldh, F_in, packed_prev, meta_prev, nullptr, 0, Mb, ldmb, w.spmm,
+                   spmm_workspace_bytes(*csr, F_in), stream);
+  if (s != GNN_OK) return s;
+  if ((s = dense_fwd_impl(Mb, ldmb, csr->n, F_in, W, F_out, relu, H_out, ldo, w.dense, st)) != GNN_OK)
+    return s;
+  return join_from(f, st, ax);
+}
+
+extern "C" gnn_status gnn_layer_bwd_async(const gnn_csr* csr, const gnn_boundary* bnd,
+                                          const float* dH_out, int64_t ldg, const float* H_out,
+                                          int64_t ldo, int32_t relu, const uint16_t* Mb,
+                                          int64_t ldmb, const uint16_t* W, int32_t F_in,
+                                          int32_t F_out, uint32_t seed,
+                                          const uint8_t* packed_prev, const float* meta_prev,
+                                          uint8_t* packed_next, float* meta_next, float* dW,
+                                          float* dH_in, int64_t ldh, void* ws, size_t ws_bytes,
+                                          gnn_stream_t stream, gnn_stream_t aux) {
+  GNN_REQUIRE(csr && bnd, "gnn_layer_bwd_async: csr and boundary required");
+  gnn_status s = check_dims(csr->n, F_in, F_out, "gnn_layer_bwd_async");
+  if (s != GNN_OK) return s;
+  if (csr->n == 0) return GNN_OK;
+  bool ok;
+  LayerWs w = layer_ws_layout(ws, ws_bytes, *csr, F_in, F_out, &ok);
+  GNN_REQUIRE(ws && ok, "gnn_layer_bwd_async: workspace too small (%zu < %zu)", ws_bytes, w.bytes);
+  GNN_REQUIRE(dW, "gnn_layer_bwd_async: dW is NULL");
+  const int64_t ldm = round_up(F_in, 4);
+  s = gnn_dense_bwd(Mb, ldmb, csr->n, F_in, W, F_out, dH_out, ldg, H_out, ldo, relu,
+                    dH_in ? w.dM : nullptr, ldm, dW, w.dense.wt, w.dense.bytes, stream);
+  if (s != GNN_OK || !dH_in) return s;
+  cudaStream_t st = as_stream(stream), ax = as_stream(aux);
+  Fork f;
+  if ((s = fork_to(f, st, ax)) != GNN_OK) return s;
+  if ((s = gnn_halo_quant_pack(bnd, w.dM, ldm, F_in, seed, packed_next, meta_next, aux)) != GNN_OK)
+    return s;
+  s = gnn_spmm_bwd_local(csr, bnd, w.dM, ldm, F_in, packed_prev, meta_prev, dH_in, ldh, w.spmm,
+                         spmm_workspace_bytes(*csr, F_in), stream);
+  if (s != GNN_OK) return s;
+  return join_from(f, st, ax);
+}

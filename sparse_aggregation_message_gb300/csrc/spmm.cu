@@ -549,6 +549,10 @@ gnn_status launch_halo_quant_pack(const gnn_boundary& b, const float* Gm, int64_
   return GNN_OK;
 }
 
+gnn_status launch_spmm_bwd_local(const gnn_csr& csr, const gnn_boundary& bnd, const float* Gm,
+                                 int64_t ldg, int F, const uint8_t* packed, const float2* meta,
+                                 float* dH, int64_t ldh, float* partial, cudaStream_t st);
+
 gnn_status launch_spmm_bwd(const gnn_csr& csr, const gnn_boundary* bnd, const float* Gm,
                            int64_t ldg, int F, uint32_t seed, uint8_t* packed_ws,
                            float2* meta_ws, float* dH, int64_t ldh, float* partial,
@@ -559,9 +563,16 @@ gnn_status launch_spmm_bwd(const gnn_csr& csr, const gnn_boundary* bnd, const fl
                                  nullptr, partial, dH, ldh, nullptr, 0, st);
   gnn_status s = launch_halo_quant_pack(*bnd, Gm, ldg, F, seed, packed_ws, meta_ws, st);
   if (s != GNN_OK) return s;
-  SlotMsgs msg{packed_ws, meta_ws, bnd->slot_off, bnd->slot_bits};
-  return dispatch_rows<kBwdOwned>(csr, bnd->col_remap, bnd->val_remap, bnd->local_cnt, Gm, ldg, F,
-                                  msg, bnd->own_ptr, bnd->own_slot, partial, dH, ldh, nullptr, 0, st);
+  return launch_spmm_bwd_local(csr, *bnd, Gm, ldg, F, packed_ws, meta_ws, dH, ldh, partial, st);
+}
+
+gnn_status launch_spmm_bwd_local(const gnn_csr& csr, const gnn_boundary& bnd, const float* Gm,
+                                 int64_t ldg, int F, const uint8_t* packed, const float2* meta,
+                                 float* dH, int64_t ldh, float* partial, cudaStream_t st) {
+  if (csr.n == 0) return GNN_OK;
+  SlotMsgs msg{packed, meta, bnd.slot_off, bnd.slot_bits};
+  return dispatch_rows<kBwdOwned>(csr, bnd.col_remap, bnd.val_remap, bnd.local_cnt, Gm, ldg, F, msg,
+                                  bnd.own_ptr, bnd.own_slot, partial, dH, ldh, nullptr, 0, st);
 }
 
 size_t spmm_workspace_bytes(const gnn_csr& csr, int F) {
@@ -737,4 +748,54 @@ extern "C" gnn_status gnn_spmm_fwd_noalloc(const gnn_csr* csr, const gnn_boundar
   if ((st = noalloc_scratch(&scratch)) != GNN_OK) return st;
   return launch_spmm_fwd(*csr, bnd, H, ldh, F, packed, reinterpret_cast<const float2*>(meta), M,
                          ldm, Mb, ldmb, scratch, as_stream(stream));
+}
+
+extern "C" gnn_status gnn_halo_quant_pack(const gnn_boundary* bnd, const float* G, int64_t ldg,
+                                          int32_t F, uint32_t seed, uint8_t* packed, float* meta,
+                                          gnn_stream_t stream) {
+  GNN_REQUIRE(bnd, "gnn_halo_quant_pack: boundary is NULL");
+  GNN_REQUIRE(F >= 1, "gnn_halo_quant_pack: F must be >= 1");
+  if (F > kMaxF) return fail(GNN_ERR_UNSUPPORTED, "gnn_halo_quant_pack: F=%d > %d", F, kMaxF);
+  GNN_REQUIRE(bnd->F == F, "gnn_halo_quant_pack: boundary offsets are for F=%d, call has F=%d",
+              bnd->F, F);
+  if (bnd->n_slots == 0) return GNN_OK;
+  GNN_REQUIRE(bnd->slot_rowptr && bnd->slot_bits && bnd->slot_off &&
+                  (bnd->nnz_cut == 0 || (bnd->slot_col && bnd->slot_val)),
+              "gnn_halo_quant_pack: boundary arrays are NULL");
+  GNN_REQUIRE(bnd->long_slot_len == 0 ||
+                  (bnd->long_slot_len >= 32 && bnd->n_long_slots >= 0 &&
+                   (bnd->n_long_slots == 0 || bnd->long_slots)),
+              "gnn_halo_quant_pack: incomplete long-slot list");
+  GNN_REQUIRE(G && ldg >= F && ldg % 4 == 0 && ((uintptr_t)G & 15) == 0,
+              "gnn_halo_quant_pack: ldg must be >= F, a multiple of 4, G 16-byte aligned");
+  GNN_REQUIRE(packed && meta && ((uintptr_t)packed & 15) == 0 && ((uintptr_t)meta & 7) == 0,
+              "gnn_halo_quant_pack: packed (16-byte aligned) and meta required");
+  return launch_halo_quant_pack(*bnd, G, ldg, F, seed, packed, reinterpret_cast<float2*>(meta),
+                                as_stream(stream));
+}
+
+extern "C" gnn_status gnn_spmm_bwd_local(const gnn_csr* csr, const gnn_boundary* bnd,
+                                         const float* G, int64_t ldg, int32_t F,
+                                         const uint8_t* packed, const float* meta, float* dH,
+                                         int64_t ldh, void* ws, size_t ws_bytes,
+                                         gnn_stream_t stream) {
+  gnn_status st = check_csr(csr, "gnn_spmm_bwd_local");
+  if (st != GNN_OK) return st;
+  GNN_REQUIRE(bnd, "gnn_spmm_bwd_local: boundary is NULL (use gnn_spmm_bwd)");
+  GNN_REQUIRE(F >= 1, "gnn_spmm_bwd_local: F must be >= 1");
+  if (F > kMaxF) return fail(GNN_ERR_UNSUPPORTED, "gnn_spmm_bwd_local: F=%d > %d", F, kMaxF);
+  if (!csr->symmetric)
+    return fail(GNN_ERR_UNSUPPORTED, "gnn_spmm_bwd_local: needs a symmetric CSR (A^T = A)");
+  if ((st = check_bnd(csr, bnd, F, true, "gnn_spmm_bwd_local")) != GNN_OK) return st;
+  if ((st = check_ws(csr, F, ws, ws_bytes, "gnn_spmm_bwd_local")) != GNN_OK) return st;
+  if (csr->n == 0) return GNN_OK;
+  GNN_REQUIRE(G && dH, "gnn_spmm_bwd_local: NULL G or dH");
+  GNN_REQUIRE(ldg >= F && ldg % 4 == 0 && ((uintptr_t)G & 15) == 0,
+              "gnn_spmm_bwd_local: ldg must be >= F, a multiple of 4, G 16-byte aligned");
+  GNN_REQUIRE(ldh >= F && ldh % 4 == 0 && ((uintptr_t)dH & 15) == 0,
+              "gnn_spmm_bwd_local: ldh must be >= F, a multiple of 4, dH 16-byte aligned");
+  GNN_REQUIRE(bnd->n_slots == 0 || (packed && meta && ((uintptr_t)packed & 15) == 0),
+              "gnn_spmm_bwd_local: packed (16-byte aligned) and meta required");
+  return launch_spmm_bwd_local(*csr, *bnd, G, ldg, F, packed, reinterpret_cast<const float2*>(meta),
+                               dH, ldh, static_cast<float*>(ws), as_stream(stream));
 }
