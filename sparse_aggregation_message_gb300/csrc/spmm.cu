@@ -45,33 +45,22 @@ struct RowSplit {
   const int64_t* piece_beg;
 };
 
-// acc += sum over entries [beg, end) of val * x.  Local entries gather H[col];
-// with REMOTE, every entry is a remote slot (~s) whose dequantised message is
-// read from the packed buffer.  The group covers chunks c0 + gl + i*G (i <
-// CPL) below c_end.  One accumulator per chunk; U entries are gathered before
-// they are added, so U*CPL 16-byte loads per lane are in flight.
-template <int G, int CPL, bool REMOTE, int U>
-__device__ __forceinline__ void gather_range(int64_t beg, int64_t end, const int32_t* __restrict__ col,
+// acc += sum over local entries [beg, end) of val * H[col].  The group covers
+// chunks c0 + gl + i*G (i < CPL) below c_end.  One accumulator per chunk; U
+// entries are gathered before they are added, so U*CPL 16-byte loads per lane
+// are in flight.
+template <int G, int CPL, int U>
+__device__ __forceinline__ void gather_local(int64_t beg, int64_t end, const int32_t* __restrict__ col,
                                              const float* __restrict__ val,
                                              const float4* __restrict__ H4, int64_t ldh4, int c0,
-                                             int c_end, const SlotMsgs& msg, int gl, uint32_t gmask,
-                                             float4 (&acc)[CPL]) {
+                                             int c_end, int gl, uint32_t gmask, float4 (&acc)[CPL]) {
   for (int64_t base = beg; base < end; base += G) {
     const int64_t e = base + gl;
     int cc = 0;
     float w = 0.f;
-    int sb = 0;
-    uint32_t so16 = 0;
-    float2 sm = make_float2(0.f, 0.f);
     if (e < end) {
       cc = __ldg(col + e);
       w = __ldg(val + e);
-      if (REMOTE) {
-        const int s = ~cc;
-        sb = __ldg(msg.bits + s);
-        so16 = (uint32_t)(__ldg(msg.off + s) >> 4);
-        sm = __ldg(msg.meta + s);
-      }
     }
     const int cnt = (int)min((int64_t)G, end - base);
     for (int k = 0; k < cnt; k += U) {
@@ -82,32 +71,108 @@ __device__ __forceinline__ void gather_range(int64_t beg, int64_t end, const int
         const bool valid = k + u < cnt;
         const int src = valid ? k + u : k;
         wk[u] = valid ? __shfl_sync(gmask, w, src, G) : 0.f;
-        if (REMOTE) {
-          const int bk = __shfl_sync(gmask, sb, src, G);
-          const uint32_t ok = __shfl_sync(gmask, so16, src, G);
-          const float mnk = __shfl_sync(gmask, sm.x, src, G);
-          const float sck = __shfl_sync(gmask, sm.y, src, G);
+        const int ck = __shfl_sync(gmask, cc, src, G);
 #pragma unroll
-          for (int i = 0; i < CPL; ++i) {
-            const int c = c0 + gl + i * G;
-            x[u][i] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (valid && c < c_end)
-              x[u][i] = dequant_chunk(msg.packed + ((size_t)ok << 4), bk, mnk, sck, c);
-          }
-        } else {
-          const int ck = __shfl_sync(gmask, cc, src, G);
-#pragma unroll
-          for (int i = 0; i < CPL; ++i) {
-            const int c = c0 + gl + i * G;
-            x[u][i] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (valid && c < c_end) x[u][i] = __ldg(H4 + (int64_t)ck * ldh4 + c);
-          }
+        for (int i = 0; i < CPL; ++i) {
+          const int c = c0 + gl + i * G;
+          x[u][i] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (valid && c < c_end) x[u][i] = __ldg(H4 + (int64_t)ck * ldh4 + c);
         }
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
 #pragma unroll
         for (int i = 0; i < CPL; ++i) fma4(acc[i], wk[u], x[u][i]);
+      }
+    }
+  }
+}
+
+// acc += sum over remote entries [beg, end) (slot ~col) of val * the slot's
+// dequantised message.  The G lanes load G entries' (val, slot width, offset,
+// meta) in one coalesced step and broadcast them with shuffles; a round then
+// loads, for UR entries, the one 32-bit word that holds each chunk's four
+// codes (widths 1, 2, 4, 8 never straddle a word) before it dequantises and
+// adds them in entry order -- one register per chunk in flight instead of
+// four.  A round that meets a raw fp32 slot (width 32) reads float4 chunks.
+template <int G, int CPL, int UR>
+__device__ __forceinline__ void gather_remote(int64_t beg, int64_t end,
+                                                    const int32_t* __restrict__ col,
+                                                    const float* __restrict__ val, int c0,
+                                                    int c_end, const SlotMsgs& msg, int gl,
+                                                    uint32_t gmask, float4 (&acc)[CPL]) {
+  for (int64_t base = beg; base < end; base += G) {
+    const int64_t e = base + gl;
+    float w = 0.f;
+    int sb = 0;
+    uint32_t so16 = 0;
+    float2 sm = make_float2(0.f, 0.f);
+    if (e < end) {
+      const int s = ~__ldg(col + e);
+      w = __ldg(val + e);
+      sb = __ldg(msg.bits + s);
+      so16 = (uint32_t)(__ldg(msg.off + s) >> 4);
+      sm = __ldg(msg.meta + s);
+    }
+    const int cnt = (int)min((int64_t)G, end - base);
+    for (int k = 0; k < cnt; k += UR) {
+      float wk[UR], mnk[UR], sck[UR];
+      int bk[UR];
+      uint32_t ok[UR];
+      bool raw = false;
+#pragma unroll
+      for (int u = 0; u < UR; ++u) {
+        const bool valid = k + u < cnt;
+        const int src = valid ? k + u : k;
+        wk[u] = valid ? __shfl_sync(gmask, w, src, G) : 0.f;
+        bk[u] = __shfl_sync(gmask, sb, src, G);
+        ok[u] = __shfl_sync(gmask, so16, src, G);
+        mnk[u] = __shfl_sync(gmask, sm.x, src, G);
+        sck[u] = __shfl_sync(gmask, sm.y, src, G);
+        raw |= valid && bk[u] == 32;
+      }
+      if (raw) {
+#pragma unroll
+        for (int u = 0; u < UR; ++u) {
+          if (k + u >= cnt) continue;
+#pragma unroll
+          for (int i = 0; i < CPL; ++i) {
+            const int c = c0 + gl + i * G;
+            if (c < c_end)
+              fma4(acc[i], wk[u], dequant_chunk(msg.packed + ((size_t)ok[u] << 4), bk[u], mnk[u], sck[u], c));
+          }
+        }
+        continue;
+      }
+      uint32_t wd[UR][CPL];
+#pragma unroll
+      for (int u = 0; u < UR; ++u) {
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) {
+          const int c = c0 + gl + i * G;
+          wd[u][i] = 0u;
+          if (k + u < cnt && c < c_end) {
+            const uint32_t bitpos = (uint32_t)(4 * c * bk[u]);
+            wd[u][i] = __ldg(reinterpret_cast<const uint32_t*>(msg.packed + ((size_t)ok[u] << 4)) +
+                             (bitpos >> 5));
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < UR; ++u) {
+        const int b = bk[u];
+        const uint32_t m = (1u << b) - 1u;
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) {
+          const int c = c0 + gl + i * G;
+          const uint32_t bits4 = wd[u][i] >> ((uint32_t)(4 * c * b) & 31u);
+          float4 x;
+          x.x = __fadd_rn(__fmul_rn(sck[u], (float)(bits4 & m)), mnk[u]);
+          x.y = __fadd_rn(__fmul_rn(sck[u], (float)((bits4 >> b) & m)), mnk[u]);
+          x.z = __fadd_rn(__fmul_rn(sck[u], (float)((bits4 >> (2 * b)) & m)), mnk[u]);
+          x.w = __fadd_rn(__fmul_rn(sck[u], (float)((bits4 >> (3 * b)) & m)), mnk[u]);
+          fma4(acc[i], wk[u], x);
+        }
       }
     }
   }
@@ -172,9 +237,9 @@ struct Slices {
 #ifndef GNN_ROWS_BLOCK
 #define GNN_ROWS_BLOCK 64
 #endif
-// Entries gathered per round for lanes holding 1 or 2 chunks: local (U; the
-// forward with remote rows has its own, measured best) and remote (UR)
-// entries; the 3-chunk layout gathers 2 of either.
+// Entries gathered per round: local (U, by chunks per lane; the forward with
+// remote rows has its own) and remote (UR) entries, each measured best on the
+// power-law workloads; the 3-chunk layout gathers 2 local entries.
 #ifndef GNN_U1
 #define GNN_U1 6
 #endif
@@ -182,16 +247,19 @@ struct Slices {
 #define GNN_U2 3
 #endif
 #ifndef GNN_U1_FWD
-#define GNN_U1_FWD 8
+#define GNN_U1_FWD 6
 #endif
 #ifndef GNN_U2_FWD
 #define GNN_U2_FWD 4
 #endif
 #ifndef GNN_UR1
-#define GNN_UR1 4
+#define GNN_UR1 3
 #endif
 #ifndef GNN_UR2
 #define GNN_UR2 2
+#endif
+#ifndef GNN_UR3
+#define GNN_UR3 2
 #endif
 // Widest feature slice a group covers (in 16-byte chunks).
 #ifndef GNN_SLICE_CHUNKS
@@ -236,17 +304,12 @@ __global__ void __launch_bounds__(GNN_ROWS_BLOCK, ((MODE == 1 && CPL == 3) ? 768
     end = __ldg(rowptr + row + 1);
     if (sp.T > 0 && end - beg > sp.T) return;  // a long row: its pieces cover it
   }
-  if (MODE == kPlain) {
-    gather_range<G, CPL, false, U>(beg, end, col, val, H4, ldh4, c0, min(c1, nch), msg, gl, gmask, acc);
-  } else {
-    // local entries lead each row, remote slots follow
-    const int64_t mid = (piece ? __ldg(rowptr + row) : beg) + __ldg(local_cnt + row);
-    gather_range<G, CPL, false, U>(beg, min(end, mid), col, val, H4, ldh4, c0, min(c1, nch), msg,
-                                   gl, gmask, acc);
-    if (MODE == kFwdRemote)
-      gather_range<G, CPL, true, UR>(max(beg, mid), end, col, val, H4, ldh4, c0, min(c1, nch), msg,
-                                     gl, gmask, acc);
-  }
+  // local entries lead each row, remote slots follow
+  const int64_t mid =
+      MODE == kPlain ? end : (piece ? __ldg(rowptr + row) : beg) + __ldg(local_cnt + row);
+  gather_local<G, CPL, U>(beg, min(end, mid), col, val, H4, ldh4, c0, min(c1, nch), gl, gmask, acc);
+  if constexpr (MODE == kFwdRemote)
+    gather_remote<G, CPL, UR>(max(beg, mid), end, col, val, c0, min(c1, nch), msg, gl, gmask, acc);
   if (piece) {
     float4* prow = reinterpret_cast<float4*>(partial) + unit * nch;
 #pragma unroll
@@ -480,7 +543,7 @@ static gnn_status dispatch_rows(const gnn_csr& csr, const int32_t* colv, const f
   else if (sl.cs <= 16) GNN_ROWS(16, 1, U1, GNN_UR1);
   else if (cpl == 1) GNN_ROWS(32, 1, U1, GNN_UR1);
   else if (cpl == 2) GNN_ROWS(32, 2, U2, GNN_UR2);
-  else if (cpl == 3) GNN_ROWS(32, 3, 2, 2);
+  else if (cpl == 3) GNN_ROWS(32, 3, 2, GNN_UR3);
   else return fail(GNN_ERR_UNSUPPORTED, "spmm: F=%d exceeds %d", F, kMaxF);
 #undef GNN_ROWS
   return GNN_OK;
