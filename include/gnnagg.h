@@ -231,6 +231,17 @@ gnn_status gnn_quant_pack(const float* X, int64_t ldx, int32_t F,
                           uint32_t seed, uint8_t* packed, float* meta,
                           gnn_stream_t stream);
 
+/* The division (x - min) / scale exactly as the quantiser performs it:
+ * q[i] = a[i] / b[i] rounded to nearest fp32, for verification against
+ * IEEE division.  For 2^-76 <= b <= 2^100 the library forms it from the
+ * reciprocal of b and two fused corrections (Markstein's method); a result
+ * there is exact whenever it is >= 2^-26, and below 2^-25 otherwise (where
+ * the quantiser's code is 0 whatever its last bits).  Other b use the IEEE
+ * divide.  Device pointers, n elements each.  The pages have no counterpart:
+ * it exists so the division the codes depend on can be tested directly. */
+gnn_status gnn_quant_divide(const float* a, const float* b, float* q, int64_t n,
+                            gnn_stream_t stream);
+
 /* Receive side of section 6: out[r][j] = scale*code_j + mn (fp32 multiply,
  * then fp32 add; width 32 copies the stored value). */
 gnn_status gnn_dequant_unpack(const uint8_t* packed, const float* meta,

@@ -22,7 +22,7 @@ __all__ = [
     "rowbytes", "ld_for", "ldb_for", "gnn_dense_workspace", "gnn_dense_fwd", "gnn_dense_bwd",
     "gnn_layer_workspace", "gnn_layer_fwd", "gnn_layer_bwd",
     "gnn_halo_quant_pack", "gnn_spmm_bwd_local", "gnn_layer_fwd_async", "gnn_layer_bwd_async",
-    "LdrState", "gnn_ldr_init", "gnn_ldr_update",
+    "LdrState", "gnn_ldr_init", "gnn_ldr_update", "gnn_quant_divide",
 ]
 
 
@@ -279,6 +279,11 @@ def gnn_quant_pack(X, F: int, row_idx, n_rows: int, row_bits, row_off, seed: int
                    stream=None) -> None:
     call("gnn_quant_pack", _ptr(X), X.stride(0), F, _ptr(row_idx), n_rows, _ptr(row_bits),
          _ptr(row_off), seed & 0xFFFFFFFF, _ptr(packed), _ptr(meta), _stream(stream))
+
+
+def gnn_quant_divide(a, b, q, stream=None) -> None:
+    """q = a / b as the quantiser divides (fp32 tensors of equal size)."""
+    call("gnn_quant_divide", _ptr(a), _ptr(b), _ptr(q), a.numel(), _stream(stream))
 
 
 def gnn_dequant_unpack(packed, meta, row_off, row_bits, n_rows: int, F: int, out,

@@ -103,6 +103,7 @@ PROTOTYPES = {
     "gnn_ldr_init": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_double, c_i32, c_i32, c_i32]),
     "gnn_ldr_update": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_double), c_i32,
                                       ctypes.c_double]),
+    "gnn_quant_divide": (ctypes.c_int, [c_vp, c_vp, c_vp, c_i64, c_vp]),
     "gnn_sync_check": (ctypes.c_int, [c_vp]),
 }
 

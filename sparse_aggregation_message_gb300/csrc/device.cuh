@@ -39,13 +39,46 @@ __device__ __forceinline__ uint32_t rowbytes_dev(int b, int F) {
   return b == 32 ? 16u * ((4u * F + 15u) / 16u) : 16u * ((uint32_t)(F * b + 127) / 128u);
 }
 
+// The quantiser's true division a / b, correctly rounded, with the
+// reciprocal of the row's scale b formed once per row.  Markstein's method
+// (P. Markstein, "Computation of elementary functions on the IBM RISC
+// System/6000 processor", IBM J. Res. Dev. 34(1), 1990): with y = RN(1/b) and
+// a faithful quotient q, the residual r = a - b q is exact and RN(q + r y) is
+// RN(a / b).  q0 = RN(a y) is within 1.5 ulp of a/b; one correction makes it
+// faithful, the second rounds it correctly.  The identity needs the residuals
+// and the reciprocal to stay normal: for 2^-76 <= b <= 2^100 every quotient at
+// or above 2^-26 is exact, and a smaller one stays below 2^-25, where the
+// stochastic rounding gives code 0 whatever its last bits (t + u < 1 - 2^-25
+// for every u <= 1 - 2^-24).  Other b take the IEEE divide.
+struct Divisor {
+  float b, y;
+  bool fast;
+};
+
+__device__ __forceinline__ Divisor make_divisor(float b) {
+  Divisor d;
+  d.b = b;
+  d.fast = b >= 0x1p-76f && b <= 0x1p100f;
+  d.y = d.fast ? __frcp_rn(b) : 0.f;
+  return d;
+}
+
+// FAST: the row's divisor is in the reciprocal method's range (d.fast).
+template <bool FAST>
+__device__ __forceinline__ float div_rn(float a, const Divisor& d) {
+  if (!FAST) return __fdiv_rn(a, d.b);
+  float q = __fmul_rn(a, d.y);
+  q = __fmaf_rn(__fmaf_rn(-d.b, q, a), d.y, q);     // faithful
+  return __fmaf_rn(__fmaf_rn(-d.b, q, a), d.y, q);  // correctly rounded
+}
+
 // Codes of one quantised row at compile-time width B, packed into 32-bit
 // words: the 8/B chunks of a word sit on consecutive lanes of the group and
 // are OR-ed together with shuffles; zero words pad the row to rowbytes(B, F).
 // u_j * 2^24 is an integer below 2^24, so RN(t + u) is formed by one fused
 // multiply-add of that integer by 2^-24 (exact) and t.
-template <int G, int CPL, int B>
-__device__ __forceinline__ void pack_codes(const float4 (&v)[CPL], int F, float mn, float scale,
+template <int G, int CPL, int B, bool FAST>
+__device__ __forceinline__ void pack_codes(const float4 (&v)[CPL], int F, float mn, const Divisor& dv,
                                            bool flat, uint32_t key, uint32_t* __restrict__ words,
                                            int gl, uint32_t gmask) {
   constexpr uint32_t TOP = (1u << B) - 1u;
@@ -62,7 +95,7 @@ __device__ __forceinline__ void pack_codes(const float4 (&v)[CPL], int F, float 
       for (int k = 0; k < 4; ++k) {
         const int j = 4 * c + k;
         if (full || j < F) {
-          const float t = __fdiv_rn(__fsub_rn(elem(v[i], k), mn), scale);
+          const float t = div_rn<FAST>(__fsub_rn(elem(v[i], k), mn), dv);
           const float m = static_cast<float>(fmix32(key ^ (uint32_t)j) >> 8);
           // floor(t + u) >= 0 and below 2^24: round down while converting
           const uint32_t q = min(__float2uint_rd(__fmaf_rn(m, 5.9604644775390625e-08f, t)), TOP);
@@ -129,11 +162,21 @@ __device__ __forceinline__ void quantize_pack_row(const float4 (&v)[CPL], int F,
   const bool flat = !(mx > mn);
   const float scale = flat ? 0.f : __fdiv_rn(__fsub_rn(mx, mn), top);
   uint32_t* words = reinterpret_cast<uint32_t*>(out);
-  switch (b) {
-    case 1: pack_codes<G, CPL, 1>(v, F, mn, scale, flat, key, words, gl, gmask); break;
-    case 2: pack_codes<G, CPL, 2>(v, F, mn, scale, flat, key, words, gl, gmask); break;
-    case 4: pack_codes<G, CPL, 4>(v, F, mn, scale, flat, key, words, gl, gmask); break;
-    default: pack_codes<G, CPL, 8>(v, F, mn, scale, flat, key, words, gl, gmask); break;
+  const Divisor dv = make_divisor(scale);
+  if (dv.fast || flat) {
+    switch (b) {
+      case 1: pack_codes<G, CPL, 1, true>(v, F, mn, dv, flat, key, words, gl, gmask); break;
+      case 2: pack_codes<G, CPL, 2, true>(v, F, mn, dv, flat, key, words, gl, gmask); break;
+      case 4: pack_codes<G, CPL, 4, true>(v, F, mn, dv, flat, key, words, gl, gmask); break;
+      default: pack_codes<G, CPL, 8, true>(v, F, mn, dv, flat, key, words, gl, gmask); break;
+    }
+  } else {
+    switch (b) {
+      case 1: pack_codes<G, CPL, 1, false>(v, F, mn, dv, flat, key, words, gl, gmask); break;
+      case 2: pack_codes<G, CPL, 2, false>(v, F, mn, dv, flat, key, words, gl, gmask); break;
+      case 4: pack_codes<G, CPL, 4, false>(v, F, mn, dv, flat, key, words, gl, gmask); break;
+      default: pack_codes<G, CPL, 8, false>(v, F, mn, dv, flat, key, words, gl, gmask); break;
+    }
   }
   if (gl == 0) *meta = make_float2(mn, scale);
 }

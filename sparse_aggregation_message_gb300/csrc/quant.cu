@@ -49,6 +49,17 @@ __global__ void __launch_bounds__(256) dequant_unpack_kernel(
   for (int c = gl; c < nch; c += G) store_chunk_f32(o, c, F, dequant_chunk(row, b, m.x, m.y, c));
 }
 
+__global__ void __launch_bounds__(256) quant_divide_kernel(const float* __restrict__ a,
+                                                          const float* __restrict__ b,
+                                                          float* __restrict__ q, int64_t n) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x)
+  {
+    const Divisor d = make_divisor(__ldg(b + i));
+    q[i] = d.fast ? div_rn<true>(__ldg(a + i), d) : div_rn<false>(__ldg(a + i), d);
+  }
+}
+
 // Chunk slots a packed row of width 1 (the widest padding) spans.
 static int quant_chunk_slots(int F) { return 32 * ((F + 127) / 128) > (F + 3) / 4 ? 32 * ((F + 127) / 128) : (F + 3) / 4; }
 
@@ -124,6 +135,18 @@ extern "C" gnn_status gnn_quant_pack(const float* X, int64_t ldx, int32_t F, con
               "gnn_quant_pack: X and packed must be 16-byte aligned, meta 8-byte aligned");
   return launch_quant_pack(X, ldx, F, row_idx, n_rows, row_bits, row_off, seed, packed,
                            reinterpret_cast<float2*>(meta), as_stream(stream));
+}
+
+extern "C" gnn_status gnn_quant_divide(const float* a, const float* b, float* q, int64_t n,
+                                       gnn_stream_t stream) {
+  GNN_REQUIRE(n >= 0, "gnn_quant_divide: n < 0");
+  if (n == 0) return GNN_OK;
+  GNN_REQUIRE(a && b && q, "gnn_quant_divide: NULL pointer");
+  int64_t grid = (n + 255) / 256;
+  if (grid > 152 * 32) grid = 152 * 32;
+  quant_divide_kernel<<<(unsigned)grid, 256, 0, as_stream(stream)>>>(a, b, q, n);
+  GNN_CHECK_LAUNCH();
+  return GNN_OK;
 }
 
 extern "C" gnn_status gnn_dequant_unpack(const uint8_t* packed, const float* meta,
