@@ -188,7 +188,9 @@ def run_gpu(args, rank, world, local_rank):
     wl = make_workload(args.workload)
     n, P, dims, L = wl.n, wl.P, wl.dims, wl.layers
     base = args.base_bits if args.base_bits else wl.base_bits[0]
-    csr = G.gnn_csr_build(n, torch.from_numpy(wl.src).to(dev), torch.from_numpy(wl.dst).to(dev))
+    flags = G.CSR_GCN | (G.CSR_MEAN if args.aggregator == "mean" else 0)
+    csr = G.gnn_csr_build(n, torch.from_numpy(wl.src).to(dev), torch.from_numpy(wl.dst).to(dev),
+                          flags)
     csr = G.gnn_csr_split(csr, args.split_len)
     rule = G.BitRule(wl.rule_pct, wl.rule_bits)
     F0 = dims[0]
@@ -471,15 +473,17 @@ class OracleBaseline:
     first layer width.  Rates use the same algorithmic byte model as the GPU
     arm, scaled by the fraction of rows processed."""
 
-    def __init__(self, workload):
+    def __init__(self, workload, aggregator="gcn"):
         import oracle as O
         from synth import make_workload
 
         self.O = O
         wl = make_workload(workload)
         self.n = n = wl.n
-        self.rp, self.col, self.val = O.csr_build(n, wl.src, wl.dst)
-        self.b = O.boundary_index(n, self.rp, self.col, self.val, wl.P)
+        flags = O.FLAGS_GCN | (O.FLAG_MEAN if aggregator == "mean" else 0)
+        self.rp, self.col, self.val = O.csr_build(n, wl.src, wl.dst, flags)
+        vt = O.transpose_values(n, self.rp, self.col, self.val) if aggregator == "mean" else None
+        self.b = O.boundary_index(n, self.rp, self.col, self.val, wl.P, vt)
         nb = O.node_bits(n, self.rp, self.b, wl.rule_pct, wl.rule_bits, wl.base_bits[0])
         self.sb = nb[self.b["slot_node"]]
         self.F = F = wl.dims[0]
@@ -520,6 +524,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="yelp", choices=sorted(WORKLOAD_TEXT))
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
+    ap.add_argument("--aggregator", default="gcn", choices=["gcn", "mean"],
+                    help="GCN weights 1/sqrt(d_v d_u) or GraphSAGE mean weights 1/d_v")
     ap.add_argument("--split-len", type=int, default=128)
     ap.add_argument("--base-bits", type=int, default=0,
                     help="epoch base width (1, 2, 4, 8); default: the workload's first")
@@ -543,13 +549,14 @@ def main():
             torch.cuda.set_device(local_rank)
 
     config = {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload,
+              "aggregator": args.aggregator,
               "base_bits": args.base_bits or None,
               "timing": "inputs larger than L2 (no flush); CUDA events on the launching stream",
               "parallelism": f"replicas x{world}"}
 
     if args.impl == "reference":
         if rank == 0:
-            ob = OracleBaseline(args.workload)
+            ob = OracleBaseline(args.workload, args.aggregator)
             per_step = max(1.0, args.cpu_budget / max(1, args.steps))
             for _ in range(args.warmup):
                 ob.sample(0.2)
@@ -626,7 +633,7 @@ def main():
                                "what": "remote sources read the previous step's messages; this "
                                        "step's are packed on a second stream meanwhile"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cb = OracleBaseline(args.workload).sample(args.cpu_budget)
+        cb = OracleBaseline(args.workload, args.aggregator).sample(args.cpu_budget)
         line["cpu_baseline"] = {k: cb[k] for k in ["value", "unit", "cores", "kind", "sample"]}
     if rank == 0:
         print(json.dumps(line), flush=True)

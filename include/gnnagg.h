@@ -62,11 +62,15 @@ unsigned long long gnn_kernel_launches(void);
 #define GNN_CSR_SYMMETRIZE 1u /* add v->u for every u->v                     */
 #define GNN_CSR_DEDUP 2u      /* keep one copy of repeated edges             */
 #define GNN_CSR_SELF_LOOPS 4u /* drop given self-loops, add one per node     */
+#define GNN_CSR_MEAN 8u       /* GraphSAGE mean: weight 1/d_v, not GCN's     */
 
 /* Row v lists the sources u it aggregates (ascending); val[e] is the GCN
- * weight 1/sqrt(d_v d_u), computed in fp64 and rounded to fp32, d = row
- * length including the self-loop.  `symmetric` is 1 when the rows were
- * symmetrised (the backward call requires it). */
+ * weight 1/sqrt(d_v d_u) or, with GNN_CSR_MEAN, the mean weight 1/d_v
+ * (SYLVIE guide section 2: GraphSAGE changes the neighbour aggregation),
+ * computed in fp64 and rounded to fp32, d = row length including the
+ * self-loop.  `symmetric` is 1 when A = A^T (symmetrised GCN weights).  The
+ * backward calls need A^T: A itself when symmetric, else val_t, the weights
+ * of A^T on the same (symmetrised) pattern. */
 typedef struct gnn_csr {
   int32_t n;         /* nodes                                     */
   int32_t symmetric; /* 1 if A = A^T by construction              */
@@ -86,6 +90,10 @@ typedef struct gnn_csr {
   int64_t* piece_ptr; /* [n_long+1] first piece of long row i                */
   int32_t* piece_row; /* [n_pieces] row of piece p                           */
   int64_t* piece_beg; /* [n_pieces] first entry of piece p                   */
+  /* Optional A^T weights (NULL: none).  gnn_csr_build fills a caller buffer
+   * [capacity] here for GNN_CSR_MEAN with GNN_CSR_SYMMETRIZE: entry e of row
+   * u holds A[col[e]][u] = 1/d_col[e].                                      */
+  float* val_t;
 } gnn_csr;
 
 /* Workspace bytes for gnn_csr_build with these sizes. */
@@ -164,6 +172,10 @@ typedef struct gnn_boundary {
   int32_t long_slot_len;
   int32_t n_long_slots;
   int32_t* long_slots;  /* [n_long_slots] ascending                          */
+  /* [nnz] the A^T weights (csr->val_t) in col_remap order; filled by
+   * gnn_boundary_index when both it and csr->val_t are non-NULL, and then
+   * used by the backward calls in place of val_remap (NULL: A symmetric).   */
+  float* val_remap_t;
 } gnn_boundary;
 
 /* Workspace bytes for gnn_boundary_count / _index / _set_bits on this CSR. */

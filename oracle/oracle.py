@@ -42,6 +42,7 @@ U32 = np.uint32
 FLAG_SYMMETRIZE = 1
 FLAG_DEDUP = 2
 FLAG_SELF_LOOPS = 4
+FLAG_MEAN = 8
 FLAGS_GCN = FLAG_SYMMETRIZE | FLAG_DEDUP | FLAG_SELF_LOOPS
 
 
@@ -75,7 +76,10 @@ def sr_uniform(seed, s, j):
 def csr_build(n, src, dst, flags=FLAGS_GCN):
     """Rows are destinations v, columns sources u.  Optionally symmetrise,
     deduplicate and give every node exactly one self-loop.  val = fp32 of
-    1/sqrt(d_v * d_u) computed in fp64, d = row length (self-loop included)."""
+    1/sqrt(d_v * d_u) computed in fp64, d = row length (self-loop included);
+    with FLAG_MEAN the GraphSAGE mean weight 1/d_v instead (section 2 names
+    GraphSAGE's aggregator as the alternative; the mean over N(v) + {v} is
+    the reading taken)."""
     src = np.asarray(src, np.int64)
     dst = np.asarray(dst, np.int64)
     rows, cols = dst, src
@@ -92,8 +96,23 @@ def csr_build(n, src, dst, flags=FLAGS_GCN):
     rowptr = np.zeros(n + 1, np.int64)
     rowptr[1:] = np.cumsum(np.bincount(rows, minlength=n))
     deg = np.diff(rowptr).astype(np.float64)
-    val = (1.0 / np.sqrt(deg[rows] * deg[cols])).astype(F32)
+    if flags & FLAG_MEAN:
+        val = (1.0 / deg[rows]).astype(F32)
+    else:
+        val = (1.0 / np.sqrt(deg[rows] * deg[cols])).astype(F32)
     return rowptr, cols.astype(np.int32), val
+
+
+def transpose_values(n, rowptr, col, val):
+    """A^T on A's own pattern (which must be symmetric): entry e = (v, u)
+    receives the value of entry (u, v)."""
+    rows = csr_rows(rowptr)
+    key = rows * n + col.astype(np.int64)
+    tkey = col.astype(np.int64) * n + rows
+    at = np.searchsorted(key, tkey)
+    assert np.all(at < key.size) and np.array_equal(key[np.minimum(at, key.size - 1)], tkey), \
+        "pattern is not symmetric"
+    return np.asarray(val)[at]
 
 
 def _distinct_sorted(a):
@@ -121,11 +140,12 @@ def part_of(x, starts):
     return np.searchsorted(starts, np.asarray(x, np.int64), side="right") - 1
 
 
-def boundary_index(n, rowptr, col, val, P):
+def boundary_index(n, rowptr, col, val, P, val_t=None):
     """Slots are the pairs (q, u) where a node of partition q aggregates u and
     u is not in q; ordered by q then u.  Each row's entries are listed with
     local sources first (their ids) and remote ones after (~slot), both in CSR
-    order, with the weights in the same order.  Returns a dict of the arrays."""
+    order, with the weights in the same order (and the A^T weights val_t, when
+    given, as val_remap_t).  Returns a dict of the arrays."""
     starts = partition_starts(n, P)
     rows = csr_rows(rowptr)
     col64 = col.astype(np.int64)
@@ -145,6 +165,7 @@ def boundary_index(n, rowptr, col, val, P):
     order = np.lexsort((np.arange(rows.size), cut, rows))
     col_remap = remap_csr[order]
     val_remap = val[order]
+    extra = {} if val_t is None else dict(val_remap_t=np.asarray(val_t)[order])
     local_cnt = np.bincount(rows[~cut], minlength=n).astype(np.int32)
     ev = rows[cut]
     order = np.lexsort((ev, s_of_edge))
@@ -159,7 +180,7 @@ def boundary_index(n, rowptr, col, val, P):
                 send_start=send_start, slot_node=slot_node, col_remap=col_remap,
                 val_remap=val_remap, local_cnt=local_cnt,
                 slot_rowptr=slot_rowptr, slot_col=slot_col, slot_val=slot_val,
-                own_ptr=own_ptr, own_slot=own_slot)
+                own_ptr=own_ptr, own_slot=own_slot, **extra)
 
 
 def importance_counts(deg, pool):
@@ -394,8 +415,10 @@ def slot_partials(bnd, G, F, slots=None):
 
 
 def spmm_bwd(n, rowptr, col, val, G, F, bnd=None, slot_bits=None, seed=0, rows=None, G_msg=None):
-    """dH = A^T G (A symmetric).  With partitions: dH[u] = sum of A_vu G[v]
-    over local v, plus the dequantised halo partials of every slot u owns
+    """dH = A^T G.  With partitions (A's pattern symmetric): dH[u] = sum of
+    A_vu G[v] over local v -- A_vu is val_remap_t when the boundary has it,
+    else A is symmetric and val_remap serves -- plus the dequantised halo
+    partials of every slot u owns
     (each quantised with key s and ``seed``).  fp64 accumulation; returns
     (dH, T) for ``rows`` (default all).  ``G_msg``: the matrix the halo
     partials are formed from (default G; the previous epoch's in an
@@ -413,7 +436,8 @@ def spmm_bwd(n, rowptr, col, val, G, F, bnd=None, slot_bits=None, seed=0, rows=N
     loc = cr >= 0
     src = cr[loc].astype(np.int64)
     uniq, inv = np.unique(src, return_inverse=True)
-    A = sp.csr_matrix((bnd["val_remap"][e][loc].astype(np.float64), (out_row[loc], inv)),
+    wt = bnd["val_remap_t"] if "val_remap_t" in bnd else bnd["val_remap"]
+    A = sp.csr_matrix((wt[e][loc].astype(np.float64), (out_row[loc], inv)),
                       shape=(rows.size, uniq.size))
     Xl = np.asarray(G)[uniq, :F].astype(np.float64)
     dH = A @ Xl

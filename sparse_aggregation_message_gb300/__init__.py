@@ -10,7 +10,8 @@ from dataclasses import dataclass, field
 from typing import Optional, Sequence
 
 from . import _abi
-from ._abi import (CSR_DEDUP, CSR_GCN, CSR_SELF_LOOPS, CSR_SYMMETRIZE, GnnBitRule,  # noqa: F401
+from ._abi import (CSR_DEDUP, CSR_GCN, CSR_MEAN, CSR_SELF_LOOPS, CSR_SYMMETRIZE,  # noqa: F401
+                   GnnBitRule,
                    GnnBoundary, GnnCsr, GnnError, GnnLdrState, call, load)
 
 LdrState = GnnLdrState
@@ -92,13 +93,14 @@ class Csr:
     n_long: int = 0
     n_pieces: int = 0
     split: dict = field(default_factory=dict)
+    val_t: object = None  # A^T weights (mean aggregation); None when A is symmetric
 
     def c(self) -> GnnCsr:
         s = self.split
         return GnnCsr(self.n, int(self.symmetric), self.nnz, _ptr(self.rowptr), _ptr(self.col),
                       _ptr(self.val), self.split_len, self.n_long, self.n_pieces,
                       _ptr(s.get("long_rows")), _ptr(s.get("piece_ptr")), _ptr(s.get("piece_row")),
-                      _ptr(s.get("piece_beg")))
+                      _ptr(s.get("piece_beg")), _ptr(self.val_t))
 
 
 @dataclass
@@ -130,6 +132,7 @@ class Boundary:
         b.slot_off = _ptr(a["slot_off"] if slot_off is None else slot_off)
         b.long_slot_len, b.n_long_slots = self.long_slot_len, self.n_long_slots
         b.long_slots = _ptr(a.get("long_slots"))
+        b.val_remap_t = _ptr(a.get("val_remap_t"))
         return b
 
 
@@ -139,7 +142,8 @@ def _workspace(nbytes: int, device):
 
 
 def gnn_csr_build(n: int, src, dst, flags: int = CSR_GCN, stream=None) -> Csr:
-    """Edge list (int32 device tensors) -> Csr with GCN weights."""
+    """Edge list (int32 device tensors) -> Csr with GCN weights (or mean
+    weights with CSR_MEAN, plus the A^T weights when symmetrised)."""
     torch = _torch()
     dev = src.device
     m = int(src.numel())
@@ -150,12 +154,15 @@ def gnn_csr_build(n: int, src, dst, flags: int = CSR_GCN, stream=None) -> Csr:
     rowptr = torch.empty(n + 1, dtype=torch.int64, device=dev)
     col = torch.empty(max(cap, 1), dtype=torch.int32, device=dev)
     val = torch.empty(max(cap, 1), dtype=torch.float32, device=dev)
+    want_t = bool(flags & CSR_MEAN) and bool(flags & CSR_SYMMETRIZE)
+    val_t = torch.empty(max(cap, 1), dtype=torch.float32, device=dev) if want_t else None
     out = GnnCsr(n, 0, 0, rowptr.data_ptr(), col.data_ptr(), val.data_ptr())
+    out.val_t = _ptr(val_t)
     call("gnn_csr_build", n, m, _ptr(src), _ptr(dst), flags, cap, ctypes.byref(out), _ptr(ws),
          ws.numel(), _stream(stream))
     nnz = int(out.nnz)
     return Csr(n=n, nnz=nnz, symmetric=bool(out.symmetric), rowptr=rowptr, col=col[:nnz],
-               val=val[:nnz])
+               val=val[:nnz], val_t=val_t[:nnz] if (val_t is not None and out.val_t) else None)
 
 
 def gnn_csr_split(csr: Csr, split_len: int = 512, stream=None) -> Csr:
@@ -176,7 +183,8 @@ def gnn_csr_split(csr: Csr, split_len: int = 512, stream=None) -> Csr:
                  piece_ptr=torch.empty(nl + 1, dtype=torch.int64, device=dev),
                  piece_row=torch.empty(max(npc, 1), dtype=torch.int32, device=dev),
                  piece_beg=torch.empty(max(npc, 1), dtype=torch.int64, device=dev))
-    out = Csr(csr.n, csr.nnz, csr.symmetric, csr.rowptr, csr.col, csr.val, split_len, nl, npc, split)
+    out = Csr(csr.n, csr.nnz, csr.symmetric, csr.rowptr, csr.col, csr.val, split_len, nl, npc, split,
+              csr.val_t)
     c2 = out.c()
     call("gnn_csr_split", ctypes.byref(c2), _ptr(ws), ws.numel(), st)
     return out
@@ -218,13 +226,15 @@ def gnn_boundary_index(csr: Csr, P: int, rule: BitRule, base_bits: int, F: int,
              slot_rowptr=e(S + 1, i64), slot_col=e(nc, i32),
              slot_val=e(nc, f32), own_ptr=e(n + 1, i64), own_slot=e(S, i32), node_bits=e(n, u8),
              slot_bits=e(S, u8), slot_off=e(S + 1, i64))
+    if csr.val_t is not None:
+        a["val_remap_t"] = e(csr.nnz, f32)
     b = Boundary(P=P, n=n, n_slots=S, nnz_cut=nc, F=F, arrays=a)
     cb = b.c()
     call("gnn_boundary_index", ctypes.byref(c), ctypes.byref(rule.to_c()), base_bits, F,
          ctypes.byref(cb), _ptr(ws), ws.numel(), st)
     sizes = dict(part_start=P + 1, send_start=P + 1, slot_node=S, col_remap=csr.nnz,
                  val_remap=csr.nnz, local_cnt=n, slot_rowptr=S + 1, slot_col=nc, slot_val=nc, own_ptr=n + 1, own_slot=S,
-                 node_bits=n, slot_bits=S, slot_off=S + 1)
+                 node_bits=n, slot_bits=S, slot_off=S + 1, val_remap_t=csr.nnz)
     b.arrays = {k: v[:sizes[k]] for k, v in a.items()}
     return b
 

@@ -15,7 +15,7 @@ P_size = ctypes.POINTER(c_size)
 STATUS = {0: "GNN_OK", 1: "GNN_ERR_INVALID_ARG", 2: "GNN_ERR_UNSUPPORTED", 3: "GNN_ERR_CUDA",
           4: "GNN_ERR_DEVICE_CHECK", 5: "GNN_ERR_TIMEOUT", 6: "GNN_ERR_CAPACITY"}
 
-CSR_SYMMETRIZE, CSR_DEDUP, CSR_SELF_LOOPS = 1, 2, 4
+CSR_SYMMETRIZE, CSR_DEDUP, CSR_SELF_LOOPS, CSR_MEAN = 1, 2, 4, 8
 CSR_GCN = CSR_SYMMETRIZE | CSR_DEDUP | CSR_SELF_LOOPS
 
 
@@ -23,7 +23,7 @@ class GnnCsr(ctypes.Structure):
     _fields_ = [("n", c_i32), ("symmetric", c_i32), ("nnz", c_i64), ("rowptr", c_vp),
                 ("col", c_vp), ("val", c_vp), ("split_len", c_i32), ("n_long", c_i32),
                 ("n_pieces", c_i64), ("long_rows", c_vp), ("piece_ptr", c_vp),
-                ("piece_row", c_vp), ("piece_beg", c_vp)]
+                ("piece_row", c_vp), ("piece_beg", c_vp), ("val_t", c_vp)]
 
 
 class GnnBitRule(ctypes.Structure):
@@ -37,7 +37,8 @@ class GnnBoundary(ctypes.Structure):
                 ("slot_rowptr", c_vp),
                 ("slot_col", c_vp), ("slot_val", c_vp), ("own_ptr", c_vp), ("own_slot", c_vp),
                 ("node_bits", c_vp), ("slot_bits", c_vp), ("slot_off", c_vp),
-                ("long_slot_len", c_i32), ("n_long_slots", c_i32), ("long_slots", c_vp)]
+                ("long_slot_len", c_i32), ("n_long_slots", c_i32), ("long_slots", c_vp),
+                ("val_remap_t", c_vp)]
 
 
 GNN_LDR_MAX_DELTA = 64

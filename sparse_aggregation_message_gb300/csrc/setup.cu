@@ -82,9 +82,12 @@ __global__ void csr_rowptr_kernel(int n, const uint64_t* __restrict__ keys, int6
   rowptr[v] = lower_bound_dev(keys, nnz, (uint64_t)v << shift);
 }
 
+// GCN weight 1/sqrt(d_v d_u) or mean weight 1/d_v, in fp64 rounded to fp32;
+// val_t (optional) receives the weight of the transposed entry (u, v).
 __global__ void csr_fill_kernel(const uint64_t* __restrict__ keys, int64_t nnz, int shift,
-                                const int64_t* __restrict__ rowptr, int32_t* __restrict__ col,
-                                float* __restrict__ val) {
+                                const int64_t* __restrict__ rowptr, int mean,
+                                int32_t* __restrict__ col, float* __restrict__ val,
+                                float* __restrict__ val_t) {
   const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= nnz) return;
   const uint64_t k = keys[e];
@@ -93,7 +96,13 @@ __global__ void csr_fill_kernel(const uint64_t* __restrict__ keys, int64_t nnz, 
   col[e] = (int32_t)u;
   const double dv = (double)(rowptr[v + 1] - rowptr[v]);
   const double du = (double)(rowptr[u + 1] - rowptr[u]);
-  val[e] = (float)(1.0 / sqrt(dv * du));
+  if (mean) {
+    val[e] = (float)(1.0 / dv);
+    if (val_t) val_t[e] = (float)(1.0 / du);
+  } else {
+    val[e] = (float)(1.0 / sqrt(dv * du));
+    if (val_t) val_t[e] = val[e];
+  }
 }
 
 struct CsrWs {
@@ -185,8 +194,9 @@ __global__ void cut_remap_kernel(int n, const int64_t* __restrict__ rowptr,
 // group keeping CSR order; weights follow their entries.
 __global__ void reorder_rows_kernel(int n, const int64_t* __restrict__ rowptr,
                                     const int32_t* __restrict__ remap_csr,
-                                    const float* __restrict__ val, int32_t* __restrict__ col_remap,
-                                    float* __restrict__ val_remap, int32_t* __restrict__ local_cnt) {
+                                    const float* __restrict__ val, const float* __restrict__ val_t,
+                                    int32_t* __restrict__ col_remap, float* __restrict__ val_remap,
+                                    float* __restrict__ val_remap_t, int32_t* __restrict__ local_cnt) {
   const int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (v >= n) return;
   const int64_t beg = rowptr[v], end = rowptr[v + 1];
@@ -200,6 +210,7 @@ __global__ void reorder_rows_kernel(int n, const int64_t* __restrict__ rowptr,
     const int64_t at = c >= 0 ? li++ : ri++;
     col_remap[at] = c;
     val_remap[at] = w;
+    if (val_remap_t) val_remap_t[at] = val_t[e];
   }
 }
 
@@ -500,7 +511,7 @@ extern "C" gnn_status gnn_csr_build(int32_t n, int64_t n_edges, const int32_t* s
   GNN_REQUIRE(n_edges == 0 || (src && dst), "gnn_csr_build: NULL edge list");
   GNN_REQUIRE(out->rowptr && (capacity == 0 || (out->col && out->val)),
               "gnn_csr_build: NULL output arrays");
-  GNN_REQUIRE((flags & ~7u) == 0, "gnn_csr_build: unknown flag bits");
+  GNN_REQUIRE((flags & ~15u) == 0, "gnn_csr_build: unknown flag bits");
   cudaStream_t st = as_stream(stream);
   CsrWs w;
   size_t need = 0;
@@ -550,14 +561,19 @@ extern "C" gnn_status gnn_csr_build(int32_t n, int64_t n_edges, const int32_t* s
   }
   out->n = n;
   out->nnz = nnz;
-  out->symmetric = sym ? 1 : 0;
+  const bool mean = flags & GNN_CSR_MEAN;
+  out->symmetric = sym && !mean ? 1 : 0;
+  // A^T weights exist on the pattern only when it is symmetric
+  float* val_t = sym && mean ? out->val_t : nullptr;
+  if (!(sym && mean)) out->val_t = nullptr;
   if (nnz > capacity)
     return fail(GNN_ERR_CAPACITY, "gnn_csr_build: %lld entries exceed capacity %lld",
                 (long long)nnz, (long long)capacity);
   csr_rowptr_kernel<<<GRID1((int64_t)n + 1), 0, st>>>(n, sorted, nnz, shift, out->rowptr);
   GNN_CHECK_LAUNCH();
   if (nnz > 0) {
-    csr_fill_kernel<<<GRID1(nnz), 0, st>>>(sorted, nnz, shift, out->rowptr, out->col, out->val);
+    csr_fill_kernel<<<GRID1(nnz), 0, st>>>(sorted, nnz, shift, out->rowptr, mean ? 1 : 0,
+                                           out->col, out->val, val_t);
     GNN_CHECK_LAUNCH();
   }
   GNN_CUDA(cudaStreamSynchronize(st));
@@ -641,8 +657,10 @@ extern "C" gnn_status gnn_boundary_index(const gnn_csr* csr, const gnn_bit_rule*
   }
   bound_ptr_kernel<<<GRID1(S + 1), 0, st>>>(w.k3, nc, shift, S, out->slot_rowptr);
   GNN_CHECK_LAUNCH();
-  reorder_rows_kernel<<<GRID1(n), 0, st>>>(n, csr->rowptr, remap_csr, csr->val, out->col_remap,
-                                           out->val_remap, out->local_cnt);
+  float* vrt = csr->val_t ? out->val_remap_t : nullptr;
+  if (!csr->val_t) out->val_remap_t = nullptr;
+  reorder_rows_kernel<<<GRID1(n), 0, st>>>(n, csr->rowptr, remap_csr, csr->val, csr->val_t,
+                                           out->col_remap, out->val_remap, vrt, out->local_cnt);
   GNN_CHECK_LAUNCH();
   // owner lists keyed (u, s)
   if (S > 0) {

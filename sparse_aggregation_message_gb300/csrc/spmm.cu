@@ -622,8 +622,8 @@ gnn_status launch_spmm_bwd(const gnn_csr& csr, const gnn_boundary* bnd, const fl
                            cudaStream_t st) {
   if (csr.n == 0) return GNN_OK;
   if (!bnd)
-    return dispatch_rows<kPlain>(csr, csr.col, csr.val, nullptr, Gm, ldg, F, SlotMsgs{}, nullptr,
-                                 nullptr, partial, dH, ldh, nullptr, 0, st);
+    return dispatch_rows<kPlain>(csr, csr.col, csr.val_t ? csr.val_t : csr.val, nullptr, Gm, ldg,
+                                 F, SlotMsgs{}, nullptr, nullptr, partial, dH, ldh, nullptr, 0, st);
   gnn_status s = launch_halo_quant_pack(*bnd, Gm, ldg, F, seed, packed_ws, meta_ws, st);
   if (s != GNN_OK) return s;
   return launch_spmm_bwd_local(csr, *bnd, Gm, ldg, F, packed_ws, meta_ws, dH, ldh, partial, st);
@@ -634,7 +634,9 @@ gnn_status launch_spmm_bwd_local(const gnn_csr& csr, const gnn_boundary& bnd, co
                                  float* dH, int64_t ldh, float* partial, cudaStream_t st) {
   if (csr.n == 0) return GNN_OK;
   SlotMsgs msg{packed, meta, bnd.slot_off, bnd.slot_bits};
-  return dispatch_rows<kBwdOwned>(csr, bnd.col_remap, bnd.val_remap, bnd.local_cnt, Gm, ldg, F, msg,
+  // row u's local entries weighted by A^T: A[v][u] for each local source v
+  const float* wt = bnd.val_remap_t ? bnd.val_remap_t : bnd.val_remap;
+  return dispatch_rows<kBwdOwned>(csr, bnd.col_remap, wt, bnd.local_cnt, Gm, ldg, F, msg,
                                   bnd.own_ptr, bnd.own_slot, partial, dH, ldh, nullptr, 0, st);
 }
 
@@ -683,6 +685,9 @@ static gnn_status check_bnd(const gnn_csr* csr, const gnn_boundary* b, int F, bo
   if (bwd && (!b->own_ptr || (b->n_slots > 0 && (!b->slot_rowptr || !b->own_slot)) ||
               (b->nnz_cut > 0 && (!b->slot_col || !b->slot_val))))
     return fail(GNN_ERR_INVALID_ARG, "%s: boundary backward arrays are NULL", who);
+  if (bwd && !csr->symmetric && !b->val_remap_t)
+    return fail(GNN_ERR_INVALID_ARG, "%s: A is not symmetric and the boundary has no val_remap_t",
+                who);
   if (bwd && b->long_slot_len > 0 &&
       (b->long_slot_len < 32 || b->n_long_slots < 0 || (b->n_long_slots > 0 && !b->long_slots)))
     return fail(GNN_ERR_INVALID_ARG, "%s: incomplete long-slot list", who);
@@ -729,8 +734,8 @@ extern "C" gnn_status gnn_spmm_bwd(const gnn_csr* csr, const gnn_boundary* bnd, 
   if (st != GNN_OK) return st;
   GNN_REQUIRE(F >= 1, "gnn_spmm_bwd: F must be >= 1");
   if (F > kMaxF) return fail(GNN_ERR_UNSUPPORTED, "gnn_spmm_bwd: F=%d > %d", F, kMaxF);
-  if (!csr->symmetric)
-    return fail(GNN_ERR_UNSUPPORTED, "gnn_spmm_bwd: needs a symmetric CSR (A^T = A)");
+  if (!csr->symmetric && !csr->val_t)
+    return fail(GNN_ERR_UNSUPPORTED, "gnn_spmm_bwd: needs A^T (a symmetric CSR or val_t)");
   if ((st = check_bnd(csr, bnd, F, true, "gnn_spmm_bwd")) != GNN_OK) return st;
   if ((st = check_ws(csr, F, ws, ws_bytes, "gnn_spmm_bwd")) != GNN_OK) return st;
   if (csr->n == 0) return GNN_OK;
@@ -847,8 +852,8 @@ extern "C" gnn_status gnn_spmm_bwd_local(const gnn_csr* csr, const gnn_boundary*
   GNN_REQUIRE(bnd, "gnn_spmm_bwd_local: boundary is NULL (use gnn_spmm_bwd)");
   GNN_REQUIRE(F >= 1, "gnn_spmm_bwd_local: F must be >= 1");
   if (F > kMaxF) return fail(GNN_ERR_UNSUPPORTED, "gnn_spmm_bwd_local: F=%d > %d", F, kMaxF);
-  if (!csr->symmetric)
-    return fail(GNN_ERR_UNSUPPORTED, "gnn_spmm_bwd_local: needs a symmetric CSR (A^T = A)");
+  if (!csr->symmetric && !csr->val_t)
+    return fail(GNN_ERR_UNSUPPORTED, "gnn_spmm_bwd_local: needs A^T (a symmetric CSR or val_t)");
   if ((st = check_bnd(csr, bnd, F, true, "gnn_spmm_bwd_local")) != GNN_OK) return st;
   if ((st = check_ws(csr, F, ws, ws_bytes, "gnn_spmm_bwd_local")) != GNN_OK) return st;
   if (csr->n == 0) return GNN_OK;

@@ -47,8 +47,8 @@ def gpu_graph(n, src, dst, flags=O.FLAGS_GCN, split=0):
     return csr
 
 
-def oracle_boundary(n, rowptr, col, val, P, pct, bits, base, F):
-    b = O.boundary_index(n, rowptr, col, val, P)
+def oracle_boundary(n, rowptr, col, val, P, pct, bits, base, F, val_t=None):
+    b = O.boundary_index(n, rowptr, col, val, P, val_t)
     nb = O.node_bits(n, rowptr, b, pct, bits, base)
     sb = nb[b["slot_node"]] if b["n_slots"] else np.zeros(0, np.uint8)
     b["node_bits"] = nb

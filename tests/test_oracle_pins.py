@@ -477,3 +477,72 @@ def test_quantize_divides_rather_than_multiplies_by_reciprocal():
     kk = np.broadcast_to(k, (R, 256))
     expect = np.where((kk + u).astype(np.float32) >= kk + 1, kk + 1, kk)
     assert np.array_equal(codes, np.minimum(expect, 255).astype(np.uint32))
+
+
+# ------------------------------------------------------------------ mean aggregation (GraphSAGE)
+@pytest.mark.parametrize("n,p,seed", [(7, 0.5, 11), (40, 0.2, 12), (64, 0.08, 13)])
+def test_mean_csr_and_transpose_bruteforce(n, p, seed):
+    """Mean weights are 1/d_v on row v (d with the self-loop); the A^T
+    weights on the same pattern are 1/d_u; for GCN weights A^T = A."""
+    src, dst = erdos_renyi_edges(n, p, seed)
+    rowptr, col, val = O.csr_build(n, src, dst, O.FLAGS_GCN | O.FLAG_MEAN)
+    A = _dense_adj(n, src, dst)
+    deg = A.sum(1)
+    Am = A / deg[:, None].astype(np.float64)
+    for v in range(n):
+        assert list(col[rowptr[v]:rowptr[v + 1]]) == [u for u in range(n) if A[v, u]]
+        for k in range(rowptr[v], rowptr[v + 1]):
+            assert val[k] == np.float32(1.0 / float(deg[v]))
+    vt = O.transpose_values(n, rowptr, col, val)
+    D = _dense_ahat(n, rowptr, col, val)
+    Dt = _dense_ahat(n, rowptr, col, vt)
+    assert np.array_equal(Dt, D.T)
+    assert np.allclose(D, Am, rtol=1e-7, atol=0)
+    r2, c2, v2 = O.csr_build(n, src, dst)
+    assert np.array_equal(O.transpose_values(n, r2, c2, v2), v2)
+
+
+def test_transpose_values_rejects_unsymmetric_pattern():
+    rowptr, col, val = O.csr_build(3, [0, 1], [1, 2], flags=O.FLAG_SELF_LOOPS | O.FLAG_MEAN)
+    with pytest.raises(AssertionError):
+        O.transpose_values(3, rowptr, col, val)
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_mean_reproduces_constant_rows_on_irregular_graphs(seed):
+    """The mean of a constant column is that constant whatever the degrees;
+    GCN weights do not have this property on an irregular graph."""
+    n = 300
+    src, dst = planted_partition_edges(n, 900, 3, 0.8, seed)
+    H = np.full((n, 3), 1.5, np.float32)
+    H[:, 2] = -0.25
+    rowptr, col, val = O.csr_build(n, src, dst, O.FLAGS_GCN | O.FLAG_MEAN)
+    M, _ = O.spmm_fwd(n, rowptr, col, val, H, 3)
+    assert np.allclose(M, H, rtol=2e-7, atol=0)
+    r2, c2, v2 = O.csr_build(n, src, dst)
+    M2, _ = O.spmm_fwd(n, r2, c2, v2, H, 3)
+    assert not np.allclose(M2, H, rtol=1e-3)
+
+
+@pytest.mark.parametrize("P", [2, 5])
+def test_mean_partitioned_backward_is_the_transpose(P):
+    """With raw (32-bit) messages the partitioned backward equals the dense
+    A^T G up to fp32 rounding of the halo partials: the local entries of row
+    u must carry A[v][u] = 1/d_v, not row u's own weight 1/d_u."""
+    n, F = 64, 6
+    src, dst = planted_partition_edges(n, 300, 4, 0.7, 3)
+    rowptr, col, val = O.csr_build(n, src, dst, O.FLAGS_GCN | O.FLAG_MEAN)
+    vt = O.transpose_values(n, rowptr, col, val)
+    b = O.boundary_index(n, rowptr, col, val, P, vt)
+    sb = np.full(b["n_slots"], 32, np.uint8)
+    rng = np.random.default_rng(P)
+    G = rng.standard_normal((n, F)).astype(np.float32)
+    dH, T = O.spmm_bwd(n, rowptr, col, val, G, F, b, sb, seed=1)
+    Dt = _dense_ahat(n, rowptr, col, val).T
+    want = Dt @ G.astype(np.float64)
+    assert np.all(np.abs(dH - want) <= 1e-6 * (np.abs(Dt) @ np.abs(G)) + 1e-9)
+    dH0, _ = O.spmm_bwd(n, rowptr, col, val, G, F)
+    assert np.allclose(dH0, want, atol=1e-12)
+    b_wrong = O.boundary_index(n, rowptr, col, val, P)     # A^T weights missing
+    dHw, _ = O.spmm_bwd(n, rowptr, col, val, G, F, b_wrong, sb, seed=1)
+    assert not np.allclose(dHw, want, atol=1e-4)
