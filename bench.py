@@ -388,6 +388,7 @@ def run_gpu(args, rank, world, local_rank):
         G.gnn_sync_check()
         asy = dict(ms=a.elapsed_time(b) / args.async_steps)
         del fwd_msgs, bwd_msgs
+        torch.cuda.empty_cache()
 
     # e2e through the layer API with host buffers: every step copies its inputs
     # (layer-1 features, upstream gradient) from pinned host memory and reads
@@ -402,7 +403,8 @@ def run_gpu(args, rank, world, local_rank):
         g_in = torch.empty((n, ld[L]), dtype=torch.float32, pin_memory=True)
         g_in.copy_(dH[L].cpu())
         dW_host = [torch.empty(dW[l].shape, dtype=torch.float32, pin_memory=True) for l in range(L)]
-        bufs = [(torch.empty_like(H[0]), torch.empty_like(dH[L])) for _ in range(2)]
+        # two input buffers: the step's own H[0] / dH[L] and one more
+        bufs = [(H[0], dH[L]), (torch.empty_like(H[0]), torch.empty_like(dH[L]))]
         copy_stream = torch.cuda.Stream(dev)
         copied = [torch.cuda.Event() for _ in range(2)]
         used = [torch.cuda.Event() for _ in range(2)]
