@@ -409,6 +409,37 @@ gnn_status gnn_layer_bwd_async(const gnn_csr* csr, const gnn_boundary* bnd,
                                int64_t ldh, void* ws, size_t ws_bytes, gnn_stream_t stream,
                                gnn_stream_t aux);
 
+/* Transform-first layers.  SYLVIE guide section 2 writes the GCN layer as
+ * z_v = sum_u 1/sqrt(d_v d_u) W h_u: the transform may run before the
+ * aggregation, A (H W) = (A H) W, and then the aggregation and the boundary
+ * messages are F_out wide instead of F_in -- fewer bytes when F_out < F_in.
+ *
+ * gnn_layer_fwd_tf: Hb = bf16(H_in) (caller buffer [n x ldhb], ldhb >=
+ * round_up(F_in, 16), kept for the backward); Y = Hb W on tcgen05 (fp32
+ * accumulate, caller buffer [n x ldy], ldy >= round_up(F_out, 4)); Y's
+ * boundary rows are quantised and packed (bnd offsets for width F_out, key
+ * s, `seed`); H_out = act(A Y) with the dequantised messages for remote
+ * sources, fp32.  bnd may be NULL (no partitions).
+ *
+ * gnn_layer_bwd_tf: dZ = dH_out * 1[H_out > 0] (relu) in fp32; dY = A^T dZ
+ * with the backward messages at width F_out (as gnn_spmm_bwd); then
+ * dW = Hb^T bf16(dY) and, unless dH_in is NULL, dH_in = bf16(dY) W^T.
+ * F_out: a multiple of 16, at most 256; workspace from
+ * gnn_layer_tf_workspace. */
+gnn_status gnn_layer_tf_workspace(const gnn_csr* csr, int32_t F_in, int32_t F_out,
+                                  size_t* ws_bytes);
+gnn_status gnn_layer_fwd_tf(const gnn_csr* csr, const gnn_boundary* bnd, const float* H_in,
+                            int64_t ldh, int32_t F_in, const uint16_t* W, int32_t F_out,
+                            int32_t relu, uint32_t seed, uint8_t* packed_ws, float* meta_ws,
+                            uint16_t* Hb, int64_t ldhb, float* Y, int64_t ldy, float* H_out,
+                            int64_t ldo, void* ws, size_t ws_bytes, gnn_stream_t stream);
+gnn_status gnn_layer_bwd_tf(const gnn_csr* csr, const gnn_boundary* bnd, const float* dH_out,
+                            int64_t ldg, const float* H_out, int64_t ldo, int32_t relu,
+                            const uint16_t* Hb, int64_t ldhb, const uint16_t* W, int32_t F_in,
+                            int32_t F_out, uint32_t seed, uint8_t* packed_ws, float* meta_ws,
+                            float* dW, float* dH_in, int64_t ldh, void* ws, size_t ws_bytes,
+                            gnn_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Epoch control (SYLVIE guide, sections 8 and 11).  Host code.              */
 /* ------------------------------------------------------------------------ */

@@ -24,6 +24,7 @@ __all__ = [
     "gnn_layer_workspace", "gnn_layer_fwd", "gnn_layer_bwd",
     "gnn_halo_quant_pack", "gnn_spmm_bwd_local", "gnn_layer_fwd_async", "gnn_layer_bwd_async",
     "LdrState", "gnn_ldr_init", "gnn_ldr_update", "gnn_quant_divide",
+    "gnn_layer_tf_workspace", "gnn_layer_fwd_tf", "gnn_layer_bwd_tf",
 ]
 
 
@@ -457,6 +458,43 @@ def gnn_layer_bwd_async(csr: Csr, bnd: Boundary, dH_out, H_out, relu: bool, Mb, 
          _ptr(packed_next), _ptr(meta_next), _ptr(dW), _ptr(dH_in),
          dH_in.stride(0) if dH_in is not None else 0, _ptr(ws), ws.numel(), _stream(stream),
          aux.cuda_stream)
+
+
+# ---------------------------------------------------------------- transform-first layers
+def gnn_layer_tf_workspace(csr: Csr, F_in: int, F_out: int) -> int:
+    nb = ctypes.c_size_t()
+    c = csr.c()
+    call("gnn_layer_tf_workspace", ctypes.byref(c), F_in, F_out, ctypes.byref(nb))
+    return nb.value
+
+
+def gnn_layer_fwd_tf(csr: Csr, bnd: Optional[Boundary], H_in, F_in: int, W, F_out: int,
+                     relu: bool, seed: int, packed_ws, meta_ws, Hb, Y, H_out, slot_off=None,
+                     ws=None, stream=None) -> None:
+    """Y = bf16(H_in) W, messages from Y, H_out = act(A Y) (aggregation at
+    width F_out; bnd offsets for F_out)."""
+    c = csr.c()
+    cb = bnd.c(slot_off, F_out if slot_off is not None else None) if bnd is not None else None
+    if ws is None:
+        ws = _workspace(gnn_layer_tf_workspace(csr, F_in, F_out), H_in.device)
+    call("gnn_layer_fwd_tf", ctypes.byref(c), ctypes.byref(cb) if cb is not None else None,
+         _ptr(H_in), H_in.stride(0), F_in, _ptr(W), F_out, int(relu), seed & 0xFFFFFFFF,
+         _ptr(packed_ws), _ptr(meta_ws), _ptr(Hb), Hb.stride(0), _ptr(Y), Y.stride(0), _ptr(H_out),
+         H_out.stride(0), _ptr(ws), ws.numel(), _stream(stream))
+
+
+def gnn_layer_bwd_tf(csr: Csr, bnd: Optional[Boundary], dH_out, H_out, relu: bool, Hb, W,
+                     F_in: int, F_out: int, seed: int, packed_ws, meta_ws, dW, dH_in=None,
+                     slot_off=None, ws=None, stream=None) -> None:
+    c = csr.c()
+    cb = bnd.c(slot_off, F_out if slot_off is not None else None) if bnd is not None else None
+    if ws is None:
+        ws = _workspace(gnn_layer_tf_workspace(csr, F_in, F_out), dH_out.device)
+    call("gnn_layer_bwd_tf", ctypes.byref(c), ctypes.byref(cb) if cb is not None else None,
+         _ptr(dH_out), dH_out.stride(0), _ptr(H_out), H_out.stride(0) if H_out is not None else 0,
+         int(relu), _ptr(Hb), Hb.stride(0), _ptr(W), F_in, F_out, seed & 0xFFFFFFFF,
+         _ptr(packed_ws), _ptr(meta_ws), _ptr(dW), _ptr(dH_in),
+         dH_in.stride(0) if dH_in is not None else 0, _ptr(ws), ws.numel(), _stream(stream))
 
 
 # ---------------------------------------------------------------- epoch control (host only)

@@ -101,6 +101,13 @@ PROTOTYPES = {
     "gnn_layer_bwd_async": (ctypes.c_int, [P_csr, P_bnd, c_vp, c_i64, c_vp, c_i64, c_i32, c_vp, c_i64,
                                            c_vp, c_i32, c_i32, c_u32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
                                            c_i64, c_vp, c_size, c_vp, c_vp]),
+    "gnn_layer_tf_workspace": (ctypes.c_int, [P_csr, c_i32, c_i32, P_size]),
+    "gnn_layer_fwd_tf": (ctypes.c_int, [P_csr, P_bnd, c_vp, c_i64, c_i32, c_vp, c_i32, c_i32, c_u32,
+                                        c_vp, c_vp, c_vp, c_i64, c_vp, c_i64, c_vp, c_i64, c_vp, c_size,
+                                        c_vp]),
+    "gnn_layer_bwd_tf": (ctypes.c_int, [P_csr, P_bnd, c_vp, c_i64, c_vp, c_i64, c_i32, c_vp, c_i64,
+                                        c_vp, c_i32, c_i32, c_u32, c_vp, c_vp, c_vp, c_vp, c_i64,
+                                        c_vp, c_size, c_vp]),
     "gnn_ldr_init": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_double, c_i32, c_i32, c_i32]),
     "gnn_ldr_update": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_double), c_i32,
                                       ctypes.c_double]),

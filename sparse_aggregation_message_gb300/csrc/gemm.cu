@@ -371,6 +371,50 @@ __global__ void relu_mask_bf16_kernel(int64_t n, int F, const float* __restrict_
   *reinterpret_cast<uint2*>(dZ + r * ldz + c) = p;
 }
 
+// Xb = bf16(X) (nearest-even), columns F..ldb-1 zero.
+__global__ void cast_bf16_kernel(int64_t n, int F, const float* __restrict__ X, int64_t ldx,
+                                 __nv_bfloat16* __restrict__ Xb, int64_t ldb) {
+  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int per_row = (int)(ldb / 4);
+  if (idx >= n * per_row) return;
+  const int64_t r = idx / per_row;
+  const int c = (int)(idx % per_row) * 4;
+  float v[4] = {0.f, 0.f, 0.f, 0.f};
+  if (c < F) {
+    const float4 x4 = *reinterpret_cast<const float4*>(X + r * ldx + c);
+    v[0] = x4.x; v[1] = x4.y; v[2] = x4.z; v[3] = x4.w;
+    for (int k = 0; k < 4; ++k)
+      if (c + k >= F) v[k] = 0.f;
+  }
+  __nv_bfloat162 lo = __floats2bfloat162_rn(v[0], v[1]);
+  __nv_bfloat162 hi = __floats2bfloat162_rn(v[2], v[3]);
+  uint2 p;
+  p.x = *reinterpret_cast<uint32_t*>(&lo);
+  p.y = *reinterpret_cast<uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(Xb + r * ldb + c) = p;
+}
+
+// dZ = dH' * 1[H' > 0] in fp32, columns F..ldz-1 zero.
+__global__ void relu_mask_f32_kernel(int64_t n, int F, const float* __restrict__ dH, int64_t ldg,
+                                     const float* __restrict__ Hout, int64_t ldh,
+                                     float* __restrict__ dZ, int64_t ldz) {
+  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int per_row = (int)(ldz / 4);
+  if (idx >= n * per_row) return;
+  const int64_t r = idx / per_row;
+  const int c = (int)(idx % per_row) * 4;
+  float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (c < F) {
+    v = *reinterpret_cast<const float4*>(dH + r * ldg + c);
+    const float4 h4 = *reinterpret_cast<const float4*>(Hout + r * ldh + c);
+    if (!(h4.x > 0.f) || c >= F) v.x = 0.f;
+    if (!(h4.y > 0.f) || c + 1 >= F) v.y = 0.f;
+    if (!(h4.z > 0.f) || c + 2 >= F) v.z = 0.f;
+    if (!(h4.w > 0.f) || c + 3 >= F) v.w = 0.f;
+  }
+  *reinterpret_cast<float4*>(dZ + r * ldz + c) = v;
+}
+
 // Wt[j][i] = W[i][j] (i < F_in), zero for F_in <= i < K.
 __global__ void transpose_w_kernel(const __nv_bfloat16* __restrict__ W, int F_in, int F_out, int K,
                                    __nv_bfloat16* __restrict__ Wt) {
@@ -538,6 +582,26 @@ gnn_status launch_relu_mask_bf16(int64_t n, int F, const float* dH, int64_t ldg,
   const int64_t total = n * (ldz / 4);
   relu_mask_bf16_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(
       n, F, dH, ldg, Hout, ldh, relu, reinterpret_cast<__nv_bfloat16*>(dZ), ldz);
+  GNN_CHECK_LAUNCH();
+  return GNN_OK;
+}
+
+gnn_status launch_cast_bf16(int64_t n, int F, const float* X, int64_t ldx, uint16_t* Xb,
+                            int64_t ldb, cudaStream_t st) {
+  if (n == 0) return GNN_OK;
+  const int64_t total = n * (ldb / 4);
+  cast_bf16_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(
+      n, F, X, ldx, reinterpret_cast<__nv_bfloat16*>(Xb), ldb);
+  GNN_CHECK_LAUNCH();
+  return GNN_OK;
+}
+
+gnn_status launch_relu_mask_f32(int64_t n, int F, const float* dH, int64_t ldg, const float* Hout,
+                                int64_t ldh, float* dZ, int64_t ldz, cudaStream_t st) {
+  if (n == 0) return GNN_OK;
+  const int64_t total = n * (ldz / 4);
+  relu_mask_f32_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(n, F, dH, ldg, Hout, ldh,
+                                                                        dZ, ldz);
   GNN_CHECK_LAUNCH();
   return GNN_OK;
 }

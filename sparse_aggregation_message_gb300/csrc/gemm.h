@@ -27,6 +27,14 @@ void gemm_mn_plan(int Mi, int Nj, int K, int* splits, int* kb_per_split, int* BN
 gnn_status launch_relu_mask_bf16(int64_t n, int F, const float* dH, int64_t ldg, const float* Hout,
                                  int64_t ldh, int relu, uint16_t* dZ, int64_t ldz, cudaStream_t st);
 
+// Xb = bf16(X) with row stride ldb (a multiple of 4), columns F.. zero.
+gnn_status launch_cast_bf16(int64_t n, int F, const float* X, int64_t ldx, uint16_t* Xb,
+                            int64_t ldb, cudaStream_t st);
+
+// dZ = dH' * 1[H' > 0] in fp32 with row stride ldz (a multiple of 4).
+gnn_status launch_relu_mask_f32(int64_t n, int F, const float* dH, int64_t ldg, const float* Hout,
+                                int64_t ldh, float* dZ, int64_t ldz, cudaStream_t st);
+
 gnn_status launch_transpose_w(const uint16_t* W, int F_in, int F_out, int K, uint16_t* Wt,
                               cudaStream_t st);
 

@@ -18,13 +18,13 @@ gnn_status launch_dequant_unpack(const uint8_t* packed, const float2* meta, cons
                                  int64_t ldo, cudaStream_t st);
 
 // M = A H (bnd NULL) or the partitioned forward aggregation; fp32 and/or bf16
-// outputs (either may be NULL).
+// outputs (either may be NULL), ReLU'd when relu != 0.
 // `partial` holds one fp32 row per piece of csr's split plan (may be NULL
 // without a plan).
 gnn_status launch_spmm_fwd(const gnn_csr& csr, const gnn_boundary* bnd, const float* H,
                            int64_t ldh, int F, const uint8_t* packed, const float2* meta,
                            float* M, int64_t ldm, uint16_t* Mb, int64_t ldmb, float* partial,
-                           cudaStream_t st);
+                           cudaStream_t st, int relu = 0);
 
 gnn_status launch_spmm_bwd(const gnn_csr& csr, const gnn_boundary* bnd, const float* G,
                            int64_t ldg, int F, uint32_t seed, uint8_t* packed_ws,
@@ -40,5 +40,11 @@ gnn_status launch_halo_quant_pack(const gnn_boundary& b, const float* Gm, int64_
                                   cudaStream_t st);
 
 size_t spmm_workspace_bytes(const gnn_csr& csr, int F);
+
+// gnn_spmm_fwd with its argument checks, the output ReLU'd when relu != 0.
+gnn_status spmm_fwd_checked(const gnn_csr* csr, const gnn_boundary* bnd, const float* H,
+                            int64_t ldh, int32_t F, const uint8_t* packed, const float* meta,
+                            float* M, int64_t ldm, uint16_t* Mb, int64_t ldmb, void* ws,
+                            size_t ws_bytes, gnn_stream_t stream, int relu);
 
 }  // namespace gnn

@@ -315,3 +315,126 @@ extern "C" gnn_status gnn_layer_bwd_async(const gnn_csr* csr, const gnn_boundary
   if (s != GNN_OK) return s;
   return join_from(f, st, ax);
 }
+
+// ------------------------------------------------------------------ transform-first layers
+// A (H W) = (A H) W: when F_out < F_in the aggregation (and the message) runs
+// at the narrower width F_out.
+struct TfWs {
+  DenseWs dense;
+  float* dz;  // masked upstream gradient, fp32 [n x round_up(F_out, 4)]
+  float* dy;  // A^T dz, fp32 [n x round_up(F_out, 4)]
+  float* spmm;
+  size_t bytes;
+};
+
+static TfWs tf_ws_layout(void* base, size_t cap, const gnn_csr& csr, int F_in, int F_out, bool* ok) {
+  TfWs w{};
+  bool ok1;
+  DenseWs probe = dense_ws_layout(nullptr, 0, csr.n, F_in, F_out, &ok1);
+  Arena ar(base, cap);
+  void* dbase = ar.take_bytes(probe.bytes);
+  w.dense = dense_ws_layout(dbase, probe.bytes, csr.n, F_in, F_out, &ok1);
+  const size_t ldy = (size_t)round_up(F_out, 4);
+  w.dz = ar.take<float>((size_t)csr.n * ldy);
+  w.dy = ar.take<float>((size_t)csr.n * ldy);
+  const size_t sp = spmm_workspace_bytes(csr, F_out);
+  w.spmm = sp ? reinterpret_cast<float*>(ar.take_bytes(sp)) : nullptr;
+  w.bytes = ar.used;
+  *ok = ar.ok();
+  return w;
+}
+
+extern "C" gnn_status gnn_layer_tf_workspace(const gnn_csr* csr, int32_t F_in, int32_t F_out,
+                                             size_t* ws_bytes) {
+  GNN_REQUIRE(csr && ws_bytes, "gnn_layer_tf_workspace: NULL argument");
+  gnn_status s = check_dims(csr->n, F_in, F_out, "gnn_layer_tf_workspace");
+  if (s != GNN_OK) return s;
+  bool ok;
+  *ws_bytes = tf_ws_layout(nullptr, 0, *csr, F_in, F_out, &ok).bytes;
+  return GNN_OK;
+}
+
+extern "C" gnn_status gnn_layer_fwd_tf(const gnn_csr* csr, const gnn_boundary* bnd,
+                                       const float* H_in, int64_t ldh, int32_t F_in,
+                                       const uint16_t* W, int32_t F_out, int32_t relu,
+                                       uint32_t seed, uint8_t* packed_ws, float* meta_ws,
+                                       uint16_t* Hb, int64_t ldhb, float* Y, int64_t ldy,
+                                       float* H_out, int64_t ldo, void* ws, size_t ws_bytes,
+                                       gnn_stream_t stream) {
+  GNN_REQUIRE(csr, "gnn_layer_fwd_tf: csr is NULL");
+  gnn_status s = check_dims(csr->n, F_in, F_out, "gnn_layer_fwd_tf");
+  if (s != GNN_OK) return s;
+  if (csr->n == 0) return GNN_OK;
+  if ((s = check_mb(Hb, ldhb, F_in, "gnn_layer_fwd_tf")) != GNN_OK) return s;
+  GNN_REQUIRE(H_in && ldh >= F_in && ldh % 4 == 0 && ((uintptr_t)H_in & 15) == 0,
+              "gnn_layer_fwd_tf: bad H_in");
+  GNN_REQUIRE(W && Y && ldy >= round_up(F_out, 4) && ldy % 4 == 0 && ((uintptr_t)Y & 15) == 0,
+              "gnn_layer_fwd_tf: bad W or Y");
+  GNN_REQUIRE(H_out && ldo >= F_out && ldo % 4 == 0 && ((uintptr_t)H_out & 15) == 0,
+              "gnn_layer_fwd_tf: bad H_out");
+  bool ok;
+  TfWs w = tf_ws_layout(ws, ws_bytes, *csr, F_in, F_out, &ok);
+  GNN_REQUIRE(ws && ok, "gnn_layer_fwd_tf: workspace too small (%zu < %zu)", ws_bytes, w.bytes);
+  cudaStream_t st = as_stream(stream);
+  // Y = bf16(H_in) W
+  if ((s = launch_cast_bf16(csr->n, F_in, H_in, ldh, Hb, ldhb, st)) != GNN_OK) return s;
+  if ((s = dense_fwd_impl(Hb, ldhb, csr->n, F_in, W, F_out, 0, Y, ldy, w.dense, st)) != GNN_OK)
+    return s;
+  // the messages are Y's boundary rows
+  if (bnd && bnd->n_slots > 0) {
+    GNN_REQUIRE(bnd->slot_node && bnd->slot_bits && bnd->slot_off && bnd->F == F_out,
+                "gnn_layer_fwd_tf: boundary offsets must be for F_out");
+    GNN_REQUIRE(packed_ws && meta_ws && ((uintptr_t)packed_ws & 15) == 0 && ((uintptr_t)meta_ws & 7) == 0,
+                "gnn_layer_fwd_tf: packed_ws/meta_ws required with a boundary");
+    s = launch_quant_pack(Y, ldy, F_out, bnd->slot_node, bnd->n_slots, bnd->slot_bits,
+                          bnd->slot_off, seed, packed_ws, reinterpret_cast<float2*>(meta_ws), st);
+    if (s != GNN_OK) return s;
+  } else if (bnd) {
+    GNN_REQUIRE(bnd->F == F_out, "gnn_layer_fwd_tf: boundary offsets must be for F_out");
+  }
+  // H_out = act(A Y)
+  return spmm_fwd_checked(csr, bnd, Y, ldy, F_out, packed_ws, meta_ws, H_out, ldo, nullptr, 0,
+                          w.spmm, spmm_workspace_bytes(*csr, F_out), stream, relu);
+}
+
+extern "C" gnn_status gnn_layer_bwd_tf(const gnn_csr* csr, const gnn_boundary* bnd,
+                                       const float* dH_out, int64_t ldg, const float* H_out,
+                                       int64_t ldo, int32_t relu, const uint16_t* Hb,
+                                       int64_t ldhb, const uint16_t* W, int32_t F_in,
+                                       int32_t F_out, uint32_t seed, uint8_t* packed_ws,
+                                       float* meta_ws, float* dW, float* dH_in, int64_t ldh,
+                                       void* ws, size_t ws_bytes, gnn_stream_t stream) {
+  GNN_REQUIRE(csr, "gnn_layer_bwd_tf: csr is NULL");
+  gnn_status s = check_dims(csr->n, F_in, F_out, "gnn_layer_bwd_tf");
+  if (s != GNN_OK) return s;
+  if (csr->n == 0) return GNN_OK;
+  if ((s = check_mb(Hb, ldhb, F_in, "gnn_layer_bwd_tf")) != GNN_OK) return s;
+  GNN_REQUIRE(W && dW, "gnn_layer_bwd_tf: W and dW required");
+  GNN_REQUIRE(dH_out && ldg >= F_out && ldg % 4 == 0 && ((uintptr_t)dH_out & 15) == 0,
+              "gnn_layer_bwd_tf: bad dH_out");
+  GNN_REQUIRE(!relu || (H_out && ldo >= F_out && ldo % 4 == 0 && ((uintptr_t)H_out & 15) == 0),
+              "gnn_layer_bwd_tf: relu needs H_out");
+  GNN_REQUIRE(!dH_in || (ldh >= round_up(F_in, 4) && ldh % 4 == 0 && ((uintptr_t)dH_in & 15) == 0),
+              "gnn_layer_bwd_tf: dH_in needs ldh >= round_up(F_in,4), a multiple of 4");
+  bool ok;
+  TfWs w = tf_ws_layout(ws, ws_bytes, *csr, F_in, F_out, &ok);
+  GNN_REQUIRE(ws && ok, "gnn_layer_bwd_tf: workspace too small (%zu < %zu)", ws_bytes, w.bytes);
+  cudaStream_t st = as_stream(stream);
+  const int64_t ldy = round_up(F_out, 4);
+  // dZ = dH_out * 1[H_out > 0]
+  const float* dz = dH_out;
+  int64_t ldz = ldg;
+  if (relu) {
+    if ((s = launch_relu_mask_f32(csr->n, F_out, dH_out, ldg, H_out, ldo, w.dz, ldy, st)) != GNN_OK)
+      return s;
+    dz = w.dz;
+    ldz = ldy;
+  }
+  // dY = A^T dZ with the backward messages at width F_out
+  s = gnn_spmm_bwd(csr, bnd, dz, ldz, F_out, seed, packed_ws, meta_ws, w.dy, ldy, w.spmm,
+                   spmm_workspace_bytes(*csr, F_out), stream);
+  if (s != GNN_OK) return s;
+  // dW = Hb^T bf16(dY), dH_in = bf16(dY) W^T
+  return dense_bwd_impl(Hb, ldhb, csr->n, F_in, W, F_out, w.dy, ldy, nullptr, 0, 0, dH_in, ldh, dW,
+                        w.dense, st);
+}

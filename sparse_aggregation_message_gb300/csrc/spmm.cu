@@ -199,12 +199,22 @@ __device__ __forceinline__ void add_owned(int64_t r, const int64_t* __restrict__
 }
 
 // Writes the group's chunks of row r: fp32 chunks below nch, bf16 chunks
-// below nch_b (zeros past F), both limited to the group's slice [c0, c1).
+// below nch_b (zeros past F), both limited to the group's slice [c0, c1);
+// with relu, max(x, 0) of each.
 template <int G, int CPL>
-__device__ __forceinline__ void store_row(int64_t r, const float4 (&acc)[CPL], int F, int nch,
+__device__ __forceinline__ void store_row(int64_t r, float4 (&acc)[CPL], int F, int nch,
                                           int nch_b, int c0, int c1, int gl,
                                           float* __restrict__ M, int64_t ldm,
-                                          __nv_bfloat16* __restrict__ Mb, int64_t ldmb) {
+                                          __nv_bfloat16* __restrict__ Mb, int64_t ldmb, int relu) {
+  if (relu) {
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+      acc[i].x = fmaxf(acc[i].x, 0.f);
+      acc[i].y = fmaxf(acc[i].y, 0.f);
+      acc[i].z = fmaxf(acc[i].z, 0.f);
+      acc[i].w = fmaxf(acc[i].w, 0.f);
+    }
+  }
   if (M) {
     float* mrow = M + r * ldm;
 #pragma unroll
@@ -276,7 +286,7 @@ __global__ void __launch_bounds__(GNN_ROWS_BLOCK, ((MODE == 1 && CPL == 3) ? 768
     const float* __restrict__ H, int64_t ldh, int F,
     SlotMsgs msg, const int64_t* __restrict__ own_ptr, const int32_t* __restrict__ own_slot,
     RowSplit sp, Slices sl, float* __restrict__ partial, float* __restrict__ M, int64_t ldm,
-    __nv_bfloat16* __restrict__ Mb, int64_t ldmb, int nch_b) {
+    __nv_bfloat16* __restrict__ Mb, int64_t ldmb, int nch_b, int relu) {
   const int lane = threadIdx.x & 31;
   const int gl = lane & (G - 1);
   const int64_t g = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / G;
@@ -320,7 +330,7 @@ __global__ void __launch_bounds__(GNN_ROWS_BLOCK, ((MODE == 1 && CPL == 3) ? 768
     return;
   }
   if (MODE == kBwdOwned) add_owned<G, CPL>(row, own_ptr, own_slot, msg, c0, min(c1, nch), gl, acc);
-  store_row<G, CPL>(row, acc, F, nch, nch_b, c0, c1, gl, M, ldm, Mb, ldmb);
+  store_row<G, CPL>(row, acc, F, nch, nch_b, c0, c1, gl, M, ldm, Mb, ldmb, relu);
 }
 
 // Long rows: sum of their pieces' partial rows, 16 pieces at a time and then
@@ -330,7 +340,7 @@ __global__ void __launch_bounds__(256) spmm_fixup_kernel(
     RowSplit sp, Slices sl, const float* __restrict__ partial, int F, SlotMsgs msg,
     const int64_t* __restrict__ own_ptr, const int32_t* __restrict__ own_slot,
     float* __restrict__ M, int64_t ldm, __nv_bfloat16* __restrict__ Mb, int64_t ldmb,
-    int nch_b) {
+    int nch_b, int relu) {
   const int lane = threadIdx.x & 31;
   const int gl = lane & (G - 1);
   const int64_t g = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / G;
@@ -361,7 +371,7 @@ __global__ void __launch_bounds__(256) spmm_fixup_kernel(
     for (int k = 0; k < CPL; ++k) add4(acc[k], blk[k]);
   }
   if (MODE == kBwdOwned) add_owned<G, CPL>(row, own_ptr, own_slot, msg, c0, min(c1, nch), gl, acc);
-  store_row<G, CPL>(row, acc, F, nch, nch_b, c0, c1, gl, M, ldm, Mb, ldmb);
+  store_row<G, CPL>(row, acc, F, nch, nch_b, c0, c1, gl, M, ldm, Mb, ldmb, relu);
 }
 
 // Backward messages: halo partial of slot s over its entries in ascending v,
@@ -506,7 +516,7 @@ static gnn_status dispatch_rows(const gnn_csr& csr, const int32_t* colv, const f
                                 const int32_t* local_cnt, const float* H, int64_t ldh, int F,
                                 SlotMsgs msg, const int64_t* own_ptr, const int32_t* own_slot,
                                 float* partial, float* M, int64_t ldm, __nv_bfloat16* Mb,
-                                int64_t ldmb, cudaStream_t st) {
+                                int64_t ldmb, cudaStream_t st, int relu = 0) {
   const int nch = (F + 3) / 4;
   const int nch_b = Mb ? ((F + 15) / 16) * 4 : nch;
   const int need = nch_b > nch ? nch_b : nch;
@@ -525,12 +535,12 @@ static gnn_status dispatch_rows(const gnn_csr& csr, const int32_t* colv, const f
     const int64_t grid = (groups * G_ + block - 1) / block;                                    \
     spmm_rows_kernel<G_, CPL_, MODE, U_, UR_><<<(unsigned)grid, block, 0, st>>>(               \
         csr.n, csr.rowptr, colv, valv, local_cnt, H, ldh, F, msg, own_ptr, own_slot, sp, sl,   \
-        partial, M, ldm, Mb, ldmb, nch_b);                                                     \
+        partial, M, ldm, Mb, ldmb, nch_b, relu);                                               \
     GNN_CHECK_LAUNCH();                                                                        \
     if (sp.n_long > 0) {                                                                       \
       const int64_t g2 = ((int64_t)sp.n_long * sl.ns * G_ + 255) / 256;                        \
       spmm_fixup_kernel<G_, CPL_, MODE><<<(unsigned)g2, 256, 0, st>>>(                         \
-          sp, sl, partial, F, msg, own_ptr, own_slot, M, ldm, Mb, ldmb, nch_b);                \
+          sp, sl, partial, F, msg, own_ptr, own_slot, M, ldm, Mb, ldmb, nch_b, relu);          \
       GNN_CHECK_LAUNCH();                                                                      \
     }                                                                                          \
   } while (0)
@@ -552,15 +562,15 @@ static gnn_status dispatch_rows(const gnn_csr& csr, const int32_t* colv, const f
 gnn_status launch_spmm_fwd(const gnn_csr& csr, const gnn_boundary* bnd, const float* H,
                            int64_t ldh, int F, const uint8_t* packed, const float2* meta,
                            float* M, int64_t ldm, uint16_t* Mb, int64_t ldmb, float* partial,
-                           cudaStream_t st) {
+                           cudaStream_t st, int relu) {
   if (csr.n == 0) return GNN_OK;
   auto* mb = reinterpret_cast<__nv_bfloat16*>(Mb);
   if (!bnd)
     return dispatch_rows<kPlain>(csr, csr.col, csr.val, nullptr, H, ldh, F, SlotMsgs{}, nullptr,
-                                 nullptr, partial, M, ldm, mb, ldmb, st);
+                                 nullptr, partial, M, ldm, mb, ldmb, st, relu);
   SlotMsgs msg{packed, meta, bnd->slot_off, bnd->slot_bits};
   return dispatch_rows<kFwdRemote>(csr, bnd->col_remap, bnd->val_remap, bnd->local_cnt, H, ldh, F,
-                                   msg, nullptr, nullptr, partial, M, ldm, mb, ldmb, st);
+                                   msg, nullptr, nullptr, partial, M, ldm, mb, ldmb, st, relu);
 }
 
 static int quant_chunk_slots(int F) {
@@ -706,6 +716,14 @@ extern "C" gnn_status gnn_spmm_fwd(const gnn_csr* csr, const gnn_boundary* bnd, 
                                    int64_t ldh, int32_t F, const uint8_t* packed,
                                    const float* meta, float* M, int64_t ldm, uint16_t* Mb,
                                    int64_t ldmb, void* ws, size_t ws_bytes, gnn_stream_t stream) {
+  return gnn::spmm_fwd_checked(csr, bnd, H, ldh, F, packed, meta, M, ldm, Mb, ldmb, ws, ws_bytes,
+                               stream, 0);
+}
+
+gnn_status gnn::spmm_fwd_checked(const gnn_csr* csr, const gnn_boundary* bnd, const float* H,
+                                 int64_t ldh, int32_t F, const uint8_t* packed, const float* meta,
+                                 float* M, int64_t ldm, uint16_t* Mb, int64_t ldmb, void* ws,
+                                 size_t ws_bytes, gnn_stream_t stream, int relu) {
   gnn_status st = check_csr(csr, "gnn_spmm_fwd");
   if (st != GNN_OK) return st;
   GNN_REQUIRE(F >= 1, "gnn_spmm_fwd: F must be >= 1");
@@ -723,7 +741,7 @@ extern "C" gnn_status gnn_spmm_fwd(const gnn_csr* csr, const gnn_boundary* bnd, 
   GNN_REQUIRE(!bnd || bnd->n_slots == 0 || (packed && meta),
               "gnn_spmm_fwd: packed/meta required with a boundary");
   return launch_spmm_fwd(*csr, bnd, H, ldh, F, packed, reinterpret_cast<const float2*>(meta), M,
-                         ldm, Mb, ldmb, static_cast<float*>(ws), as_stream(stream));
+                         ldm, Mb, ldmb, static_cast<float*>(ws), as_stream(stream), relu);
 }
 
 extern "C" gnn_status gnn_spmm_bwd(const gnn_csr* csr, const gnn_boundary* bnd, const float* G,
