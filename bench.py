@@ -175,6 +175,19 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------- GPU arm
+def layer_orders(order, dims):
+    """Per layer: True to transform first (aggregate Y = H W at width F_out).
+    "auto" does so where it gathers fewer bytes: the first layer runs one
+    aggregation aggregate-first (its input gradient is never formed) but two
+    transform-first (dY is needed for dW); later layers run two either way."""
+    L = len(dims) - 1
+    if order == "af":
+        return [False] * L
+    if order == "tf":
+        return [dims[l + 1] < dims[l] for l in range(L)]
+    return [2 * dims[l + 1] < dims[l] * (1 if l == 0 else 2) for l in range(L)]
+
+
 def run_gpu(args, rank, world, local_rank):
     import torch
 
@@ -197,7 +210,10 @@ def run_gpu(args, rank, world, local_rank):
     bnd = G.gnn_boundary_index(csr, P, rule, base, F0)
     G.gnn_boundary_long_slots(csr, bnd, args.long_slot_len)
     S = bnd.n_slots
-    widths = sorted(set(dims[:-1]))
+    tf = layer_orders(args.order, dims)
+    # message (and aggregation) width of each layer
+    mwid = [dims[l + 1] if tf[l] else dims[l] for l in range(L)]
+    widths = sorted(set(mwid))
     offs = {F: (bnd.slot_off if F == F0 else G.gnn_slot_offsets(bnd.slot_bits, S, F)) for F in widths}
     Qmax = max(int(offs[F][-1].item()) for F in widths)
     packed = torch.zeros(max(Qmax, 16), dtype=torch.uint8, device=dev)
@@ -214,11 +230,14 @@ def run_gpu(args, rank, world, local_rank):
     W = [torch.from_numpy(make_weight_bf16(dims[l], dims[l + 1], wl.seed, l).view(np.int16)).to(dev)
          for l in range(L)]
     dW = [torch.empty((dims[l], dims[l + 1]), device=dev) for l in range(L)]
+    # transform-first layers keep Y = bf16(H) W (their Mb holds bf16(H))
+    Y = [torch.empty((n, ld[l + 1]), device=dev) if tf[l] else None for l in range(L)]
     # gradients w.r.t. each layer's input; the first layer's is never formed
     dH = [None] + [torch.empty((n, ld[l]), device=dev) for l in range(1, L + 1)]
     dH[L].copy_(torch.randn((n, ld[L]), generator=g, device=dev))
     # workspaces sized for the largest layer
-    ws_layer = max(G.gnn_layer_workspace(csr, dims[l], dims[l + 1]) for l in range(L))
+    ws_layer = max(G.gnn_layer_tf_workspace(csr, dims[l], dims[l + 1]) if tf[l] else
+                   G.gnn_layer_workspace(csr, dims[l], dims[l + 1]) for l in range(L))
     ws = torch.empty(ws_layer, dtype=torch.uint8, device=dev)
     dense_ws = max(G.gnn_dense_workspace(n, dims[l], dims[l + 1]) for l in range(L))
     wsd = torch.empty(dense_ws, dtype=torch.uint8, device=dev)
@@ -230,7 +249,7 @@ def run_gpu(args, rank, world, local_rank):
     slot_cut = (bnd.slot_rowptr[1:] - bnd.slot_rowptr[:-1]).cpu().numpy()
     slot_bits = bnd.slot_bits.cpu().numpy()
 
-    kinds = ["quant", "spmm_fwd", "gemm_fwd", "mask_dM_dW", "spmm_bwd"]
+    kinds = ["quant", "spmm_fwd", "gemm_fwd", "mask_dM_dW", "spmm_bwd", "tf_fwd", "tf_bwd"]
     ev = {}
 
     def rec(key):
@@ -244,10 +263,27 @@ def run_gpu(args, rank, world, local_rank):
         if ld[l] not in dM_by_ld:
             dM_by_ld[ld[l]] = torch.empty((n, ld[l]), device=dev)
 
+    def tf_fwd(l, Hs):
+        F, Fo = dims[l], dims[l + 1]
+        G.gnn_layer_fwd_tf(csr, bnd, Hs[l], F, W[l], Fo, l < L - 1, 2 * l, packed, meta, Mb[l], Y[l],
+                           Hs[l + 1], slot_off=offs[Fo], ws=ws)
+
+    def tf_bwd(l, Hs, dHs):
+        F, Fo = dims[l], dims[l + 1]
+        G.gnn_layer_bwd_tf(csr, bnd, dHs[l + 1], Hs[l + 1], l < L - 1, Mb[l], W[l], F, Fo, 2 * l + 1,
+                           packed, meta, dW[l], dHs[l] if l > 0 else None, slot_off=offs[Fo], ws=ws)
+
     def run_step(timed):
         for l in range(L):
             F, Fo = dims[l], dims[l + 1]
-            so = offs[F]
+            so = offs[mwid[l]]
+            if tf[l]:
+                if timed:
+                    rec(("tf_fwd", l, 0))
+                tf_fwd(l, H)
+                if timed:
+                    rec(("tf_fwd", l, 1))
+                continue
             if timed:
                 rec(("quant", l, 0))
             G.gnn_quant_pack(H[l], F, bnd.slot_node, S, bnd.slot_bits, so, 2 * l, packed, meta)
@@ -261,8 +297,15 @@ def run_gpu(args, rank, world, local_rank):
                 rec(("gemm_fwd", l, 1))
         for l in reversed(range(L)):
             F, Fo = dims[l], dims[l + 1]
-            so = offs[F]
+            so = offs[mwid[l]]
             dMl = dM_by_ld.get(ld[l])
+            if tf[l]:
+                if timed:
+                    rec(("tf_bwd", l, 0))
+                tf_bwd(l, H, dH)
+                if timed:
+                    rec(("tf_bwd", l, 1))
+                continue
             if timed:
                 rec(("mask_dM_dW", l, 0))
             G.gnn_dense_bwd(Mb[l], n, F, W[l], Fo, dH[l + 1], H[l + 1], l < L - 1,
@@ -313,7 +356,8 @@ def run_gpu(args, rank, world, local_rank):
         if which != 1:
             continue
         start_key = {"quant": ("quant", l, 0), "spmm_fwd": ("quant", l, 1), "gemm_fwd": ("spmm_fwd", l, 1),
-                     "mask_dM_dW": ("mask_dM_dW", l, 0), "spmm_bwd": ("mask_dM_dW", l, 1)}[kind]
+                     "mask_dM_dW": ("mask_dM_dW", l, 0), "spmm_bwd": ("mask_dM_dW", l, 1),
+                     "tf_fwd": ("tf_fwd", l, 0), "tf_bwd": ("tf_bwd", l, 0)}[kind]
         starts = ev[start_key]
         tot = sum(a.elapsed_time(b) for a, b in zip(starts, lst)) / args.steps
         per[kind] += tot
@@ -326,8 +370,18 @@ def run_gpu(args, rank, world, local_rank):
     spmm_fwd_bytes_l = {}
     for l in range(L):
         F, Fo = dims[l], dims[l + 1]
-        kb = kernel_bytes(n, nnz, nc, S, F, slot_bits, slot_cut, 2 * ldb[l])
         gb = gemm_bytes(n, F, Fo)
+        if tf[l]:
+            # cast, transform, messages and aggregation at F_out (fp32 out);
+            # backward: mask, aggregation at F_out, dense backward
+            kb = kernel_bytes(n, nnz, nc, S, Fo, slot_bits, slot_cut, 4 * Fo)
+            byt["tf_fwd"] += 6 * n * F + gb["fwd"] + kb["quant"] + kb["fwd"]
+            byt["tf_bwd"] += (12 * n * Fo if l < L - 1 else 0) + kb["bwd"] + gb["mask"] + gb["dW"] + \
+                (gb["dM"] if l > 0 else 0)
+            flops["spmm"] += 4.0 * nnz * Fo
+            flops["gemm"] += 2.0 * n * F * Fo * (3 if l > 0 else 2)
+            continue
+        kb = kernel_bytes(n, nnz, nc, S, F, slot_bits, slot_cut, 2 * ldb[l])
         byt["quant"] += kb["quant"]
         byt["spmm_fwd"] += kb["fwd"]
         spmm_fwd_bytes_l[l] = kb["fwd"]
@@ -347,7 +401,7 @@ def run_gpu(args, rank, world, local_rank):
     # model as the synchronous step; per layer and direction two message
     # buffers alternate between steps.
     asy = None
-    if args.async_steps > 0:
+    if args.async_steps > 0 and not any(tf):
         aux = torch.cuda.Stream(dev)
 
         def msgbufs(F):
@@ -428,11 +482,17 @@ def run_gpu(args, rank, world, local_rank):
             Hs = [H0d] + H[1:]
             for l in range(L):
                 F, Fo = dims[l], dims[l + 1]
+                if tf[l]:
+                    tf_fwd(l, Hs)
+                    continue
                 G.gnn_layer_fwd(csr, bnd, Hs[l], F, W[l], Fo, l < L - 1, 2 * l, packed, meta, Mb[l],
                                 Hs[l + 1], slot_off=offs[F], ws=ws)
             dHs = dH[:L] + [dHLd]
             for l in reversed(range(L)):
                 F, Fo = dims[l], dims[l + 1]
+                if tf[l]:
+                    tf_bwd(l, Hs, dHs)
+                    continue
                 G.gnn_layer_bwd(csr, bnd, dHs[l + 1], Hs[l + 1], l < L - 1, Mb[l], W[l], F, Fo,
                                 2 * l + 1, packed, meta, dW[l], dHs[l] if l > 0 else None,
                                 slot_off=offs[F], ws=ws)
@@ -463,8 +523,8 @@ def run_gpu(args, rank, world, local_rank):
 
     return dict(ms=ms, per=per, per_layer=per_layer, byt=byt, flops=flops, total_bytes=total_bytes,
                 launches=launches, clocks=clk.summary(), e2e=e2e, asy=asy, S=S, nnz=nnz, nnz_cut=nc, n=n,
-                Q=int(offs[F0][-1].item()), spmm_fwd_bytes_l=spmm_fwd_bytes_l, n_long=csr.n_long,
-                n_pieces=csr.n_pieces, dims=dims, P=P)
+                Q=int(offs[mwid[0]][-1].item()), spmm_fwd_bytes_l=spmm_fwd_bytes_l, n_long=csr.n_long,
+                n_pieces=csr.n_pieces, dims=dims, P=P, tf=tf)
 
 
 # --------------------------------------------------------------- oracle (CPU) arm
@@ -526,6 +586,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="yelp", choices=sorted(WORKLOAD_TEXT))
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
+    ap.add_argument("--order", default="af", choices=["af", "tf", "auto"],
+                    help="aggregate first (the message is H), transform first where F_out < F_in "
+                         "(the message is H W), or per layer where it gathers fewer bytes")
     ap.add_argument("--aggregator", default="gcn", choices=["gcn", "mean"],
                     help="GCN weights 1/sqrt(d_v d_u) or GraphSAGE mean weights 1/d_v")
     ap.add_argument("--split-len", type=int, default=128)
@@ -551,7 +614,7 @@ def main():
             torch.cuda.set_device(local_rank)
 
     config = {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload,
-              "aggregator": args.aggregator,
+              "aggregator": args.aggregator, "order": args.order,
               "base_bits": args.base_bits or None,
               "timing": "inputs larger than L2 (no flush); CUDA events on the launching stream",
               "parallelism": f"replicas x{world}"}
@@ -592,12 +655,14 @@ def main():
 
     spmm_ms = per["spmm_fwd"] + per["spmm_bwd"]
     gemm_ms = per["gemm_fwd"] + per["mask_dM_dW"]
-    # dominant kernel: the forward aggregation of the first layer
-    L0 = 0
-    t_dom = r["per_layer"].get("spmm_fwd_l1")
-    dom_bytes = r["spmm_fwd_bytes_l"][L0]
+    # dominant kernel: the forward aggregation of the first aggregate-first layer
+    L0 = next((l for l, t in enumerate(r["tf"]) if not t), None)
+    t_dom = r["per_layer"].get(f"spmm_fwd_l{L0 + 1}") if L0 is not None else None
+    dom_bytes = r["spmm_fwd_bytes_l"].get(L0) if L0 is not None else None
     achieved = dom_bytes / (t_dom * 1e-3) / 1e9 if t_dom else None
-    traffic = committed_traffic() if args.workload == "yelp" else None
+    default_path = (args.workload == "yelp" and args.order == "af" and args.aggregator == "gcn"
+                    and not args.base_bits)
+    traffic = committed_traffic() if default_path else None
     line = {
         "metric": METRIC, "value": gbs, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -609,13 +674,14 @@ def main():
             "quant_pack_GBs": rate("quant"),
             "spmm_GFLOPs": r["flops"]["spmm"] / (spmm_ms * 1e-3) / 1e9 if spmm_ms else None,
             "gemm_TFLOPs": r["flops"]["gemm"] / (gemm_ms * 1e-3) / 1e12 if gemm_ms else None,
-            "ms": per, "ms_per_layer": r["per_layer"],
+            "ms": per, "ms_per_layer": r["per_layer"], "transform_first_layers": r["tf"],
             "hbm_frac": {k: (rate(k) / hbm if rate(k) else None) for k in ["spmm_fwd", "spmm_bwd", "quant"]},
         },
         "graph": {"n": r["n"], "nnz": r["nnz"], "nnz_cut": r["nnz_cut"], "slots": r["S"],
                   "packed_bytes_layer1": r["Q"], "long_rows": r["n_long"], "pieces": r["n_pieces"],
                   "dims": r["dims"], "P": r["P"]},
-        "roofline": {"kernel": "gnn_spmm_fwd, layer 1 (aggregation with in-gather dequantisation)",
+        "roofline": {"kernel": f"gnn_spmm_fwd, layer {(L0 or 0) + 1} (aggregation with in-gather "
+                               "dequantisation)",
                      "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": (achieved / hbm) if achieved else None, "traffic": traffic,
                      "peak_source": peak_src},
