@@ -383,9 +383,11 @@ __global__ void __launch_bounds__(256) spmm_fixup_kernel(
 // then thread t adds chunk t of those rows in entry order.  The remaining
 // blocks give every ordinary slot a group of G lanes that loads U entries
 // ahead of their adds.  Both keep each element's additions in entry order,
-// so the result is the same as one sequential loop.
+// so the result is the same as one sequential loop.  Rows of up to three
+// chunks per lane keep 64 registers (four blocks per SM: the loads of a slot
+// are few and short, so more slots in flight pay more than deeper unrolling).
 template <int G, int CPL, int U>
-__global__ void __launch_bounds__(256) halo_quant_pack_kernel(
+__global__ void __launch_bounds__(256, (G == 32 && CPL <= 3) ? 4 : 1) halo_quant_pack_kernel(
     int64_t S, const int64_t* __restrict__ srp, const int32_t* __restrict__ scol,
     const float* __restrict__ sval, const float* __restrict__ Gm, int64_t ldg, int F,
     const uint8_t* __restrict__ slot_bits, const int64_t* __restrict__ slot_off, uint32_t seed,
@@ -607,8 +609,8 @@ gnn_status launch_halo_quant_pack(const gnn_boundary& b, const float* Gm, int64_
   else {
     switch ((slots + 31) / 32) {
       case 1: GNN_HALO(32, 1, 4); break;
-      case 2: GNN_HALO(32, 2, 4); break;
-      case 3: GNN_HALO(32, 3, 2); break;
+      case 2: GNN_HALO(32, 2, 2); break;
+      case 3: GNN_HALO(32, 3, 1); break;
       case 4: GNN_HALO(32, 4, 2); break;
       case 5: GNN_HALO(32, 5, 2); break;
       case 6: GNN_HALO(32, 6, 2); break;
