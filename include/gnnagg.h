@@ -440,6 +440,58 @@ gnn_status gnn_layer_bwd_tf(const gnn_csr* csr, const gnn_boundary* bnd, const f
                             float* dW, float* dH_in, int64_t ldh, void* ws, size_t ws_bytes,
                             gnn_stream_t stream);
 
+/* Attention aggregator (SYLVIE guide section 2: GAT weights the aggregation
+ * by attention coefficients alpha_vu; section 12: one head).  Reading: the
+ * single-head graph attention layer on the transformed rows,
+ *   Y = bf16(H) W,  s_l = Y a_l,  s_r = Y a_r,
+ *   e_vu = LeakyReLU(s_l[v] + s_r[u]) (slope 0.2) over u in N(v) + {v},
+ *   alpha_v. = softmax(e_v.) (fp32, expf),  H' = act(sum_u alpha_vu Y_u),
+ * where a remote source is seen through its dequantised message Y~_u (its
+ * score a_r . Y~_u is formed by the receiver).  The pattern must be
+ * symmetrised.
+ *
+ * gnn_gat_index: position maps for the backward: tpos [nnz] (entry order of
+ * the aggregation: col_remap with a boundary, col without) gives, for a local
+ * entry of row u reading v, the position of v's entry reading u (-1 for a
+ * remote entry); spos [nnz_cut] gives, for each slot-CSR entry (s, v), the
+ * position of v's entry reading slot s.  Computed once per graph.
+ *
+ * gnn_gat_layer_fwd: Hb = bf16(H_in), Y (fp32, ldy >= round_up(F_out, 4)),
+ * the messages of Y's boundary rows (offsets for F_out, key s, `seed`), the
+ * attention alpha [nnz] (entry order as above) and H_out = act(A_alpha Y).
+ *
+ * gnn_gat_layer_bwd: dZ = dH_out * 1[H_out > 0] (relu); per entry
+ * dalpha = dZ_v . x_u (x the row the forward aggregated: Y_u or the
+ * dequantised message of packed_fwd/meta_fwd), g = alpha (dalpha -
+ * sum alpha dalpha) LeakyReLU'(e) (written to g_out [nnz] when given).  The
+ * backward message of slot s is the fixed-order halo partial
+ * sum_v alpha_vs dZ_v (start +0, v ascending, products and sums in fp32)
+ * followed by fl(P + fl(r_s a_r)), r_s = sum_v g_vs in entry order, then
+ * quantised with key s and `seed` into packed_ws/meta_ws.  dY = the local
+ * transposed aggregation + the owned messages + ds_r a_r + ds_l a_l;
+ * da_l = sum_v ds_l[v] Y_v, da_r = sum_u ds_r[u] Y_u + sum_s r_s Y~_s;
+ * dW = Hb^T bf16(dY) and, unless dH_in is NULL, dH_in = bf16(dY) W^T.
+ * Workspace from gnn_gat_workspace (same for both directions). */
+gnn_status gnn_gat_index(const gnn_csr* csr, const gnn_boundary* bnd, int64_t* tpos,
+                         int64_t* spos, gnn_stream_t stream);
+gnn_status gnn_gat_workspace(const gnn_csr* csr, const gnn_boundary* bnd, int32_t F_in,
+                             int32_t F_out, size_t* ws_bytes);
+gnn_status gnn_gat_layer_fwd(const gnn_csr* csr, const gnn_boundary* bnd, const float* H_in,
+                             int64_t ldh, int32_t F_in, const uint16_t* W, int32_t F_out,
+                             const float* a_l, const float* a_r, int32_t relu, uint32_t seed,
+                             uint8_t* packed, float* meta, uint16_t* Hb, int64_t ldhb, float* Y,
+                             int64_t ldy, float* alpha, float* H_out, int64_t ldo, void* ws,
+                             size_t ws_bytes, gnn_stream_t stream);
+gnn_status gnn_gat_layer_bwd(const gnn_csr* csr, const gnn_boundary* bnd, const int64_t* tpos,
+                             const int64_t* spos, const float* dH_out, int64_t ldg,
+                             const float* H_out, int64_t ldo, int32_t relu, const uint16_t* Hb,
+                             int64_t ldhb, const float* Y, int64_t ldy, const float* alpha,
+                             const uint8_t* packed_fwd, const float* meta_fwd, const uint16_t* W,
+                             const float* a_l, const float* a_r, int32_t F_in, int32_t F_out,
+                             uint32_t seed, uint8_t* packed_ws, float* meta_ws, float* dW,
+                             float* da_l, float* da_r, float* dH_in, int64_t ldh, float* g_out,
+                             void* ws, size_t ws_bytes, gnn_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Epoch control (SYLVIE guide, sections 8 and 11).  Host code.              */
 /* ------------------------------------------------------------------------ */

@@ -25,6 +25,7 @@ __all__ = [
     "gnn_halo_quant_pack", "gnn_spmm_bwd_local", "gnn_layer_fwd_async", "gnn_layer_bwd_async",
     "LdrState", "gnn_ldr_init", "gnn_ldr_update", "gnn_quant_divide",
     "gnn_layer_tf_workspace", "gnn_layer_fwd_tf", "gnn_layer_bwd_tf",
+    "gnn_gat_index", "gnn_gat_workspace", "gnn_gat_layer_fwd", "gnn_gat_layer_bwd",
 ]
 
 
@@ -495,6 +496,63 @@ def gnn_layer_bwd_tf(csr: Csr, bnd: Optional[Boundary], dH_out, H_out, relu: boo
          int(relu), _ptr(Hb), Hb.stride(0), _ptr(W), F_in, F_out, seed & 0xFFFFFFFF,
          _ptr(packed_ws), _ptr(meta_ws), _ptr(dW), _ptr(dH_in),
          dH_in.stride(0) if dH_in is not None else 0, _ptr(ws), ws.numel(), _stream(stream))
+
+
+# ---------------------------------------------------------------- attention aggregator
+def gnn_gat_index(csr: Csr, bnd: Optional[Boundary], stream=None):
+    """Position maps (tpos [nnz], spos [nnz_cut] or None) for the backward."""
+    torch = _torch()
+    dev = csr.rowptr.device
+    tpos = torch.empty(max(csr.nnz, 1), dtype=torch.int64, device=dev)
+    spos = torch.empty(max(bnd.nnz_cut, 1), dtype=torch.int64, device=dev) if bnd is not None else None
+    c = csr.c()
+    cb = bnd.c() if bnd is not None else None
+    call("gnn_gat_index", ctypes.byref(c), ctypes.byref(cb) if cb is not None else None, _ptr(tpos),
+         _ptr(spos), _stream(stream))
+    return tpos, spos
+
+
+def gnn_gat_workspace(csr: Csr, bnd: Optional[Boundary], F_in: int, F_out: int) -> int:
+    nb = ctypes.c_size_t()
+    c = csr.c()
+    cb = bnd.c() if bnd is not None else None
+    call("gnn_gat_workspace", ctypes.byref(c), ctypes.byref(cb) if cb is not None else None, F_in,
+         F_out, ctypes.byref(nb))
+    return nb.value
+
+
+def _gat_bnd(bnd, slot_off, F_out):
+    return bnd.c(slot_off, F_out if slot_off is not None else None) if bnd is not None else None
+
+
+def gnn_gat_layer_fwd(csr: Csr, bnd: Optional[Boundary], H_in, F_in: int, W, F_out: int, a_l, a_r,
+                      relu: bool, seed: int, packed, meta, Hb, Y, alpha, H_out, slot_off=None,
+                      ws=None, stream=None) -> None:
+    c = csr.c()
+    cb = _gat_bnd(bnd, slot_off, F_out)
+    if ws is None:
+        ws = _workspace(gnn_gat_workspace(csr, bnd, F_in, F_out), H_in.device)
+    call("gnn_gat_layer_fwd", ctypes.byref(c), ctypes.byref(cb) if cb is not None else None,
+         _ptr(H_in), H_in.stride(0), F_in, _ptr(W), F_out, _ptr(a_l), _ptr(a_r), int(relu),
+         seed & 0xFFFFFFFF, _ptr(packed), _ptr(meta), _ptr(Hb), Hb.stride(0), _ptr(Y), Y.stride(0),
+         _ptr(alpha), _ptr(H_out), H_out.stride(0), _ptr(ws), ws.numel(), _stream(stream))
+
+
+def gnn_gat_layer_bwd(csr: Csr, bnd: Optional[Boundary], tpos, spos, dH_out, H_out, relu: bool, Hb,
+                      Y, alpha, packed_fwd, meta_fwd, W, a_l, a_r, F_in: int, F_out: int, seed: int,
+                      packed_ws, meta_ws, dW, da_l, da_r, dH_in=None, g_out=None, slot_off=None,
+                      ws=None, stream=None) -> None:
+    c = csr.c()
+    cb = _gat_bnd(bnd, slot_off, F_out)
+    if ws is None:
+        ws = _workspace(gnn_gat_workspace(csr, bnd, F_in, F_out), dH_out.device)
+    call("gnn_gat_layer_bwd", ctypes.byref(c), ctypes.byref(cb) if cb is not None else None,
+         _ptr(tpos), _ptr(spos), _ptr(dH_out), dH_out.stride(0), _ptr(H_out),
+         H_out.stride(0) if H_out is not None else 0, int(relu), _ptr(Hb), Hb.stride(0), _ptr(Y),
+         Y.stride(0), _ptr(alpha), _ptr(packed_fwd), _ptr(meta_fwd), _ptr(W), _ptr(a_l), _ptr(a_r),
+         F_in, F_out, seed & 0xFFFFFFFF, _ptr(packed_ws), _ptr(meta_ws), _ptr(dW), _ptr(da_l),
+         _ptr(da_r), _ptr(dH_in), dH_in.stride(0) if dH_in is not None else 0, _ptr(g_out),
+         _ptr(ws), ws.numel(), _stream(stream))
 
 
 # ---------------------------------------------------------------- epoch control (host only)

@@ -108,6 +108,15 @@ PROTOTYPES = {
     "gnn_layer_bwd_tf": (ctypes.c_int, [P_csr, P_bnd, c_vp, c_i64, c_vp, c_i64, c_i32, c_vp, c_i64,
                                         c_vp, c_i32, c_i32, c_u32, c_vp, c_vp, c_vp, c_vp, c_i64,
                                         c_vp, c_size, c_vp]),
+    "gnn_gat_index": (ctypes.c_int, [P_csr, P_bnd, c_vp, c_vp, c_vp]),
+    "gnn_gat_workspace": (ctypes.c_int, [P_csr, P_bnd, c_i32, c_i32, P_size]),
+    "gnn_gat_layer_fwd": (ctypes.c_int, [P_csr, P_bnd, c_vp, c_i64, c_i32, c_vp, c_i32, c_vp, c_vp, c_i32,
+                                         c_u32, c_vp, c_vp, c_vp, c_i64, c_vp, c_i64, c_vp, c_vp, c_i64,
+                                         c_vp, c_size, c_vp]),
+    "gnn_gat_layer_bwd": (ctypes.c_int, [P_csr, P_bnd, c_vp, c_vp, c_vp, c_i64, c_vp, c_i64, c_i32, c_vp,
+                                         c_i64, c_vp, c_i64, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32,
+                                         c_i32, c_u32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_vp,
+                                         c_vp, c_size, c_vp]),
     "gnn_ldr_init": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_double, c_i32, c_i32, c_i32]),
     "gnn_ldr_update": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_double), c_i32,
                                       ctypes.c_double]),

@@ -39,6 +39,26 @@ gnn_status launch_halo_quant_pack(const gnn_boundary& b, const float* Gm, int64_
                                   uint32_t seed, uint8_t* packed_ws, float2* meta_ws,
                                   cudaStream_t st);
 
+// The halo quant-pack with other entry weights (sval, slot-CSR order) and,
+// when score_r is given, the score term fl(P + fl(score_r[s] * a_r[j])) added
+// to each slot's partial before it is quantised.
+gnn_status launch_halo_quant_pack_ex(const gnn_boundary& b, const float* Gm, int64_t ldg, int F,
+                                     uint32_t seed, uint8_t* packed_ws, float2* meta_ws,
+                                     const float* sval, const float* score_r, const float* a_r,
+                                     cudaStream_t st);
+
+// Aggregations with caller weights in place of the CSR's (CSR order without
+// a boundary, col_remap order with one): the forward (fp32 out, optional
+// ReLU) and the owner-side backward (local entries plus owned messages).
+gnn_status launch_spmm_fwd_w(const gnn_csr& csr, const gnn_boundary* bnd, const float* weights,
+                             const float* H, int64_t ldh, int F, const uint8_t* packed,
+                             const float2* meta, float* M, int64_t ldm, float* partial, int relu,
+                             cudaStream_t st);
+gnn_status launch_spmm_bwd_local_w(const gnn_csr& csr, const gnn_boundary* bnd,
+                                   const float* weights, const float* Gm, int64_t ldg, int F,
+                                   const uint8_t* packed, const float2* meta, float* dH,
+                                   int64_t ldh, float* partial, cudaStream_t st);
+
 size_t spmm_workspace_bytes(const gnn_csr& csr, int F);
 
 // gnn_spmm_fwd with its argument checks, the output ReLU'd when relu != 0.

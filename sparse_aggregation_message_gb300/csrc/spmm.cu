@@ -374,6 +374,17 @@ __global__ void __launch_bounds__(256) spmm_fixup_kernel(
   store_row<G, CPL>(row, acc, F, nch, nch_b, c0, c1, gl, M, ldm, Mb, ldmb, relu);
 }
 
+// P = fl(P + fl(r * a_r[j])) for the elements j of chunk c below F (the score
+// term of an attention layer's backward message).
+__device__ __forceinline__ void add_score_term(float4& p, float r, const float* __restrict__ a_r,
+                                               int c, int F) {
+  const int j = 4 * c;
+  if (j < F) p.x = __fadd_rn(p.x, __fmul_rn(r, __ldg(a_r + j)));
+  if (j + 1 < F) p.y = __fadd_rn(p.y, __fmul_rn(r, __ldg(a_r + j + 1)));
+  if (j + 2 < F) p.z = __fadd_rn(p.z, __fmul_rn(r, __ldg(a_r + j + 2)));
+  if (j + 3 < F) p.w = __fadd_rn(p.w, __fmul_rn(r, __ldg(a_r + j + 3)));
+}
+
 // Backward messages: halo partial of slot s over its entries in ascending v,
 // every product and sum rounded to fp32 (start +0), then quantised and packed
 // in registers with row key s.
@@ -392,7 +403,8 @@ __global__ void __launch_bounds__(256, (G == 32 && CPL <= 3) ? 4 : 1) halo_quant
     const float* __restrict__ sval, const float* __restrict__ Gm, int64_t ldg, int F,
     const uint8_t* __restrict__ slot_bits, const int64_t* __restrict__ slot_off, uint32_t seed,
     uint8_t* __restrict__ packed, float2* __restrict__ meta, int n_long,
-    const int32_t* __restrict__ long_slots, int long_len, int E) {
+    const int32_t* __restrict__ long_slots, int long_len, int E, const float* __restrict__ score_r,
+    const float* __restrict__ a_r) {
   constexpr int CPLQ = (G * CPL + 31) / 32;  // chunks per lane when one warp quantises
   extern __shared__ float4 tile[];
   const int lane = threadIdx.x & 31;
@@ -431,7 +443,10 @@ __global__ void __launch_bounds__(256, (G == 32 && CPL <= 3) ? 4 : 1) halo_quant
       }
       __syncthreads();
     }
-    if (t < nch) tile[t] = acc;
+    if (t < nch) {
+      if (score_r) add_score_term(acc, __ldg(score_r + s), a_r, t, F);
+      tile[t] = acc;
+    }
     __syncthreads();
     if (t < 32) {
       float4 v[CPLQ];
@@ -493,6 +508,12 @@ __global__ void __launch_bounds__(256, (G == 32 && CPL <= 3) ? 4 : 1) halo_quant
         }
       }
     }
+  }
+  if (score_r) {
+    const float r = __ldg(score_r + s);
+#pragma unroll
+    for (int i = 0; i < CPL; ++i)
+      if (gl + i * G < nch) add_score_term(acc[i], r, a_r, gl + i * G, F);
   }
   quantize_pack_row<G, CPL>(acc, F, __ldg(slot_bits + s), row_key(seed, (uint32_t)s),
                             packed + __ldg(slot_off + s), meta + s, gl, gmask);
@@ -575,6 +596,32 @@ gnn_status launch_spmm_fwd(const gnn_csr& csr, const gnn_boundary* bnd, const fl
                                    msg, nullptr, nullptr, partial, M, ldm, mb, ldmb, st, relu);
 }
 
+gnn_status launch_spmm_fwd_w(const gnn_csr& csr, const gnn_boundary* bnd, const float* weights,
+                             const float* H, int64_t ldh, int F, const uint8_t* packed,
+                             const float2* meta, float* M, int64_t ldm, float* partial, int relu,
+                             cudaStream_t st) {
+  if (csr.n == 0) return GNN_OK;
+  if (!bnd)
+    return dispatch_rows<kPlain>(csr, csr.col, weights, nullptr, H, ldh, F, SlotMsgs{}, nullptr,
+                                 nullptr, partial, M, ldm, nullptr, 0, st, relu);
+  SlotMsgs msg{packed, meta, bnd->slot_off, bnd->slot_bits};
+  return dispatch_rows<kFwdRemote>(csr, bnd->col_remap, weights, bnd->local_cnt, H, ldh, F, msg,
+                                   nullptr, nullptr, partial, M, ldm, nullptr, 0, st, relu);
+}
+
+gnn_status launch_spmm_bwd_local_w(const gnn_csr& csr, const gnn_boundary* bnd,
+                                   const float* weights, const float* Gm, int64_t ldg, int F,
+                                   const uint8_t* packed, const float2* meta, float* dH,
+                                   int64_t ldh, float* partial, cudaStream_t st) {
+  if (csr.n == 0) return GNN_OK;
+  if (!bnd)
+    return dispatch_rows<kPlain>(csr, csr.col, weights, nullptr, Gm, ldg, F, SlotMsgs{}, nullptr,
+                                 nullptr, partial, dH, ldh, nullptr, 0, st);
+  SlotMsgs msg{packed, meta, bnd->slot_off, bnd->slot_bits};
+  return dispatch_rows<kBwdOwned>(csr, bnd->col_remap, weights, bnd->local_cnt, Gm, ldg, F, msg,
+                                  bnd->own_ptr, bnd->own_slot, partial, dH, ldh, nullptr, 0, st);
+}
+
 static int quant_chunk_slots(int F) {
   const int a = 32 * ((F + 127) / 128), b = (F + 3) / 4;
   return a > b ? a : b;
@@ -583,6 +630,14 @@ static int quant_chunk_slots(int F) {
 gnn_status launch_halo_quant_pack(const gnn_boundary& b, const float* Gm, int64_t ldg, int F,
                                   uint32_t seed, uint8_t* packed_ws, float2* meta_ws,
                                   cudaStream_t st) {
+  return launch_halo_quant_pack_ex(b, Gm, ldg, F, seed, packed_ws, meta_ws, b.slot_val, nullptr,
+                                   nullptr, st);
+}
+
+gnn_status launch_halo_quant_pack_ex(const gnn_boundary& b, const float* Gm, int64_t ldg, int F,
+                                     uint32_t seed, uint8_t* packed_ws, float2* meta_ws,
+                                     const float* sval, const float* score_r, const float* a_r,
+                                     cudaStream_t st) {
   const int64_t S = b.n_slots;
   if (S == 0) return GNN_OK;
   const int slots = quant_chunk_slots(F);
@@ -602,8 +657,8 @@ gnn_status launch_halo_quant_pack(const gnn_boundary& b, const float* Gm, int64_
   do {                                                                                           \
     const int64_t grid = n_long + (S * G_ + block - 1) / block;                                  \
     halo_quant_pack_kernel<G_, CPL_, U_><<<(unsigned)grid, block, dyn, st>>>(                    \
-        S, b.slot_rowptr, b.slot_col, b.slot_val, Gm, ldg, F, b.slot_bits, b.slot_off, seed,     \
-        packed_ws, meta_ws, n_long, b.long_slots, long_len, E);                                  \
+        S, b.slot_rowptr, b.slot_col, sval, Gm, ldg, F, b.slot_bits, b.slot_off, seed,           \
+        packed_ws, meta_ws, n_long, b.long_slots, long_len, E, score_r, a_r);                    \
   } while (0)
   if (slots <= 32) GNN_HALO(8, 4, 2);
   else {
