@@ -201,7 +201,7 @@ def run_gpu(args, rank, world, local_rank):
     wl = make_workload(args.workload)
     n, P, dims, L = wl.n, wl.P, wl.dims, wl.layers
     base = args.base_bits if args.base_bits else wl.base_bits[0]
-    flags = G.CSR_GCN | (G.CSR_MEAN if args.aggregator == "mean" else 0)
+    flags = G.CSR_GCN | (G.CSR_MEAN if args.aggregator == "mean" else 0)  # gat: GCN pattern
     csr = G.gnn_csr_build(n, torch.from_numpy(wl.src).to(dev), torch.from_numpy(wl.dst).to(dev),
                           flags)
     csr = G.gnn_csr_split(csr, args.split_len)
@@ -210,7 +210,9 @@ def run_gpu(args, rank, world, local_rank):
     bnd = G.gnn_boundary_index(csr, P, rule, base, F0)
     G.gnn_boundary_long_slots(csr, bnd, args.long_slot_len)
     S = bnd.n_slots
-    tf = layer_orders(args.order, dims)
+    gat = args.aggregator == "gat"
+    # attention layers aggregate the transformed rows
+    tf = [True] * L if gat else layer_orders(args.order, dims)
     # message (and aggregation) width of each layer
     mwid = [dims[l + 1] if tf[l] else dims[l] for l in range(L)]
     widths = sorted(set(mwid))
@@ -263,13 +265,40 @@ def run_gpu(args, rank, world, local_rank):
         if ld[l] not in dM_by_ld:
             dM_by_ld[ld[l]] = torch.empty((n, ld[l]), device=dev)
 
+    if gat:
+        tpos, spos = G.gnn_gat_index(csr, bnd)
+        ga = torch.Generator(device=dev)
+        ga.manual_seed(wl.seed + 7)
+        a_l = [0.1 * torch.randn(dims[l + 1], generator=ga, device=dev) for l in range(L)]
+        a_r = [0.1 * torch.randn(dims[l + 1], generator=ga, device=dev) for l in range(L)]
+        alpha = [torch.empty(max(csr.nnz, 1), device=dev) for _ in range(L)]
+        da_l = [torch.empty(dims[l + 1], device=dev) for l in range(L)]
+        da_r = [torch.empty(dims[l + 1], device=dev) for l in range(L)]
+        # each layer's forward messages stay for its backward
+        fmsg = [(torch.zeros(max(int(offs[dims[l + 1]][-1].item()), 16), dtype=torch.uint8, device=dev),
+                 torch.zeros((max(S, 1), 2), device=dev)) for l in range(L)]
+        ws_gat = max(G.gnn_gat_workspace(csr, bnd, dims[l], dims[l + 1]) for l in range(L))
+        if ws_gat > ws.numel():
+            ws = torch.empty(ws_gat, dtype=torch.uint8, device=dev)
+
     def tf_fwd(l, Hs):
         F, Fo = dims[l], dims[l + 1]
+        if gat:
+            G.gnn_gat_layer_fwd(csr, bnd, Hs[l], F, W[l], Fo, a_l[l], a_r[l], l < L - 1, 2 * l,
+                                fmsg[l][0], fmsg[l][1], Mb[l], Y[l], alpha[l], Hs[l + 1],
+                                slot_off=offs[Fo], ws=ws)
+            return
         G.gnn_layer_fwd_tf(csr, bnd, Hs[l], F, W[l], Fo, l < L - 1, 2 * l, packed, meta, Mb[l], Y[l],
                            Hs[l + 1], slot_off=offs[Fo], ws=ws)
 
     def tf_bwd(l, Hs, dHs):
         F, Fo = dims[l], dims[l + 1]
+        if gat:
+            G.gnn_gat_layer_bwd(csr, bnd, tpos, spos, dHs[l + 1], Hs[l + 1], l < L - 1, Mb[l], Y[l],
+                                alpha[l], fmsg[l][0], fmsg[l][1], W[l], a_l[l], a_r[l], F, Fo,
+                                2 * l + 1, packed, meta, dW[l], da_l[l], da_r[l],
+                                dHs[l] if l > 0 else None, slot_off=offs[Fo], ws=ws)
+            return
         G.gnn_layer_bwd_tf(csr, bnd, dHs[l + 1], Hs[l + 1], l < L - 1, Mb[l], W[l], F, Fo, 2 * l + 1,
                            packed, meta, dW[l], dHs[l] if l > 0 else None, slot_off=offs[Fo], ws=ws)
 
@@ -378,6 +407,12 @@ def run_gpu(args, rank, world, local_rank):
             byt["tf_fwd"] += 6 * n * F + gb["fwd"] + kb["quant"] + kb["fwd"]
             byt["tf_bwd"] += (12 * n * Fo if l < L - 1 else 0) + kb["bwd"] + gb["mask"] + gb["dW"] + \
                 (gb["dM"] if l > 0 else 0)
+            if gat:
+                # scores (read Y), softmax (entry ids, source scores, attention),
+                # and in the backward the SDDMM's second gather of the rows plus
+                # the per-entry gradients, transposes and score sums
+                byt["tf_fwd"] += 4 * n * Fo + 12 * nnz
+                byt["tf_bwd"] += 4 * n * Fo + kb["fwd"] + 40 * nnz
             flops["spmm"] += 4.0 * nnz * Fo
             flops["gemm"] += 2.0 * n * F * Fo * (3 if l > 0 else 2)
             continue
@@ -540,6 +575,7 @@ class OracleBaseline:
         from synth import make_workload
 
         self.O = O
+        self.aggregator = aggregator
         wl = make_workload(workload)
         self.n = n = wl.n
         flags = O.FLAGS_GCN | (O.FLAG_MEAN if aggregator == "mean" else 0)
@@ -573,9 +609,11 @@ class OracleBaseline:
             t_used = time.perf_counter() - t0
             chunk = min(chunk * 2, 1 << 14)
         gbs = self.per_row_bytes * rows_done / t_used / 1e9
+        what = ("GCN-weighted aggregation; the attention oracle is not sampled"
+                if self.aggregator == "gat" else "forward + backward aggregation with quantised "
+                                                 "boundary rows")
         return dict(value=gbs, unit=UNIT, cores=1, kind="oracle",  # numpy/scipy run on one thread here
-                    sample=f"{rows_done} of {n} rows (forward + backward aggregation with quantised "
-                           f"boundary rows, F={self.F}), {t_used:.1f} s",
+                    sample=f"{rows_done} of {n} rows ({what}, F={self.F}), {t_used:.1f} s",
                     seconds=t_used, rows=rows_done)
 
 
@@ -589,8 +627,9 @@ def main():
     ap.add_argument("--order", default="af", choices=["af", "tf", "auto"],
                     help="aggregate first (the message is H), transform first where F_out < F_in "
                          "(the message is H W), or per layer where it gathers fewer bytes")
-    ap.add_argument("--aggregator", default="gcn", choices=["gcn", "mean"],
-                    help="GCN weights 1/sqrt(d_v d_u) or GraphSAGE mean weights 1/d_v")
+    ap.add_argument("--aggregator", default="gcn", choices=["gcn", "mean", "gat"],
+                    help="GCN weights 1/sqrt(d_v d_u), GraphSAGE mean weights 1/d_v, or one-head "
+                         "graph attention on the transformed rows")
     ap.add_argument("--split-len", type=int, default=128)
     ap.add_argument("--base-bits", type=int, default=0,
                     help="epoch base width (1, 2, 4, 8); default: the workload's first")

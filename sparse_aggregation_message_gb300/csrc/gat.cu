@@ -27,6 +27,18 @@ namespace {
 constexpr float kSlope = 0.2f;
 constexpr int kBlock = 256;
 
+// SDDMM launch shape: threads per block, resident blocks asked of the
+// register allocator, and entries gathered per round by 2-chunk lanes.
+#ifndef GNN_GAT_SD_BLOCK
+#define GNN_GAT_SD_BLOCK 64
+#endif
+#ifndef GNN_GAT_SD_MINB
+#define GNN_GAT_SD_MINB 16
+#endif
+#ifndef GNN_GAT_SD_U2
+#define GNN_GAT_SD_U2 4
+#endif
+
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
@@ -148,28 +160,117 @@ __device__ __forceinline__ float pre_score(float sl, int32_t c, const float* __r
 
 __device__ __forceinline__ float lrelu(float x) { return x > 0.f ? x : kSlope * x; }
 
-// alpha[k] = exp(e_k - max) / sum over the row, one warp per row.
+// alpha[k] = exp(e_k - max) / sum over the row, a group of G lanes per row:
+// e is formed once (kept in alpha), then exponentiated and summed, then
+// divided.  Each lane touches only its own entries.  Rows longer than
+// long_len are left to gat_softmax_long_kernel.
+template <int G>
 __global__ void gat_softmax_kernel(int n, const int64_t* __restrict__ rowptr,
                                    const int32_t* __restrict__ cr, const float* __restrict__ s_l,
                                    const float* __restrict__ s_r, const float* __restrict__ s_slot,
-                                   float* __restrict__ alpha) {
-  const int64_t v = warp_id();
-  if (v >= n) return;
-  const int lane = threadIdx.x & 31;
+                                   float* __restrict__ alpha, int64_t long_len) {
+  const int64_t v = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / G;
+  if (v >= n) return;  // uniform across the group
+  const int gl = threadIdx.x & (G - 1);
+  const uint32_t gmask = group_mask(G, threadIdx.x & 31);
+  const int64_t beg = rowptr[v], end = rowptr[v + 1];
+  if (long_len > 0 && end - beg > long_len) return;
+  const float sl = s_l[v];
+  float m = -INFINITY;
+  for (int64_t k = beg + gl; k < end; k += G) {
+    const float e = lrelu(pre_score(sl, cr[k], s_r, s_slot));
+    alpha[k] = e;
+    m = fmaxf(m, e);
+  }
+#pragma unroll
+  for (int o = G / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(gmask, m, o));
+  float sum = 0.f;
+  for (int64_t k = beg + gl; k < end; k += G) {
+    const float w = expf(alpha[k] - m);
+    alpha[k] = w;
+    sum += w;
+  }
+#pragma unroll
+  for (int o = G / 2; o > 0; o >>= 1) sum += __shfl_xor_sync(gmask, sum, o);
+  for (int64_t k = beg + gl; k < end; k += G) alpha[k] = alpha[k] / sum;
+}
+
+// The same for the long rows (the split plan's list), one block per row.
+__global__ void __launch_bounds__(kBlock) gat_softmax_long_kernel(
+    int n_long, const int32_t* __restrict__ long_rows, const int64_t* __restrict__ rowptr,
+    const int32_t* __restrict__ cr, const float* __restrict__ s_l, const float* __restrict__ s_r,
+    const float* __restrict__ s_slot, float* __restrict__ alpha) {
+  __shared__ float red[kBlock / 32];
+  __shared__ float bcast;
+  if ((int)blockIdx.x >= n_long) return;
+  const int v = long_rows[blockIdx.x];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int64_t beg = rowptr[v], end = rowptr[v + 1];
   const float sl = s_l[v];
   float m = -INFINITY;
-  for (int64_t k = beg + lane; k < end; k += 32) m = fmaxf(m, lrelu(pre_score(sl, cr[k], s_r, s_slot)));
+  for (int64_t k = beg + threadIdx.x; k < end; k += blockDim.x) {
+    const float e = lrelu(pre_score(sl, cr[k], s_r, s_slot));
+    alpha[k] = e;
+    m = fmaxf(m, e);
+  }
   m = warp_max(m);
+  if (lane == 0) red[wid] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = red[0];
+    for (int q = 1; q < kBlock / 32; ++q) t = fmaxf(t, red[q]);
+    bcast = t;
+  }
+  __syncthreads();
+  m = bcast;
   float sum = 0.f;
-  for (int64_t k = beg + lane; k < end; k += 32)
-    sum += expf(lrelu(pre_score(sl, cr[k], s_r, s_slot)) - m);
+  for (int64_t k = beg + threadIdx.x; k < end; k += blockDim.x) {
+    const float w = expf(alpha[k] - m);
+    alpha[k] = w;
+    sum += w;
+  }
   sum = warp_sum(sum);
-  for (int64_t k = beg + lane; k < end; k += 32)
-    alpha[k] = expf(lrelu(pre_score(sl, cr[k], s_r, s_slot)) - m) / sum;
+  __syncthreads();
+  if (lane == 0) red[wid] = sum;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int q = 0; q < kBlock / 32; ++q) t += red[q];
+    bcast = t;
+  }
+  __syncthreads();
+  sum = bcast;
+  for (int64_t k = beg + threadIdx.x; k < end; k += blockDim.x) alpha[k] = alpha[k] / sum;
 }
 
 // ---------------------------------------------------------------- backward
+// Sums of U values across the warp, one per group of 32/U lanes: d[i] of all
+// lanes is reduced, and lane L returns the sum for i = (L >> (5 - log2 U)) &
+// (U - 1).  A reduce-scatter: each halving step keeps half of the values and
+// adds the partner's other half (U - 1 shuffles in all), then the remaining
+// lanes of a group add up (5 - log2 U shuffles).
+template <int U>
+__device__ __forceinline__ float reduce_scatter(float (&d)[U], int lane) {
+  constexpr int P = U == 1 ? 0 : U == 2 ? 1 : U == 4 ? 2 : U == 8 ? 3 : U == 16 ? 4 : 5;
+  static_assert((1 << P) == U, "U must be a power of two up to 32");
+#pragma unroll
+  for (int st = 0; st < P; ++st) {
+    const int o = 16 >> st;
+    const int h = U >> (st + 1);
+    const bool hi = (lane >> (4 - st)) & 1;
+#pragma unroll
+    for (int i = 0; i < h; ++i) {
+      const float keep = hi ? d[i + h] : d[i];
+      const float send = hi ? d[i] : d[i + h];
+      d[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+  float v = d[0];
+#pragma unroll
+  for (int o = 16 >> P; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
 struct Units {  // rows, or pieces of the split plan first
   int n;
   int64_t n_pieces;
@@ -184,7 +285,7 @@ struct Units {  // rows, or pieces of the split plan first
 // and ds_l[v] = sum_k g_k.  Each group of 32 lanes holds dZ_v in registers and
 // gathers U entries' rows at a time.
 template <int CPL, int U>
-__global__ void __launch_bounds__(kBlock) gat_sddmm_kernel(
+__global__ void __launch_bounds__(GNN_GAT_SD_BLOCK, GNN_GAT_SD_MINB) gat_sddmm_kernel(
     Units un, const int64_t* __restrict__ rowptr, const int32_t* __restrict__ cr,
     const float* __restrict__ alpha, const float* __restrict__ Y, int64_t ldy, int F,
     const float* __restrict__ dZ, int64_t ldz, const uint8_t* __restrict__ packed,
@@ -236,17 +337,22 @@ __global__ void __launch_bounds__(kBlock) gat_sddmm_kernel(
       }
     }
     const int cnt = (int)min((int64_t)32, end - base);
-    float mine = 0.f;  // dalpha of this lane's entry
+    constexpr int GP = 32 / U;  // lanes that end up holding one entry's sum
     for (int k = 0; k < cnt; k += U) {
       float d[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int src = k + u < cnt ? k + u : k;
         const int32_t ck = __shfl_sync(0xffffffffu, cc, src);
-        const int bk = __shfl_sync(0xffffffffu, sb, src);
-        const uint32_t ok = __shfl_sync(0xffffffffu, so16, src);
-        const float mnk = __shfl_sync(0xffffffffu, sm.x, src);
-        const float sck = __shfl_sync(0xffffffffu, sm.y, src);
+        int bk = 0;
+        uint32_t ok = 0;
+        float mnk = 0.f, sck = 0.f;
+        if (ck < 0) {  // uniform across the warp
+          bk = __shfl_sync(0xffffffffu, sb, src);
+          ok = __shfl_sync(0xffffffffu, so16, src);
+          mnk = __shfl_sync(0xffffffffu, sm.x, src);
+          sck = __shfl_sync(0xffffffffu, sm.y, src);
+        }
         float acc = 0.f;
 #pragma unroll
         for (int i = 0; i < CPL; ++i) {
@@ -262,15 +368,13 @@ __global__ void __launch_bounds__(kBlock) gat_sddmm_kernel(
         }
         d[u] = acc;
       }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const float t = warp_sum(d[u]);
-        if (lane == k + u) mine = t;
+      const float t = reduce_scatter<U>(d, lane);
+      const int idx = lane / GP;
+      const float ae = __shfl_sync(0xffffffffu, a, k + idx);
+      if (lane % GP == 0 && k + idx < cnt) {
+        g[base + k + idx] = t;
+        c_acc = fmaf(ae, t, c_acc);
       }
-    }
-    if (e < end) {
-      g[e] = mine;
-      c_acc = fmaf(a, mine, c_acc);
     }
   }
   c_acc = warp_sum(c_acc);
@@ -291,8 +395,9 @@ __global__ void __launch_bounds__(kBlock) gat_sddmm_kernel(
   if (lane == 0) ds_l[row] = dsl;
 }
 
-// Long rows: c_v from their pieces (piece order), then g and ds_l as above.
-__global__ void gat_long_rows_kernel(int n_long, const int32_t* __restrict__ long_rows,
+// Long rows: c_v from their pieces (piece order), then g and ds_l as above;
+// one block per row.
+__global__ void __launch_bounds__(kBlock) gat_long_rows_kernel(int n_long, const int32_t* __restrict__ long_rows,
                                      const int64_t* __restrict__ piece_ptr,
                                      const float* __restrict__ cpart,
                                      const int64_t* __restrict__ rowptr,
@@ -301,22 +406,29 @@ __global__ void gat_long_rows_kernel(int n_long, const int32_t* __restrict__ lon
                                      const float* __restrict__ s_l, const float* __restrict__ s_r,
                                      const float* __restrict__ s_slot, float* __restrict__ g,
                                      float* __restrict__ ds_l) {
-  const int64_t i = warp_id();
+  __shared__ float red[kBlock / 32];
+  const int64_t i = blockIdx.x;
   if (i >= n_long) return;
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int row = long_rows[i];
   float c = 0.f;
   for (int64_t p = piece_ptr[i]; p < piece_ptr[i + 1]; ++p) c += cpart[p];
   const float sl = s_l[row];
   float dsl = 0.f;
-  for (int64_t k = rowptr[row] + lane; k < rowptr[row + 1]; k += 32) {
+  for (int64_t k = rowptr[row] + threadIdx.x; k < rowptr[row + 1]; k += blockDim.x) {
     const float pre = pre_score(sl, cr[k], s_r, s_slot);
     const float gk = alpha[k] * (g[k] - c) * (pre > 0.f ? 1.f : kSlope);
     g[k] = gk;
     dsl += gk;
   }
   dsl = warp_sum(dsl);
-  if (lane == 0) ds_l[row] = dsl;
+  if (lane == 0) red[wid] = dsl;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int q = 0; q < kBlock / 32; ++q) t += red[q];
+    ds_l[row] = t;
+  }
 }
 
 // Attention and score gradients at the transposed positions: alpha_t / g_t
@@ -364,17 +476,26 @@ __global__ void gat_slot_sum_kernel(int64_t S, const int64_t* __restrict__ srp,
   r[s] = acc;
 }
 
-// dY[u] += ds_r[u] a_r + ds_l[u] a_l.
+// dY[u] += ds_r[u] a_r + ds_l[u] a_l: a block of (F/4) x rows threads, one
+// float4 of a row each.
 __global__ void gat_score_terms_kernel(int64_t n, int F, const float* __restrict__ ds_r,
                                        const float* __restrict__ ds_l,
                                        const float* __restrict__ a_r,
                                        const float* __restrict__ a_l, float* __restrict__ dY,
                                        int64_t ldy) {
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= n * F) return;
-  const int64_t u = i / F;
-  const int j = (int)(i - u * F);
-  dY[u * ldy + j] += fmaf(ds_r[u], __ldg(a_r + j), ds_l[u] * __ldg(a_l + j));
+  const int c = threadIdx.x;  // chunk; F is a multiple of 16
+  const int64_t u = (int64_t)blockIdx.x * blockDim.y + threadIdx.y;
+  if (u >= n || 4 * c >= F) return;
+  const float r = ds_r[u], l = ds_l[u];
+  const float4 ar = __ldg(reinterpret_cast<const float4*>(a_r) + c);
+  const float4 al = __ldg(reinterpret_cast<const float4*>(a_l) + c);
+  float4* p = reinterpret_cast<float4*>(dY + u * ldy) + c;
+  float4 v = *p;
+  v.x += fmaf(r, ar.x, l * al.x);
+  v.y += fmaf(r, ar.y, l * al.y);
+  v.z += fmaf(r, ar.z, l * al.z);
+  v.w += fmaf(r, ar.w, l * al.w);
+  *p = v;
 }
 
 // part[blockIdx][j] = sum over the block's rows i (in order) of w[i] X_i[j],
@@ -389,23 +510,49 @@ __global__ void gat_colsum_kernel(int64_t rows, int64_t rows_per_block, int F,
   if (j >= F) return;
   const int64_t r0 = (int64_t)blockIdx.x * rows_per_block;
   const int64_t r1 = min(rows, r0 + rows_per_block);
-  float acc = 0.f;
-  for (int64_t i = r0; i < r1; ++i) {
+  // eight independent chains (row i feeds chain (i - r0) % 8), added in order
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  int64_t i = r0;
+  for (; i + 8 <= r1; i += 8) {
+    float x[8], wv[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int64_t r = i + q;
+      wv[q] = __ldg(w + r);
+      x[q] = packed ? dequant_elem(packed + __ldg(off + r), __ldg(bits + r), __ldg(meta + r).x,
+                                   __ldg(meta + r).y, j)
+                    : __ldg(X + r * ldx + j);
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) acc[q] = fmaf(wv[q], x[q], acc[q]);
+  }
+  for (int q = 0; i < r1; ++i, ++q) {
     const float x = packed ? dequant_elem(packed + __ldg(off + i), __ldg(bits + i), __ldg(meta + i).x,
                                           __ldg(meta + i).y, j)
                            : __ldg(X + i * ldx + j);
-    acc = fmaf(__ldg(w + i), x, acc);
+    acc[q] = fmaf(__ldg(w + i), x, acc[q]);
   }
-  part[(int64_t)blockIdx.x * F + j] = acc;
+  float sum = 0.f;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) sum += acc[q];
+  part[(int64_t)blockIdx.x * F + j] = sum;
 }
 
 __global__ void gat_colsum_reduce_kernel(int nparts, int F, const float* __restrict__ part,
                                          float* __restrict__ out) {
   const int j = blockIdx.x * blockDim.x + threadIdx.x;
   if (j >= F) return;
-  float acc = 0.f;
-  for (int b = 0; b < nparts; ++b) acc += part[(int64_t)b * F + j];
-  out[j] = acc;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  int b = 0;
+  for (; b + 8 <= nparts; b += 8) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) acc[q] += part[(int64_t)(b + q) * F + j];
+  }
+  for (int q = 0; b < nparts; ++b, ++q) acc[q] += part[(int64_t)b * F + j];
+  float sum = 0.f;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) sum += acc[q];
+  out[j] = sum;
 }
 
 unsigned warps_grid(int64_t warps) { return (unsigned)((warps * 32 + kBlock - 1) / kBlock); }
@@ -465,13 +612,13 @@ GatWs gat_ws_layout(void* base, size_t cap, const gnn_csr& csr, const gnn_bounda
 }
 
 gnn_status check_gat(const gnn_csr* csr, const gnn_boundary* bnd, int F_in, int F_out,
-                     const char* who) {
+                     const char* who, bool offsets = true) {
   if (!csr || csr->n < 1 || !csr->rowptr || (csr->nnz > 0 && !csr->col))
     return fail(GNN_ERR_INVALID_ARG, "%s: invalid csr", who);
   if (F_in < 1 || F_in > kMaxF) return fail(GNN_ERR_UNSUPPORTED, "%s: F_in=%d", who, F_in);
   if (F_out < 16 || F_out % 16 || F_out > 256)
     return fail(GNN_ERR_UNSUPPORTED, "%s: F_out must be a multiple of 16 in [16, 256]", who);
-  if (bnd && (bnd->n != csr->n || bnd->F != F_out || !bnd->col_remap || !bnd->local_cnt))
+  if (bnd && (bnd->n != csr->n || (offsets && bnd->F != F_out) || !bnd->col_remap || !bnd->local_cnt))
     return fail(GNN_ERR_INVALID_ARG, "%s: boundary must match csr with offsets for F_out", who);
   return GNN_OK;
 }
@@ -503,7 +650,7 @@ extern "C" gnn_status gnn_gat_index(const gnn_csr* csr, const gnn_boundary* bnd,
 
 extern "C" gnn_status gnn_gat_workspace(const gnn_csr* csr, const gnn_boundary* bnd, int32_t F_in,
                                         int32_t F_out, size_t* ws_bytes) {
-  gnn_status s = check_gat(csr, bnd, F_in, F_out, "gnn_gat_workspace");
+  gnn_status s = check_gat(csr, bnd, F_in, F_out, "gnn_gat_workspace", false);
   if (s != GNN_OK) return s;
   GNN_REQUIRE(ws_bytes, "gnn_gat_workspace: NULL ws_bytes");
   bool ok;
@@ -522,6 +669,8 @@ extern "C" gnn_status gnn_gat_layer_fwd(const gnn_csr* csr, const gnn_boundary* 
   gnn_status s = check_gat(csr, bnd, F_in, F_out, "gnn_gat_layer_fwd");
   if (s != GNN_OK) return s;
   GNN_REQUIRE(H_in && W && a_l && a_r && Hb && Y && alpha && H_out, "gnn_gat_layer_fwd: NULL pointer");
+  GNN_REQUIRE(((uintptr_t)a_l & 15) == 0 && ((uintptr_t)a_r & 15) == 0,
+              "gnn_gat_layer_fwd: a_l and a_r must be 16-byte aligned");
   GNN_REQUIRE(ldh >= F_in && ldh % 4 == 0 && ((uintptr_t)H_in & 15) == 0, "gnn_gat_layer_fwd: bad H_in");
   GNN_REQUIRE(ldhb >= round_up64(F_in, 16) && ldhb % 8 == 0 && ((uintptr_t)Hb & 15) == 0,
               "gnn_gat_layer_fwd: bad Hb");
@@ -553,8 +702,15 @@ extern "C" gnn_status gnn_gat_layer_fwd(const gnn_csr* csr, const gnn_boundary* 
     GNN_CHECK_LAUNCH();
   }
   const int32_t* cr = bnd ? bnd->col_remap : csr->col;
-  gat_softmax_kernel<<<warps_grid(n), kBlock, 0, st>>>(n, csr->rowptr, cr, w.s_l, w.s_r, w.s_slot,
-                                                       alpha);
+  // ordinary rows a warp each; the split plan's long rows a block each
+  const bool plan = csr->split_len > 0 && csr->n_long > 0;
+  gat_softmax_kernel<32><<<warps_grid(n), kBlock, 0, st>>>(n, csr->rowptr, cr, w.s_l, w.s_r,
+                                                           w.s_slot, alpha, plan ? csr->split_len : 0);
+  GNN_CHECK_LAUNCH();
+  if (plan) {
+    gat_softmax_long_kernel<<<(unsigned)csr->n_long, kBlock, 0, st>>>(
+        csr->n_long, csr->long_rows, csr->rowptr, cr, w.s_l, w.s_r, w.s_slot, alpha);
+  }
   GNN_CHECK_LAUNCH();
   return launch_spmm_fwd_w(*csr, bnd, alpha, Y, ldy, F_out, packed,
                            reinterpret_cast<const float2*>(meta), H_out, ldo, w.spmm, relu, st);
@@ -573,6 +729,8 @@ extern "C" gnn_status gnn_gat_layer_bwd(
   GNN_REQUIRE(tpos && dH_out && Hb && Y && alpha && W && a_l && a_r && dW && da_l && da_r,
               "gnn_gat_layer_bwd: NULL pointer");
   GNN_REQUIRE(ldg >= F_out && ldg % 4 == 0 && ((uintptr_t)dH_out & 15) == 0, "gnn_gat_layer_bwd: bad dH_out");
+  GNN_REQUIRE(((uintptr_t)a_l & 15) == 0 && ((uintptr_t)a_r & 15) == 0,
+              "gnn_gat_layer_bwd: a_l and a_r must be 16-byte aligned");
   GNN_REQUIRE(!relu || (H_out && ldo >= F_out && ldo % 4 == 0 && ((uintptr_t)H_out & 15) == 0),
               "gnn_gat_layer_bwd: relu needs H_out");
   GNN_REQUIRE(ldy >= round_up64(F_out, 4) && ldy % 4 == 0 && ((uintptr_t)Y & 15) == 0,
@@ -619,21 +777,22 @@ extern "C" gnn_status gnn_gat_layer_bwd(
     un.piece_beg = csr->piece_beg;
   }
   const int nch = (F_out + 3) / 4;
-  const unsigned gs = warps_grid(un.n_pieces + n);
+  const unsigned gs =
+      (unsigned)(((un.n_pieces + n) * 32 + GNN_GAT_SD_BLOCK - 1) / GNN_GAT_SD_BLOCK);
   const uint8_t* pk = slots ? packed_fwd : nullptr;
   const int64_t* so = slots ? bnd->slot_off : nullptr;
   const uint8_t* sbits = slots ? bnd->slot_bits : nullptr;
   if (nch <= 32)
-    gat_sddmm_kernel<1, 4><<<gs, kBlock, 0, st>>>(un, csr->rowptr, cr, alpha, Y, ldy, F_out, dz, ldz, pk,
+    gat_sddmm_kernel<1, 8><<<gs, GNN_GAT_SD_BLOCK, 0, st>>>(un, csr->rowptr, cr, alpha, Y, ldy, F_out, dz, ldz, pk,
                                                   mf, so, sbits, w.s_l, w.s_r, w.s_slot, g, w.cpart,
                                                   w.ds_l);
   else
-    gat_sddmm_kernel<2, 4><<<gs, kBlock, 0, st>>>(un, csr->rowptr, cr, alpha, Y, ldy, F_out, dz, ldz, pk,
+    gat_sddmm_kernel<2, GNN_GAT_SD_U2><<<gs, GNN_GAT_SD_BLOCK, 0, st>>>(un, csr->rowptr, cr, alpha, Y, ldy, F_out, dz, ldz, pk,
                                                   mf, so, sbits, w.s_l, w.s_r, w.s_slot, g, w.cpart,
                                                   w.ds_l);
   GNN_CHECK_LAUNCH();
   if (un.n_pieces > 0) {
-    gat_long_rows_kernel<<<warps_grid(csr->n_long), kBlock, 0, st>>>(
+    gat_long_rows_kernel<<<(unsigned)csr->n_long, kBlock, 0, st>>>(
         csr->n_long, csr->long_rows, csr->piece_ptr, w.cpart, csr->rowptr, cr, alpha, w.s_l, w.s_r,
         w.s_slot, g, w.ds_l);
     GNN_CHECK_LAUNCH();
@@ -659,8 +818,11 @@ extern "C" gnn_status gnn_gat_layer_bwd(
   s = launch_spmm_bwd_local_w(*csr, bnd, w.alpha_t, dz, ldz, F_out, packed_ws,
                               reinterpret_cast<const float2*>(meta_ws), w.dy, ldy4, w.spmm, st);
   if (s != GNN_OK) return s;
-  gat_score_terms_kernel<<<threads_grid((int64_t)n * F_out), kBlock, 0, st>>>(
-      n, F_out, w.ds_r, w.ds_l, a_r, a_l, w.dy, ldy4);
+  {
+    const dim3 blk(F_out / 4, kBlock / (F_out / 4));
+    gat_score_terms_kernel<<<(unsigned)((n + blk.y - 1) / blk.y), blk, 0, st>>>(
+        n, F_out, w.ds_r, w.ds_l, a_r, a_l, w.dy, ldy4);
+  }
   GNN_CHECK_LAUNCH();
   // da_l = sum_v ds_l[v] Y_v;  da_r = sum_u ds_r[u] Y_u + sum_s r[s] Y~_s
   const int bn = colsum_blocks(n), bs = colsum_blocks(S);
