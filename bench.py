@@ -302,28 +302,40 @@ def run_gpu(args, rank, world, local_rank):
         G.gnn_layer_bwd_tf(csr, bnd, dHs[l + 1], Hs[l + 1], l < L - 1, Mb[l], W[l], F, Fo, 2 * l + 1,
                            packed, meta, dW[l], dHs[l] if l > 0 else None, slot_off=offs[Fo], ws=ws)
 
-    def run_step(timed):
+    # with every layer aggregate-first, each backward aggregation stores the
+    # layer below's ReLU-gated bf16 gradient directly (one buffer per width)
+    fused = not any(tf)
+    dZbuf = {}
+    if fused:
+        for l in range(1, L):
+            if dims[l] not in dZbuf:
+                dZbuf[dims[l]] = torch.empty((n, G.ldz_for(dims[l])), dtype=torch.bfloat16, device=dev)
+
+    def run_step(timed, Hs=None, dHs=None):
+        Hs = H if Hs is None else Hs
+        dHs = dH if dHs is None else dHs
         for l in range(L):
             F, Fo = dims[l], dims[l + 1]
             so = offs[mwid[l]]
             if tf[l]:
                 if timed:
                     rec(("tf_fwd", l, 0))
-                tf_fwd(l, H)
+                tf_fwd(l, Hs)
                 if timed:
                     rec(("tf_fwd", l, 1))
                 continue
             if timed:
                 rec(("quant", l, 0))
-            G.gnn_quant_pack(H[l], F, bnd.slot_node, S, bnd.slot_bits, so, 2 * l, packed, meta)
+            G.gnn_quant_pack(Hs[l], F, bnd.slot_node, S, bnd.slot_bits, so, 2 * l, packed, meta)
             if timed:
                 rec(("quant", l, 1))
-            G.gnn_spmm_fwd(csr, bnd, H[l], F, packed, meta, Mb=Mb[l], slot_off=so, ws=wss)
+            G.gnn_spmm_fwd(csr, bnd, Hs[l], F, packed, meta, Mb=Mb[l], slot_off=so, ws=wss)
             if timed:
                 rec(("spmm_fwd", l, 1))
-            G.gnn_dense_fwd(Mb[l], n, F, W[l], Fo, l < L - 1, H[l + 1], ws=wsd)
+            G.gnn_dense_fwd(Mb[l], n, F, W[l], Fo, l < L - 1, Hs[l + 1], ws=wsd)
             if timed:
                 rec(("gemm_fwd", l, 1))
+        dZ_in = None  # the gated bf16 gradient the layer above stored for this layer
         for l in reversed(range(L)):
             F, Fo = dims[l], dims[l + 1]
             so = offs[mwid[l]]
@@ -331,18 +343,27 @@ def run_gpu(args, rank, world, local_rank):
             if tf[l]:
                 if timed:
                     rec(("tf_bwd", l, 0))
-                tf_bwd(l, H, dH)
+                tf_bwd(l, Hs, dHs)
                 if timed:
                     rec(("tf_bwd", l, 1))
                 continue
             if timed:
                 rec(("mask_dM_dW", l, 0))
-            G.gnn_dense_bwd(Mb[l], n, F, W[l], Fo, dH[l + 1], H[l + 1], l < L - 1,
-                            dMl if l > 0 else None, dW[l], ws=wsd)
+            if dZ_in is not None:
+                G.gnn_dense_bwd_z(Mb[l], n, F, W[l], Fo, dZ_in, dMl if l > 0 else None, dW[l], ws=wsd)
+            else:
+                G.gnn_dense_bwd(Mb[l], n, F, W[l], Fo, dHs[l + 1], Hs[l + 1], l < L - 1,
+                                dMl if l > 0 else None, dW[l], ws=wsd)
             if timed:
                 rec(("mask_dM_dW", l, 1))
             if l > 0:
-                G.gnn_spmm_bwd(csr, bnd, dMl, F, 2 * l + 1, packed, meta, dH[l], slot_off=so, ws=wss)
+                if fused:
+                    dZ_in = dZbuf[F]
+                    G.gnn_spmm_bwd_masked(csr, bnd, dMl, F, 2 * l + 1, packed, meta, Hs[l], dZ_in,
+                                          slot_off=so, ws=wss)
+                else:
+                    G.gnn_spmm_bwd(csr, bnd, dMl, F, 2 * l + 1, packed, meta, dHs[l], slot_off=so,
+                                   ws=wss)
                 if timed:
                     rec(("spmm_bwd", l, 1))
 
@@ -426,8 +447,12 @@ def run_gpu(args, rank, world, local_rank):
         flops["gemm"] += 2.0 * n * F * Fo * (3 if l > 0 else 2)
         if l > 0:
             kb4 = kernel_bytes(n, nnz, nc, S, F, slot_bits, slot_cut, 4 * F)
-            byt["spmm_bwd"] += kb4["bwd"]
+            # fused: the store reads the gate row (4F) in place of writing fp32
+            # dH (4F) and writes the bf16 gradient; the layer below skips its mask
+            byt["spmm_bwd"] += kb4["bwd"] + (2 * G.ldz_for(F) * n if fused else 0)
             flops["spmm"] += 2.0 * nnz * F
+        if fused and l < L - 1:
+            byt["mask_dM_dW"] -= gb["mask"]
     total_bytes = sum(byt.values())
 
     # an asynchronous epoch (SYLVIE guide section 10) through the layer API:
@@ -479,7 +504,7 @@ def run_gpu(args, rank, world, local_rank):
         del fwd_msgs, bwd_msgs
         torch.cuda.empty_cache()
 
-    # e2e through the layer API with host buffers: every step copies its inputs
+    # e2e through the public API with host buffers: every step copies its inputs
     # (layer-1 features, upstream gradient) from pinned host memory and reads
     # the weight gradients back.  The copy of step i+1's inputs runs on a copy
     # stream into the other of two device buffers while step i computes; each
@@ -514,23 +539,8 @@ def run_gpu(args, rank, world, local_rank):
             if not last:
                 issue_copy(i + 1)
             H0d, dHLd = bufs[k]
-            Hs = [H0d] + H[1:]
-            for l in range(L):
-                F, Fo = dims[l], dims[l + 1]
-                if tf[l]:
-                    tf_fwd(l, Hs)
-                    continue
-                G.gnn_layer_fwd(csr, bnd, Hs[l], F, W[l], Fo, l < L - 1, 2 * l, packed, meta, Mb[l],
-                                Hs[l + 1], slot_off=offs[F], ws=ws)
-            dHs = dH[:L] + [dHLd]
-            for l in reversed(range(L)):
-                F, Fo = dims[l], dims[l + 1]
-                if tf[l]:
-                    tf_bwd(l, Hs, dHs)
-                    continue
-                G.gnn_layer_bwd(csr, bnd, dHs[l + 1], Hs[l + 1], l < L - 1, Mb[l], W[l], F, Fo,
-                                2 * l + 1, packed, meta, dW[l], dHs[l] if l > 0 else None,
-                                slot_off=offs[F], ws=ws)
+            # the same public calls as the timed step, on this step's inputs
+            run_step(False, [H0d] + H[1:], dH[:L] + [dHLd])
             used[k].record(stream)
             for l in range(L):
                 dW_host[l].copy_(dW[l], non_blocking=True)

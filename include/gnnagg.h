@@ -383,7 +383,28 @@ gnn_status gnn_spmm_bwd_local(const gnn_csr* csr, const gnn_boundary* bnd, const
                               float* dH, int64_t ldh, void* ws, size_t ws_bytes,
                               gnn_stream_t stream);
 
-/* An asynchronous forward layer: the aggregation uses the messages of the
+/* The backward aggregation with the lower layer's ReLU gate fused into its
+ * store: dZ = bf16((A^T G) * 1[H_mask > 0]) (round to nearest even; H_mask
+ * NULL: no gate), the gradient at the pre-activation of the layer below in
+ * the bf16 layout its dense backward reads (row stride ldz >=
+ * round_up(F, 64), columns F..ldz-1 written as zero).  H_mask is that
+ * layer's output, i.e. this layer's input.  Messages, workspace and checks as
+ * gnn_spmm_bwd; the fp32 sums are those gnn_spmm_bwd stores.  No counterpart
+ * on the pages: it fuses the elementwise gate into the producing kernel. */
+gnn_status gnn_spmm_bwd_masked(const gnn_csr* csr, const gnn_boundary* bnd, const float* G,
+                               int64_t ldg, int32_t F, uint32_t seed, uint8_t* packed_ws,
+                               float* meta_ws, const float* H_mask, int64_t ldhm, uint16_t* dZ,
+                               int64_t ldz, void* ws, size_t ws_bytes, gnn_stream_t stream);
+
+/* gnn_dense_bwd from a given bf16 dZ (as gnn_spmm_bwd_masked writes it; row
+ * stride ldz >= round_up(F_out, 64), columns F_out..ldz-1 zero):
+ * dM = dZ W^T and dW = Mb^T dZ.  Either output may be NULL. */
+gnn_status gnn_dense_bwd_z(const uint16_t* Mb, int64_t ldmb, int64_t n, int32_t F_in,
+                           const uint16_t* W, int32_t F_out, const uint16_t* dZ, int64_t ldz,
+                           float* dM, int64_t ldm, float* dW, void* ws, size_t ws_bytes,
+                           gnn_stream_t stream);
+
+/* An asynchronous forward layer:/* An asynchronous forward layer: the aggregation uses the messages of the
  * previous epoch (packed_prev/meta_prev, as gnn_quant_pack wrote them from
  * that epoch's H_in), while this epoch's H_in is quantised and packed into
  * packed_next/meta_next on `aux` at the same time.  The call orders `stream`

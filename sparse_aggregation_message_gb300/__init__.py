@@ -26,6 +26,7 @@ __all__ = [
     "LdrState", "gnn_ldr_init", "gnn_ldr_update", "gnn_quant_divide",
     "gnn_layer_tf_workspace", "gnn_layer_fwd_tf", "gnn_layer_bwd_tf",
     "gnn_gat_index", "gnn_gat_workspace", "gnn_gat_layer_fwd", "gnn_gat_layer_bwd",
+    "gnn_spmm_bwd_masked", "gnn_dense_bwd_z", "ldz_for",
 ]
 
 
@@ -59,6 +60,11 @@ def ld_for(F: int) -> int:
 def ldb_for(F: int) -> int:
     """bf16 row stride for dense-transform inputs: F rounded up to 16."""
     return (F + 15) // 16 * 16
+
+
+def ldz_for(F: int) -> int:
+    """bf16 row stride of a pre-activation gradient dZ: F rounded up to 64."""
+    return (F + 63) // 64 * 64
 
 
 def rowbytes(b: int, F: int) -> int:
@@ -362,6 +368,18 @@ def gnn_spmm_bwd_local(csr: Csr, bnd: Boundary, G, F: int, packed, meta, dH, slo
          _ptr(packed), _ptr(meta), _ptr(dH), dH.stride(0), wp, wn, _stream(stream))
 
 
+def gnn_spmm_bwd_masked(csr: Csr, bnd: Optional[Boundary], G, F: int, seed: int, packed_ws, meta_ws,
+                        H_mask, dZ, slot_off=None, ws=None, stream=None) -> None:
+    """dZ (bf16, row stride >= ldz_for(F)) = bf16((A^T G) * 1[H_mask > 0])."""
+    c = csr.c()
+    cb = bnd.c(slot_off, F if slot_off is not None else None) if bnd is not None else None
+    wp, wn = _ws_args(csr, F, ws, G.device)
+    call("gnn_spmm_bwd_masked", ctypes.byref(c), ctypes.byref(cb) if cb is not None else None,
+         _ptr(G), G.stride(0), F, seed & 0xFFFFFFFF, _ptr(packed_ws), _ptr(meta_ws), _ptr(H_mask),
+         H_mask.stride(0) if H_mask is not None else 0, _ptr(dZ), dZ.stride(0), wp, wn,
+         _stream(stream))
+
+
 def gnn_kernel_launches() -> int:
     """Kernels launched through the library by this process so far."""
     return int(load().gnn_kernel_launches())
@@ -393,6 +411,14 @@ def gnn_dense_bwd(Mb, n: int, F_in: int, W, F_out: int, dH_out, H_out, relu: boo
         ws = _workspace(gnn_dense_workspace(n, F_in, F_out), Mb.device)
     call("gnn_dense_bwd", _ptr(Mb), Mb.stride(0), n, F_in, _ptr(W), F_out, _ptr(dH_out),
          dH_out.stride(0), _ptr(H_out), H_out.stride(0) if H_out is not None else 0, int(relu),
+         _ptr(dM), dM.stride(0) if dM is not None else 0, _ptr(dW), _ptr(ws), ws.numel(),
+         _stream(stream))
+
+
+def gnn_dense_bwd_z(Mb, n: int, F_in: int, W, F_out: int, dZ, dM, dW, ws=None, stream=None) -> None:
+    if ws is None:
+        ws = _workspace(gnn_dense_workspace(n, F_in, F_out), Mb.device)
+    call("gnn_dense_bwd_z", _ptr(Mb), Mb.stride(0), n, F_in, _ptr(W), F_out, _ptr(dZ), dZ.stride(0),
          _ptr(dM), dM.stride(0) if dM is not None else 0, _ptr(dW), _ptr(ws), ws.numel(),
          _stream(stream))
 

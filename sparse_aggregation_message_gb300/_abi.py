@@ -117,6 +117,10 @@ PROTOTYPES = {
                                          c_i64, c_vp, c_i64, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32,
                                          c_i32, c_u32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_vp,
                                          c_vp, c_size, c_vp]),
+    "gnn_spmm_bwd_masked": (ctypes.c_int, [P_csr, P_bnd, c_vp, c_i64, c_i32, c_u32, c_vp, c_vp, c_vp, c_i64,
+                                           c_vp, c_i64, c_vp, c_size, c_vp]),
+    "gnn_dense_bwd_z": (ctypes.c_int, [c_vp, c_i64, c_i64, c_i32, c_vp, c_i32, c_vp, c_i64, c_vp, c_i64, c_vp,
+                                       c_vp, c_size, c_vp]),
     "gnn_ldr_init": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_double, c_i32, c_i32, c_i32]),
     "gnn_ldr_update": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_double), c_i32,
                                       ctypes.c_double]),

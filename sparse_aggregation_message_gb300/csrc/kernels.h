@@ -59,6 +59,14 @@ gnn_status launch_spmm_bwd_local_w(const gnn_csr& csr, const gnn_boundary* bnd,
                                    const uint8_t* packed, const float2* meta, float* dH,
                                    int64_t ldh, float* partial, cudaStream_t st);
 
+// The backward aggregation with the next layer's ReLU gate and bf16 rounding
+// fused into its store: dZ = bf16((A^T G) * 1[hmask > 0]) (hmask NULL: no
+// gate), columns F..ldz-1 zero.
+gnn_status launch_spmm_bwd_masked(const gnn_csr& csr, const gnn_boundary* bnd, const float* Gm,
+                                  int64_t ldg, int F, uint32_t seed, uint8_t* packed_ws,
+                                  float2* meta_ws, const float* hmask, int64_t ldhm, uint16_t* dZ,
+                                  int64_t ldz, float* partial, cudaStream_t st);
+
 size_t spmm_workspace_bytes(const gnn_csr& csr, int F);
 
 // gnn_spmm_fwd with its argument checks, the output ReLU'd when relu != 0.

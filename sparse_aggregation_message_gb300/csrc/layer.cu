@@ -127,7 +127,32 @@ extern "C" gnn_status gnn_dense_bwd(const uint16_t* Mb, int64_t ldmb, int64_t n,
                         w, as_stream(stream));
 }
 
-// ------------------------------------------------------------------ layers
+extern "C" gnn_status gnn_dense_bwd_z(const uint16_t* Mb, int64_t ldmb, int64_t n, int32_t F_in,
+                                      const uint16_t* W, int32_t F_out, const uint16_t* dZ,
+                                      int64_t ldz, float* dM, int64_t ldm, float* dW, void* ws,
+                                      size_t ws_bytes, gnn_stream_t stream) {
+  gnn_status s = check_dims(n, F_in, F_out, "gnn_dense_bwd_z");
+  if (s != GNN_OK) return s;
+  if ((s = check_mb(Mb, ldmb, F_in, "gnn_dense_bwd_z")) != GNN_OK) return s;
+  GNN_REQUIRE(W && dZ && ldz >= round_up(F_out, 64) && ldz % 8 == 0 && ((uintptr_t)dZ & 15) == 0,
+              "gnn_dense_bwd_z: dZ needs ldz >= round_up(F_out, 64), a multiple of 8");
+  GNN_REQUIRE(!dM || (ldm >= (F_in + 3) / 4 * 4 && ldm % 4 == 0 && ((uintptr_t)dM & 15) == 0),
+              "gnn_dense_bwd_z: dM needs ldm >= round_up(F_in,4), a multiple of 4");
+  bool ok;
+  DenseWs w = dense_ws_layout(ws, ws_bytes, n, F_in, F_out, &ok);
+  GNN_REQUIRE(ws && ok, "gnn_dense_bwd_z: workspace too small (%zu < %zu)", ws_bytes, w.bytes);
+  if (n == 0) return GNN_OK;
+  cudaStream_t st = as_stream(stream);
+  if (dM) {
+    s = launch_gemm_tn(dZ, ldz, W, F_out, (int)n, F_in, F_out, dM, ldm, (int)round_up(F_in, 4), 0,
+                       st);
+    if (s != GNN_OK) return s;
+  }
+  if (dW) return launch_gemm_mn(Mb, ldmb, dZ, ldz, F_in, F_out, (int)n, dW, F_out, w.part, st);
+  return GNN_OK;
+}
+
+// ------------------------------------------------------------------ layers// ------------------------------------------------------------------ layers
 struct LayerWs {
   DenseWs dense;
   float* dM;

@@ -200,12 +200,27 @@ __device__ __forceinline__ void add_owned(int64_t r, const int64_t* __restrict__
 
 // Writes the group's chunks of row r: fp32 chunks below nch, bf16 chunks
 // below nch_b (zeros past F), both limited to the group's slice [c0, c1);
-// with relu, max(x, 0) of each.
+// with relu, max(x, 0) of each; with hmask, x where hmask's row is > 0, else 0.
 template <int G, int CPL>
 __device__ __forceinline__ void store_row(int64_t r, float4 (&acc)[CPL], int F, int nch,
                                           int nch_b, int c0, int c1, int gl,
                                           float* __restrict__ M, int64_t ldm,
-                                          __nv_bfloat16* __restrict__ Mb, int64_t ldmb, int relu) {
+                                          __nv_bfloat16* __restrict__ Mb, int64_t ldmb, int relu,
+                                          const float* __restrict__ hmask, int64_t ldhm) {
+  if (hmask) {  // keep x where the mask row is positive (the next ReLU's gate)
+    const float4* mrow = reinterpret_cast<const float4*>(hmask + r * ldhm);
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+      const int c = c0 + gl + i * G;
+      if (c < c1 && c < nch) {
+        const float4 h = __ldg(mrow + c);
+        if (!(h.x > 0.f)) acc[i].x = 0.f;
+        if (!(h.y > 0.f)) acc[i].y = 0.f;
+        if (!(h.z > 0.f)) acc[i].z = 0.f;
+        if (!(h.w > 0.f)) acc[i].w = 0.f;
+      }
+    }
+  }
   if (relu) {
 #pragma unroll
     for (int i = 0; i < CPL; ++i) {
@@ -286,7 +301,8 @@ __global__ void __launch_bounds__(GNN_ROWS_BLOCK, ((MODE == 1 && CPL == 3) ? 768
     const float* __restrict__ H, int64_t ldh, int F,
     SlotMsgs msg, const int64_t* __restrict__ own_ptr, const int32_t* __restrict__ own_slot,
     RowSplit sp, Slices sl, float* __restrict__ partial, float* __restrict__ M, int64_t ldm,
-    __nv_bfloat16* __restrict__ Mb, int64_t ldmb, int nch_b, int relu) {
+    __nv_bfloat16* __restrict__ Mb, int64_t ldmb, int nch_b, int relu,
+    const float* __restrict__ hmask, int64_t ldhm) {
   const int lane = threadIdx.x & 31;
   const int gl = lane & (G - 1);
   const int64_t g = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / G;
@@ -330,7 +346,7 @@ __global__ void __launch_bounds__(GNN_ROWS_BLOCK, ((MODE == 1 && CPL == 3) ? 768
     return;
   }
   if (MODE == kBwdOwned) add_owned<G, CPL>(row, own_ptr, own_slot, msg, c0, min(c1, nch), gl, acc);
-  store_row<G, CPL>(row, acc, F, nch, nch_b, c0, c1, gl, M, ldm, Mb, ldmb, relu);
+  store_row<G, CPL>(row, acc, F, nch, nch_b, c0, c1, gl, M, ldm, Mb, ldmb, relu, hmask, ldhm);
 }
 
 // Long rows: sum of their pieces' partial rows, 16 pieces at a time and then
@@ -340,7 +356,7 @@ __global__ void __launch_bounds__(256) spmm_fixup_kernel(
     RowSplit sp, Slices sl, const float* __restrict__ partial, int F, SlotMsgs msg,
     const int64_t* __restrict__ own_ptr, const int32_t* __restrict__ own_slot,
     float* __restrict__ M, int64_t ldm, __nv_bfloat16* __restrict__ Mb, int64_t ldmb,
-    int nch_b, int relu) {
+    int nch_b, int relu, const float* __restrict__ hmask, int64_t ldhm) {
   const int lane = threadIdx.x & 31;
   const int gl = lane & (G - 1);
   const int64_t g = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / G;
@@ -371,7 +387,7 @@ __global__ void __launch_bounds__(256) spmm_fixup_kernel(
     for (int k = 0; k < CPL; ++k) add4(acc[k], blk[k]);
   }
   if (MODE == kBwdOwned) add_owned<G, CPL>(row, own_ptr, own_slot, msg, c0, min(c1, nch), gl, acc);
-  store_row<G, CPL>(row, acc, F, nch, nch_b, c0, c1, gl, M, ldm, Mb, ldmb, relu);
+  store_row<G, CPL>(row, acc, F, nch, nch_b, c0, c1, gl, M, ldm, Mb, ldmb, relu, hmask, ldhm);
 }
 
 // P = fl(P + fl(r * a_r[j])) for the elements j of chunk c below F (the score
@@ -539,9 +555,11 @@ static gnn_status dispatch_rows(const gnn_csr& csr, const int32_t* colv, const f
                                 const int32_t* local_cnt, const float* H, int64_t ldh, int F,
                                 SlotMsgs msg, const int64_t* own_ptr, const int32_t* own_slot,
                                 float* partial, float* M, int64_t ldm, __nv_bfloat16* Mb,
-                                int64_t ldmb, cudaStream_t st, int relu = 0) {
+                                int64_t ldmb, cudaStream_t st, int relu = 0,
+                                const float* hmask = nullptr, int64_t ldhm = 0, int ldb_pad = 0) {
   const int nch = (F + 3) / 4;
-  const int nch_b = Mb ? ((F + 15) / 16) * 4 : nch;
+  // bf16 columns written (zeros past F): round_up(F, 16), or ldb_pad
+  const int nch_b = Mb ? (ldb_pad > 0 ? ldb_pad / 4 : ((F + 15) / 16) * 4) : nch;
   const int need = nch_b > nch ? nch_b : nch;
   const RowSplit sp = row_split_of(csr);
   // feature slices of at most GNN_SLICE_CHUNKS chunks keep every lane's registers low
@@ -558,12 +576,13 @@ static gnn_status dispatch_rows(const gnn_csr& csr, const int32_t* colv, const f
     const int64_t grid = (groups * G_ + block - 1) / block;                                    \
     spmm_rows_kernel<G_, CPL_, MODE, U_, UR_><<<(unsigned)grid, block, 0, st>>>(               \
         csr.n, csr.rowptr, colv, valv, local_cnt, H, ldh, F, msg, own_ptr, own_slot, sp, sl,   \
-        partial, M, ldm, Mb, ldmb, nch_b, relu);                                               \
+        partial, M, ldm, Mb, ldmb, nch_b, relu, hmask, ldhm);                                  \
     GNN_CHECK_LAUNCH();                                                                        \
     if (sp.n_long > 0) {                                                                       \
       const int64_t g2 = ((int64_t)sp.n_long * sl.ns * G_ + 255) / 256;                        \
       spmm_fixup_kernel<G_, CPL_, MODE><<<(unsigned)g2, 256, 0, st>>>(                         \
-          sp, sl, partial, F, msg, own_ptr, own_slot, M, ldm, Mb, ldmb, nch_b, relu);          \
+          sp, sl, partial, F, msg, own_ptr, own_slot, M, ldm, Mb, ldmb, nch_b, relu, hmask,    \
+          ldhm);                                                                               \
       GNN_CHECK_LAUNCH();                                                                      \
     }                                                                                          \
   } while (0)
@@ -594,6 +613,27 @@ gnn_status launch_spmm_fwd(const gnn_csr& csr, const gnn_boundary* bnd, const fl
   SlotMsgs msg{packed, meta, bnd->slot_off, bnd->slot_bits};
   return dispatch_rows<kFwdRemote>(csr, bnd->col_remap, bnd->val_remap, bnd->local_cnt, H, ldh, F,
                                    msg, nullptr, nullptr, partial, M, ldm, mb, ldmb, st, relu);
+}
+
+gnn_status launch_spmm_bwd_masked(const gnn_csr& csr, const gnn_boundary* bnd, const float* Gm,
+                                  int64_t ldg, int F, uint32_t seed, uint8_t* packed_ws,
+                                  float2* meta_ws, const float* hmask, int64_t ldhm, uint16_t* dZ,
+                                  int64_t ldz, float* partial, cudaStream_t st) {
+  if (csr.n == 0) return GNN_OK;
+  auto* zb = reinterpret_cast<__nv_bfloat16*>(dZ);
+  if (!bnd) {
+    const float* wt = csr.val_t ? csr.val_t : csr.val;
+    return dispatch_rows<kPlain>(csr, csr.col, wt, nullptr, Gm, ldg, F, SlotMsgs{}, nullptr,
+                                 nullptr, partial, nullptr, 0, zb, ldz, st, 0, hmask, ldhm,
+                                 (int)ldz);
+  }
+  gnn_status s = launch_halo_quant_pack(*bnd, Gm, ldg, F, seed, packed_ws, meta_ws, st);
+  if (s != GNN_OK) return s;
+  SlotMsgs msg{packed_ws, meta_ws, bnd->slot_off, bnd->slot_bits};
+  const float* wt = bnd->val_remap_t ? bnd->val_remap_t : bnd->val_remap;
+  return dispatch_rows<kBwdOwned>(csr, bnd->col_remap, wt, bnd->local_cnt, Gm, ldg, F, msg,
+                                  bnd->own_ptr, bnd->own_slot, partial, nullptr, 0, zb, ldz, st, 0,
+                                  hmask, ldhm, (int)ldz);
 }
 
 gnn_status launch_spmm_fwd_w(const gnn_csr& csr, const gnn_boundary* bnd, const float* weights,
@@ -825,6 +865,35 @@ extern "C" gnn_status gnn_spmm_bwd(const gnn_csr* csr, const gnn_boundary* bnd, 
   return launch_spmm_bwd(*csr, bnd, G, ldg, F, seed, packed_ws,
                          reinterpret_cast<float2*>(meta_ws), dH, ldh, static_cast<float*>(ws),
                          as_stream(stream));
+}
+
+extern "C" gnn_status gnn_spmm_bwd_masked(const gnn_csr* csr, const gnn_boundary* bnd,
+                                          const float* G, int64_t ldg, int32_t F, uint32_t seed,
+                                          uint8_t* packed_ws, float* meta_ws, const float* H_mask,
+                                          int64_t ldhm, uint16_t* dZ, int64_t ldz, void* ws,
+                                          size_t ws_bytes, gnn_stream_t stream) {
+  gnn_status st = check_csr(csr, "gnn_spmm_bwd_masked");
+  if (st != GNN_OK) return st;
+  GNN_REQUIRE(F >= 1, "gnn_spmm_bwd_masked: F must be >= 1");
+  if (F > kMaxF) return fail(GNN_ERR_UNSUPPORTED, "gnn_spmm_bwd_masked: F=%d > %d", F, kMaxF);
+  if (!csr->symmetric && !csr->val_t)
+    return fail(GNN_ERR_UNSUPPORTED, "gnn_spmm_bwd_masked: needs A^T (a symmetric CSR or val_t)");
+  if ((st = check_bnd(csr, bnd, F, true, "gnn_spmm_bwd_masked")) != GNN_OK) return st;
+  if ((st = check_ws(csr, F, ws, ws_bytes, "gnn_spmm_bwd_masked")) != GNN_OK) return st;
+  if (csr->n == 0) return GNN_OK;
+  GNN_REQUIRE(G && dZ, "gnn_spmm_bwd_masked: NULL G or dZ");
+  GNN_REQUIRE(ldg >= F && ldg % 4 == 0 && ((uintptr_t)G & 15) == 0,
+              "gnn_spmm_bwd_masked: ldg must be >= F, a multiple of 4, G 16-byte aligned");
+  GNN_REQUIRE(ldz >= (F + 63) / 64 * 64 && ldz % 8 == 0 && ((uintptr_t)dZ & 15) == 0,
+              "gnn_spmm_bwd_masked: ldz must be >= round_up(F, 64), a multiple of 8, dZ 16-byte aligned");
+  GNN_REQUIRE(!H_mask || (ldhm >= F && ldhm % 4 == 0 && ((uintptr_t)H_mask & 15) == 0),
+              "gnn_spmm_bwd_masked: ldhm must be >= F, a multiple of 4, H_mask 16-byte aligned");
+  GNN_REQUIRE(!bnd || bnd->n_slots == 0 ||
+                  (packed_ws && meta_ws && ((uintptr_t)packed_ws & 15) == 0 && ((uintptr_t)meta_ws & 7) == 0),
+              "gnn_spmm_bwd_masked: packed_ws (16-byte aligned) and meta_ws required with a boundary");
+  return launch_spmm_bwd_masked(*csr, bnd, G, ldg, F, seed, packed_ws,
+                                reinterpret_cast<float2*>(meta_ws), H_mask, ldhm, dZ, ldz,
+                                static_cast<float*>(ws), as_stream(stream));
 }
 
 // ---------------------------------------------------------------- no-allocation forward
