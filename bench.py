@@ -454,6 +454,15 @@ def run_gpu(args, rank, world, local_rank):
         if fused and l < L - 1:
             byt["mask_dM_dW"] -= gb["mask"]
     total_bytes = sum(byt.values())
+    # every array of an aggregate-first forward aggregation touched once: CSR
+    # metadata, each source row, the messages with their meta, bf16 output
+    compulsory = {}
+    for l in range(L):
+        if not tf[l]:
+            Fl = dims[l]
+            Ql = int(offs[Fl][-1].item())
+            compulsory[l] = (8 * (n + 1) + 8 * nnz + 4 * n + 4 * Fl * n + Ql + 17 * S
+                             + 2 * ldb[l] * n)
 
     # an asynchronous epoch (SYLVIE guide section 10) through the layer API:
     # each layer aggregates with the previous step's messages while this
@@ -569,7 +578,7 @@ def run_gpu(args, rank, world, local_rank):
     return dict(ms=ms, per=per, per_layer=per_layer, byt=byt, flops=flops, total_bytes=total_bytes,
                 launches=launches, clocks=clk.summary(), e2e=e2e, asy=asy, S=S, nnz=nnz, nnz_cut=nc, n=n,
                 Q=int(offs[mwid[0]][-1].item()), spmm_fwd_bytes_l=spmm_fwd_bytes_l, n_long=csr.n_long,
-                n_pieces=csr.n_pieces, dims=dims, P=P, tf=tf)
+                n_pieces=csr.n_pieces, dims=dims, P=P, tf=tf, compulsory=compulsory)
 
 
 # --------------------------------------------------------------- oracle (CPU) arm
@@ -727,12 +736,14 @@ def main():
             "hbm_frac": {k: (rate(k) / hbm if rate(k) else None) for k in ["spmm_fwd", "spmm_bwd", "quant"]},
         },
         "graph": {"n": r["n"], "nnz": r["nnz"], "nnz_cut": r["nnz_cut"], "slots": r["S"],
-                  "packed_bytes_layer1": r["Q"], "long_rows": r["n_long"], "pieces": r["n_pieces"],
+                  "packed_bytes_layer1": r["Q"], "meta_bytes_layer1": 8 * r["S"],
+                  "long_rows": r["n_long"], "pieces": r["n_pieces"],
                   "dims": r["dims"], "P": r["P"]},
         "roofline": {"kernel": f"gnn_spmm_fwd, layer {(L0 or 0) + 1} (aggregation with in-gather "
                                "dequantisation)",
                      "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": (achieved / hbm) if achieved else None, "traffic": traffic,
+                     "compulsory_bytes": r["compulsory"].get(L0) if L0 is not None else None,
                      "peak_source": peak_src},
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
