@@ -566,14 +566,17 @@ def run_gpu(args, rank, world, local_rank):
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
+        t_issue = time.perf_counter()
         e2e_run(args.e2e_steps)
+        t_issue = time.perf_counter() - t_issue
         b.record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms = a.elapsed_time(b) / args.e2e_steps
         G.gnn_sync_check()
         h2d = h_in.numel() * 4 + g_in.numel() * 4
         d2h = sum(x.numel() * 4 for x in dW_host)
-        e2e = dict(ms=e2e_ms, h2d=h2d, d2h=d2h)
+        e2e = dict(ms=e2e_ms, h2d=h2d, d2h=d2h, issue_ms=1e3 * t_issue / args.e2e_steps,
+                   pinned=bool(h_in.is_pinned() and g_in.is_pinned()))
 
     return dict(ms=ms, per=per, per_layer=per_layer, byt=byt, flops=flops, total_bytes=total_bytes,
                 launches=launches, clocks=clk.summary(), e2e=e2e, asy=asy, S=S, nnz=nnz, nnz_cut=nc, n=n,
@@ -753,7 +756,8 @@ def main():
         e_ms = max_over_ranks(e["ms"], world, "cuda")
         line["e2e"] = {"value": whole_job_rate(r["total_bytes"], world, e_ms), "unit": UNIT,
                        "ms_per_step": e_ms, "h2d_bytes_per_step": e["h2d"],
-                       "d2h_bytes_per_step": e["d2h"]}
+                       "d2h_bytes_per_step": e["d2h"],
+                       "host_issue_ms_per_step": e["issue_ms"], "pinned_inputs": e["pinned"]}
     if r["asy"]:
         a_ms = max_over_ranks(r["asy"]["ms"], world, "cuda")
         line["async_epoch"] = {"value": whole_job_rate(r["total_bytes"], world, a_ms), "unit": UNIT,
