@@ -302,6 +302,14 @@ def run_gpu(args, rank, world, local_rank):
         G.gnn_layer_bwd_tf(csr, bnd, dHs[l + 1], Hs[l + 1], l < L - 1, Mb[l], W[l], F, Fo, 2 * l + 1,
                            packed, meta, dW[l], dHs[l] if l > 0 else None, slot_off=offs[Fo], ws=ws)
 
+    # the cluster-blocked layout (dense tiles staged in shared memory), one plan
+    # for every width
+    bl = G.gnn_blocked_build(csr, bnd, args.blocked, split_len=args.split_len) if args.blocked else None
+    blk_ws = None
+    if bl is not None:
+        blk_ws = torch.empty(max(G._blocked_ws(bl, F, dev, None).numel() for F in widths),
+                             dtype=torch.uint8, device=dev)
+
     # with every layer aggregate-first, each backward aggregation stores the
     # layer below's ReLU-gated bf16 gradient directly (one buffer per width)
     fused = not any(tf)
@@ -329,7 +337,11 @@ def run_gpu(args, rank, world, local_rank):
             G.gnn_quant_pack(Hs[l], F, bnd.slot_node, S, bnd.slot_bits, so, 2 * l, packed, meta)
             if timed:
                 rec(("quant", l, 1))
-            G.gnn_spmm_fwd(csr, bnd, Hs[l], F, packed, meta, Mb=Mb[l], slot_off=so, ws=wss)
+            if bl is not None:
+                G.gnn_spmm_fwd_blocked(csr, bnd, bl, Hs[l], F, packed, meta, Mb=Mb[l], slot_off=so,
+                                       ws=blk_ws)
+            else:
+                G.gnn_spmm_fwd(csr, bnd, Hs[l], F, packed, meta, Mb=Mb[l], slot_off=so, ws=wss)
             if timed:
                 rec(("spmm_fwd", l, 1))
             G.gnn_dense_fwd(Mb[l], n, F, W[l], Fo, l < L - 1, Hs[l + 1], ws=wsd)
@@ -357,7 +369,11 @@ def run_gpu(args, rank, world, local_rank):
             if timed:
                 rec(("mask_dM_dW", l, 1))
             if l > 0:
-                if fused:
+                if fused and bl is not None:
+                    dZ_in = dZbuf[F]
+                    G.gnn_spmm_bwd_blocked(csr, bnd, bl, dMl, F, 2 * l + 1, packed, meta, H_mask=Hs[l],
+                                           dZ=dZ_in, slot_off=so, ws=blk_ws)
+                elif fused:
                     dZ_in = dZbuf[F]
                     G.gnn_spmm_bwd_masked(csr, bnd, dMl, F, 2 * l + 1, packed, meta, Hs[l], dZ_in,
                                           slot_off=so, ws=wss)
@@ -649,6 +665,9 @@ def main():
     ap.add_argument("--order", default="af", choices=["af", "tf", "auto"],
                     help="aggregate first (the message is H), transform first where F_out < F_in "
                          "(the message is H W), or per layer where it gathers fewer bytes")
+    ap.add_argument("--blocked", type=int, default=0,
+                    help="aggregate through the cluster-blocked layout, tiles with at least this "
+                         "many entries staged in shared memory (0: off; GCN weights only)")
     ap.add_argument("--aggregator", default="gcn", choices=["gcn", "mean", "gat"],
                     help="GCN weights 1/sqrt(d_v d_u), GraphSAGE mean weights 1/d_v, or one-head "
                          "graph attention on the transformed rows")
@@ -675,7 +694,7 @@ def main():
             torch.cuda.set_device(local_rank)
 
     config = {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload,
-              "aggregator": args.aggregator, "order": args.order,
+              "aggregator": args.aggregator, "order": args.order, "blocked": args.blocked or None,
               "base_bits": args.base_bits or None,
               "timing": "inputs larger than L2 (no flush); CUDA events on the launching stream",
               "parallelism": f"replicas x{world}"}
@@ -722,7 +741,7 @@ def main():
     dom_bytes = r["spmm_fwd_bytes_l"].get(L0) if L0 is not None else None
     achieved = dom_bytes / (t_dom * 1e-3) / 1e9 if t_dom else None
     default_path = (args.workload == "yelp" and args.order == "af" and args.aggregator == "gcn"
-                    and not args.base_bits)
+                    and not args.base_bits and not args.blocked)
     traffic = committed_traffic() if default_path else None
     line = {
         "metric": METRIC, "value": gbs, "unit": UNIT, "n_gpus": world, "steps": args.steps,

@@ -513,6 +513,61 @@ gnn_status gnn_gat_layer_bwd(const gnn_csr* csr, const gnn_boundary* bnd, const 
                              float* da_l, float* da_r, float* dH_in, int64_t ldh, float* g_out,
                              void* ws, size_t ws_bytes, gnn_stream_t stream);
 
+/* Cluster-blocked aggregation (the TorchGT guide's cluster-aware layout --
+ * place the node pairs with high locality next to each other -- applied to
+ * this aggregation).  The local entries (all entries without a boundary) are
+ * cut into T x T tiles of (row block, column block); a tile with at least
+ * min_entries entries is dense.  A dense tile's source rows are staged in
+ * shared memory, 128 columns at a time, and its entries read them there.
+ * Every other entry (sparse tiles, remote entries) forms `residual`, a CSR
+ * in the aggregation order (local ids, then ~slot), aggregated by the row
+ * kernels first; the tiles are then added in tile order.  Needs symmetric
+ * weights (GCN).  T must be 128.
+ *
+ * Build: gnn_blocked_workspace, gnn_blocked_count (synchronises; sizes),
+ * allocate the arrays, then gnn_blocked_build.  A split plan for the
+ * residual (gnn_csr_split on `residual`) is optional, as for any CSR.
+ * gnn_spmm_fwd_blocked / gnn_spmm_bwd_blocked compute what gnn_spmm_fwd /
+ * gnn_spmm_bwd (or gnn_spmm_bwd_masked with dZ) compute, the same messages,
+ * the fp32 sums in another order; workspace from gnn_blocked_spmm_workspace.
+ * No counterpart on the pages for the layout's use here. */
+typedef struct gnn_blocked {
+  int32_t T;             /* tile edge: 128                                    */
+  int32_t n_rb;          /* row blocks, ceil(n / T)                           */
+  int64_t n_tiles;       /* dense tiles                                       */
+  int64_t n_entries;     /* entries in dense tiles                            */
+  int64_t* rb_tile_ptr;  /* [n_rb+1] first dense tile of each row block      */
+  int32_t* tile_cb;      /* [n_tiles] column block                           */
+  int64_t* tile_ptr;     /* [n_tiles+1] first entry of each tile             */
+  int32_t* tile_rowptr;  /* [n_tiles*(T+1)] a tile's row offsets (relative)  */
+  uint8_t* ent_col;      /* [n_entries + 16] column within the block (padded) */
+  float* ent_val;        /* [n_entries] weight                               */
+  gnn_csr residual;      /* rowptr [n+1], col/val [nnz]; nnz = residual count */
+  int32_t* res_local_cnt;/* [n] local residual entries per row (with a boundary) */
+} gnn_blocked;
+
+gnn_status gnn_blocked_workspace(const gnn_csr* csr, const gnn_boundary* bnd, int32_t T,
+                                 int32_t min_entries, size_t* ws_bytes);
+gnn_status gnn_blocked_count(const gnn_csr* csr, const gnn_boundary* bnd, int32_t T,
+                             int32_t min_entries, int64_t* n_tiles, int64_t* n_entries,
+                             int64_t* n_residual, void* ws, size_t ws_bytes, gnn_stream_t stream);
+gnn_status gnn_blocked_build(const gnn_csr* csr, const gnn_boundary* bnd, int32_t T,
+                             int32_t min_entries, gnn_blocked* out, void* ws, size_t ws_bytes,
+                             gnn_stream_t stream);
+gnn_status gnn_blocked_spmm_workspace(const gnn_blocked* bp, int32_t F, size_t* ws_bytes);
+gnn_status gnn_spmm_fwd_blocked(const gnn_csr* csr, const gnn_boundary* bnd,
+                                const gnn_blocked* bp, const float* H, int64_t ldh, int32_t F,
+                                const uint8_t* packed, const float* meta, float* M, int64_t ldm,
+                                uint16_t* Mb, int64_t ldmb, void* ws, size_t ws_bytes,
+                                gnn_stream_t stream);
+/* dH (fp32) and/or dZ = bf16(dH * 1[H_mask > 0]) (H_mask may be NULL). */
+gnn_status gnn_spmm_bwd_blocked(const gnn_csr* csr, const gnn_boundary* bnd,
+                                const gnn_blocked* bp, const float* G, int64_t ldg, int32_t F,
+                                uint32_t seed, uint8_t* packed_ws, float* meta_ws,
+                                const float* H_mask, int64_t ldhm, float* dH, int64_t ldh,
+                                uint16_t* dZ, int64_t ldz, void* ws, size_t ws_bytes,
+                                gnn_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Epoch control (SYLVIE guide, sections 8 and 11).  Host code.              */
 /* ------------------------------------------------------------------------ */

@@ -11,7 +11,7 @@ from typing import Optional, Sequence
 
 from . import _abi
 from ._abi import (CSR_DEDUP, CSR_GCN, CSR_MEAN, CSR_SELF_LOOPS, CSR_SYMMETRIZE,  # noqa: F401
-                   GnnBitRule,
+                   GnnBitRule, GnnBlocked,
                    GnnBoundary, GnnCsr, GnnError, GnnLdrState, call, load)
 
 LdrState = GnnLdrState
@@ -27,6 +27,7 @@ __all__ = [
     "gnn_layer_tf_workspace", "gnn_layer_fwd_tf", "gnn_layer_bwd_tf",
     "gnn_gat_index", "gnn_gat_workspace", "gnn_gat_layer_fwd", "gnn_gat_layer_bwd",
     "gnn_spmm_bwd_masked", "gnn_dense_bwd_z", "ldz_for",
+    "Blocked", "gnn_blocked_build", "gnn_spmm_fwd_blocked", "gnn_spmm_bwd_blocked",
 ]
 
 
@@ -522,6 +523,100 @@ def gnn_layer_bwd_tf(csr: Csr, bnd: Optional[Boundary], dH_out, H_out, relu: boo
          int(relu), _ptr(Hb), Hb.stride(0), _ptr(W), F_in, F_out, seed & 0xFFFFFFFF,
          _ptr(packed_ws), _ptr(meta_ws), _ptr(dW), _ptr(dH_in),
          dH_in.stride(0) if dH_in is not None else 0, _ptr(ws), ws.numel(), _stream(stream))
+
+
+# ---------------------------------------------------------------- cluster-blocked aggregation
+@dataclass
+class Blocked:
+    T: int
+    n_rb: int
+    n_tiles: int
+    n_entries: int
+    arrays: dict
+    residual: Csr
+
+    def c(self) -> GnnBlocked:
+        a = self.arrays
+        b = GnnBlocked()
+        b.T, b.n_rb, b.n_tiles, b.n_entries = self.T, self.n_rb, self.n_tiles, self.n_entries
+        for k in ("rb_tile_ptr", "tile_cb", "tile_ptr", "tile_rowptr", "ent_col", "ent_val",
+                  "res_local_cnt"):
+            setattr(b, k, _ptr(a.get(k)))
+        b.residual = self.residual.c()
+        return b
+
+
+def gnn_blocked_build(csr: Csr, bnd: Optional[Boundary], min_entries: int = 1024, T: int = 128,
+                      split_len: int = 128, stream=None) -> Blocked:
+    """Dense T x T tiles (at least min_entries entries) and the residual CSR,
+    with a split plan of split_len entries for the residual (0: none)."""
+    torch = _torch()
+    dev = csr.rowptr.device
+    c = csr.c()
+    cb = bnd.c() if bnd is not None else None
+    pb = ctypes.byref(cb) if cb is not None else None
+    nb = ctypes.c_size_t()
+    call("gnn_blocked_workspace", ctypes.byref(c), pb, T, min_entries, ctypes.byref(nb))
+    ws = _workspace(nb.value, dev)
+    nt, ne, nr = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+    st = _stream(stream)
+    call("gnn_blocked_count", ctypes.byref(c), pb, T, min_entries, ctypes.byref(nt), ctypes.byref(ne),
+         ctypes.byref(nr), _ptr(ws), ws.numel(), st)
+    nt, ne, nr, n = nt.value, ne.value, nr.value, csr.n
+    n_rb = (n + T - 1) // T
+
+    def e(k, dt):
+        return torch.empty(max(k, 1), dtype=dt, device=dev)
+
+    a = dict(rb_tile_ptr=e(n_rb + 1, torch.int64), tile_cb=e(nt, torch.int32),
+             tile_ptr=e(nt + 1, torch.int64), tile_rowptr=e(nt * (T + 1), torch.int32),
+             ent_col=e(ne + 16, torch.uint8), ent_val=e(ne, torch.float32))
+    if bnd is not None:
+        a["res_local_cnt"] = e(n, torch.int32)
+    res = Csr(n=n, nnz=nr, symmetric=False, rowptr=e(n + 1, torch.int64), col=e(nr, torch.int32),
+              val=e(nr, torch.float32))
+    bl = Blocked(T=T, n_rb=n_rb, n_tiles=nt, n_entries=ne, arrays=a, residual=res)
+    out = bl.c()
+    call("gnn_blocked_build", ctypes.byref(c), pb, T, min_entries, ctypes.byref(out), _ptr(ws), ws.numel(), st)
+    res.col, res.val = res.col[:nr], res.val[:nr]
+    if split_len and nr > 0:
+        bl.residual = gnn_csr_split(res, split_len, stream)
+    return bl
+
+
+def _blocked_ws(bl: Blocked, F: int, device, ws):
+    if ws is not None:
+        return ws
+    nb = ctypes.c_size_t()
+    b = bl.c()
+    call("gnn_blocked_spmm_workspace", ctypes.byref(b), F, ctypes.byref(nb))
+    return _workspace(nb.value, device)
+
+
+def gnn_spmm_fwd_blocked(csr: Csr, bnd: Optional[Boundary], bl: Blocked, H, F: int, packed=None,
+                         meta=None, M=None, Mb=None, slot_off=None, ws=None, stream=None) -> None:
+    c = csr.c()
+    cb = bnd.c(slot_off, F if slot_off is not None else None) if bnd is not None else None
+    b = bl.c()
+    ws = _blocked_ws(bl, F, H.device, ws)
+    call("gnn_spmm_fwd_blocked", ctypes.byref(c), ctypes.byref(cb) if cb is not None else None,
+         ctypes.byref(b), _ptr(H), H.stride(0), F, _ptr(packed), _ptr(meta), _ptr(M),
+         M.stride(0) if M is not None else 0, _ptr(Mb), Mb.stride(0) if Mb is not None else 0,
+         _ptr(ws), ws.numel(), _stream(stream))
+
+
+def gnn_spmm_bwd_blocked(csr: Csr, bnd: Optional[Boundary], bl: Blocked, G, F: int, seed: int,
+                         packed_ws=None, meta_ws=None, H_mask=None, dH=None, dZ=None, slot_off=None,
+                         ws=None, stream=None) -> None:
+    c = csr.c()
+    cb = bnd.c(slot_off, F if slot_off is not None else None) if bnd is not None else None
+    b = bl.c()
+    ws = _blocked_ws(bl, F, G.device, ws)
+    call("gnn_spmm_bwd_blocked", ctypes.byref(c), ctypes.byref(cb) if cb is not None else None,
+         ctypes.byref(b), _ptr(G), G.stride(0), F, seed & 0xFFFFFFFF, _ptr(packed_ws), _ptr(meta_ws),
+         _ptr(H_mask), H_mask.stride(0) if H_mask is not None else 0, _ptr(dH),
+         dH.stride(0) if dH is not None else 0, _ptr(dZ), dZ.stride(0) if dZ is not None else 0,
+         _ptr(ws), ws.numel(), _stream(stream))
 
 
 # ---------------------------------------------------------------- attention aggregator

@@ -41,6 +41,12 @@ class GnnBoundary(ctypes.Structure):
                 ("val_remap_t", c_vp)]
 
 
+class GnnBlocked(ctypes.Structure):
+    _fields_ = [("T", c_i32), ("n_rb", c_i32), ("n_tiles", c_i64), ("n_entries", c_i64),
+                ("rb_tile_ptr", c_vp), ("tile_cb", c_vp), ("tile_ptr", c_vp), ("tile_rowptr", c_vp),
+                ("ent_col", c_vp), ("ent_val", c_vp), ("residual", GnnCsr), ("res_local_cnt", c_vp)]
+
+
 GNN_LDR_MAX_DELTA = 64
 
 
@@ -53,6 +59,7 @@ class GnnLdrState(ctypes.Structure):
 P_csr = ctypes.POINTER(GnnCsr)
 P_bnd = ctypes.POINTER(GnnBoundary)
 P_rule = ctypes.POINTER(GnnBitRule)
+P_blk = ctypes.POINTER(GnnBlocked)
 
 # name -> (restype, argtypes)
 PROTOTYPES = {
@@ -121,6 +128,14 @@ PROTOTYPES = {
                                            c_vp, c_i64, c_vp, c_size, c_vp]),
     "gnn_dense_bwd_z": (ctypes.c_int, [c_vp, c_i64, c_i64, c_i32, c_vp, c_i32, c_vp, c_i64, c_vp, c_i64, c_vp,
                                        c_vp, c_size, c_vp]),
+    "gnn_blocked_workspace": (ctypes.c_int, [P_csr, P_bnd, c_i32, c_i32, P_size]),
+    "gnn_blocked_count": (ctypes.c_int, [P_csr, P_bnd, c_i32, c_i32, P_i64, P_i64, P_i64, c_vp, c_size, c_vp]),
+    "gnn_blocked_build": (ctypes.c_int, [P_csr, P_bnd, c_i32, c_i32, P_blk, c_vp, c_size, c_vp]),
+    "gnn_blocked_spmm_workspace": (ctypes.c_int, [P_blk, c_i32, P_size]),
+    "gnn_spmm_fwd_blocked": (ctypes.c_int, [P_csr, P_bnd, P_blk, c_vp, c_i64, c_i32, c_vp, c_vp, c_vp, c_i64,
+                                            c_vp, c_i64, c_vp, c_size, c_vp]),
+    "gnn_spmm_bwd_blocked": (ctypes.c_int, [P_csr, P_bnd, P_blk, c_vp, c_i64, c_i32, c_u32, c_vp, c_vp, c_vp,
+                                            c_i64, c_vp, c_i64, c_vp, c_i64, c_vp, c_size, c_vp]),
     "gnn_ldr_init": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_double, c_i32, c_i32, c_i32]),
     "gnn_ldr_update": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_double), c_i32,
                                       ctypes.c_double]),
