@@ -72,11 +72,23 @@ __device__ __forceinline__ float div_rn(float a, const Divisor& d) {
   return __fmaf_rn(__fmaf_rn(-d.b, q, a), d.y, q);  // correctly rounded
 }
 
+// The rest of fmix32 after its first step h ^= h >> 16.
+__device__ __forceinline__ uint32_t fmix32_tail(uint32_t h) {
+  h *= 0x85ebca6bu;
+  h ^= h >> 13;
+  h *= 0xc2b2ae35u;
+  h ^= h >> 16;
+  return h;
+}
+
 // Codes of one quantised row at compile-time width B, packed into 32-bit
 // words: the 8/B chunks of a word sit on consecutive lanes of the group and
 // are OR-ed together with shuffles; zero words pad the row to rowbytes(B, F).
 // u_j * 2^24 is an integer below 2^24, so RN(t + u) is formed by one fused
-// multiply-add of that integer by 2^-24 (exact) and t.
+// multiply-add of that integer by 2^-24 (exact) and t.  hash32 of element
+// j = 4c + k (k < 4) is fmix32(key ^ j); j and 4c differ only in their two
+// low bits, so key ^ j = (key ^ 4c) ^ k and (key ^ j) >> 16 = (key ^ 4c) >> 16,
+// and fmix32's first step gives A_c ^ k with A_c formed once per chunk.
 template <int G, int CPL, int B, bool FAST>
 __device__ __forceinline__ void pack_codes(const float4 (&v)[CPL], int F, float mn, const Divisor& dv,
                                            bool flat, uint32_t key, uint32_t* __restrict__ words,
@@ -90,18 +102,20 @@ __device__ __forceinline__ void pack_codes(const float4 (&v)[CPL], int F, float 
     const int c = gl + i * G;
     uint32_t part = 0;
     if (c < nch && !flat) {
-      const bool full = 4 * c + 3 < F;
+      // all four codes, then the fields of elements >= F cleared (the caller
+      // gives those elements in-row values, so no element is special-cased)
+      const uint32_t kc = key ^ (uint32_t)(4 * c);
+      const uint32_t a = kc ^ (kc >> 16);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const int j = 4 * c + k;
-        if (full || j < F) {
-          const float t = div_rn<FAST>(__fsub_rn(elem(v[i], k), mn), dv);
-          const float m = static_cast<float>(fmix32(key ^ (uint32_t)j) >> 8);
-          // floor(t + u) >= 0 and below 2^24: round down while converting
-          const uint32_t q = min(__float2uint_rd(__fmaf_rn(m, 5.9604644775390625e-08f, t)), TOP);
-          part |= q << (k * B);
-        }
+        const float t = div_rn<FAST>(__fsub_rn(elem(v[i], k), mn), dv);
+        const float m = static_cast<float>(fmix32_tail(a ^ (uint32_t)k) >> 8);
+        // floor(t + u) >= 0 and below 2^24: round down while converting
+        const uint32_t q = min(__float2uint_rd(__fmaf_rn(m, 5.9604644775390625e-08f, t)), TOP);
+        part += q << (k * B);  // disjoint fields: + is |
       }
+      const int nv = F - 4 * c;  // elements of chunk c below F, >= 1
+      if (nv < 4) part &= (1u << (B * nv)) - 1u;
     }
     if (PER_WORD > 1) {
       part <<= (c % PER_WORD) * 4 * B;
@@ -138,17 +152,23 @@ __device__ __forceinline__ void quantize_pack_row(const float4 (&v)[CPL], int F,
     if (gl == 0) *meta = make_float2(0.f, 0.f);
     return;
   }
+  // elements >= F of the last chunk take the chunk's first element: min,
+  // max and the codes of the other elements are unchanged by in-row values
+  float4 x[CPL];
   float mn = __int_as_float(0x7f800000), mx = -__int_as_float(0x7f800000);
 #pragma unroll
   for (int i = 0; i < CPL; ++i) {
     const int c = gl + i * G;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      if (c < nch && 4 * c + k < F) {
-        const float x = elem(v[i], k);
-        mn = fminf(mn, x);
-        mx = fmaxf(mx, x);
-      }
+    x[i] = v[i];
+    const int nv = F - 4 * c;
+    if (nv < 4) {
+      if (nv < 2) x[i].y = x[i].x;
+      if (nv < 3) x[i].z = x[i].x;
+      x[i].w = x[i].x;
+    }
+    if (c < nch) {
+      mn = fminf(mn, fminf(fminf(x[i].x, x[i].y), fminf(x[i].z, x[i].w)));
+      mx = fmaxf(mx, fmaxf(fmaxf(x[i].x, x[i].y), fmaxf(x[i].z, x[i].w)));
     }
   }
 #pragma unroll
@@ -165,17 +185,17 @@ __device__ __forceinline__ void quantize_pack_row(const float4 (&v)[CPL], int F,
   const Divisor dv = make_divisor(scale);
   if (dv.fast || flat) {
     switch (b) {
-      case 1: pack_codes<G, CPL, 1, true>(v, F, mn, dv, flat, key, words, gl, gmask); break;
-      case 2: pack_codes<G, CPL, 2, true>(v, F, mn, dv, flat, key, words, gl, gmask); break;
-      case 4: pack_codes<G, CPL, 4, true>(v, F, mn, dv, flat, key, words, gl, gmask); break;
-      default: pack_codes<G, CPL, 8, true>(v, F, mn, dv, flat, key, words, gl, gmask); break;
+      case 1: pack_codes<G, CPL, 1, true>(x, F, mn, dv, flat, key, words, gl, gmask); break;
+      case 2: pack_codes<G, CPL, 2, true>(x, F, mn, dv, flat, key, words, gl, gmask); break;
+      case 4: pack_codes<G, CPL, 4, true>(x, F, mn, dv, flat, key, words, gl, gmask); break;
+      default: pack_codes<G, CPL, 8, true>(x, F, mn, dv, flat, key, words, gl, gmask); break;
     }
   } else {
     switch (b) {
-      case 1: pack_codes<G, CPL, 1, false>(v, F, mn, dv, flat, key, words, gl, gmask); break;
-      case 2: pack_codes<G, CPL, 2, false>(v, F, mn, dv, flat, key, words, gl, gmask); break;
-      case 4: pack_codes<G, CPL, 4, false>(v, F, mn, dv, flat, key, words, gl, gmask); break;
-      default: pack_codes<G, CPL, 8, false>(v, F, mn, dv, flat, key, words, gl, gmask); break;
+      case 1: pack_codes<G, CPL, 1, false>(x, F, mn, dv, flat, key, words, gl, gmask); break;
+      case 2: pack_codes<G, CPL, 2, false>(x, F, mn, dv, flat, key, words, gl, gmask); break;
+      case 4: pack_codes<G, CPL, 4, false>(x, F, mn, dv, flat, key, words, gl, gmask); break;
+      default: pack_codes<G, CPL, 8, false>(x, F, mn, dv, flat, key, words, gl, gmask); break;
     }
   }
   if (gl == 0) *meta = make_float2(mn, scale);
