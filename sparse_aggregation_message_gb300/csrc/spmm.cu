@@ -95,7 +95,10 @@ __device__ __forceinline__ void gather_local(int64_t beg, int64_t end, const int
 // codes (widths 1, 2, 4, 8 never straddle a word) before it dequantises and
 // adds them in entry order -- one register per chunk in flight instead of
 // four.  A round that meets a raw fp32 slot (width 32) reads float4 chunks.
-template <int G, int CPL, int UR>
+// OWNED: entries [beg, end) of own_slot (slot ids, weight 1) instead: the
+// messages a row owns, added in list order (w = 1 makes each fused
+// multiply-add an exact add).
+template <int G, int CPL, int UR, bool OWNED = false>
 __device__ __forceinline__ void gather_remote(int64_t beg, int64_t end,
                                                     const int32_t* __restrict__ col,
                                                     const float* __restrict__ val, int c0,
@@ -108,8 +111,8 @@ __device__ __forceinline__ void gather_remote(int64_t beg, int64_t end,
     uint32_t so16 = 0;
     float2 sm = make_float2(0.f, 0.f);
     if (e < end) {
-      const int s = ~__ldg(col + e);
-      w = __ldg(val + e);
+      const int s = OWNED ? __ldg(col + e) : ~__ldg(col + e);
+      w = OWNED ? 1.f : __ldg(val + e);
       sb = __ldg(msg.bits + s);
       so16 = (uint32_t)(__ldg(msg.off + s) >> 4);
       sm = __ldg(msg.meta + s);
@@ -178,24 +181,16 @@ __device__ __forceinline__ void gather_remote(int64_t beg, int64_t end,
   }
 }
 
-// acc += dequantised messages of the slots row r owns (backward).
-template <int G, int CPL>
+// acc += dequantised messages of the slots row r owns (backward), in the
+// owner list's order; the slots' widths, offsets and meta are loaded for G
+// slots at once and their words UR slots at a time.
+template <int G, int CPL, int UR>
 __device__ __forceinline__ void add_owned(int64_t r, const int64_t* __restrict__ own_ptr,
                                           const int32_t* __restrict__ own_slot,
                                           const SlotMsgs& msg, int c0, int c_end, int gl,
-                                          float4 (&acc)[CPL]) {
-  const int64_t ob = __ldg(own_ptr + r), oe = __ldg(own_ptr + r + 1);
-  for (int64_t o = ob; o < oe; ++o) {
-    const int s = __ldg(own_slot + o);
-    const int b = __ldg(msg.bits + s);
-    const float2 m = __ldg(msg.meta + s);
-    const uint8_t* row = msg.packed + __ldg(msg.off + s);
-#pragma unroll
-    for (int i = 0; i < CPL; ++i) {
-      const int c = c0 + gl + i * G;
-      if (c < c_end) add4(acc[i], dequant_chunk(row, b, m.x, m.y, c));
-    }
-  }
+                                          uint32_t gmask, float4 (&acc)[CPL]) {
+  gather_remote<G, CPL, UR, true>(__ldg(own_ptr + r), __ldg(own_ptr + r + 1), own_slot, nullptr, c0,
+                                  c_end, msg, gl, gmask, acc);
 }
 
 // Writes the group's chunks of row r: fp32 chunks below nch, bf16 chunks
@@ -345,7 +340,8 @@ __global__ void __launch_bounds__(GNN_ROWS_BLOCK, ((MODE == 1 && CPL == 3) ? 768
     }
     return;
   }
-  if (MODE == kBwdOwned) add_owned<G, CPL>(row, own_ptr, own_slot, msg, c0, min(c1, nch), gl, acc);
+  if (MODE == kBwdOwned)
+    add_owned<G, CPL, UR>(row, own_ptr, own_slot, msg, c0, min(c1, nch), gl, gmask, acc);
   store_row<G, CPL>(row, acc, F, nch, nch_b, c0, c1, gl, M, ldm, Mb, ldmb, relu, hmask, ldhm);
 }
 
@@ -386,7 +382,8 @@ __global__ void __launch_bounds__(256) spmm_fixup_kernel(
 #pragma unroll
     for (int k = 0; k < CPL; ++k) add4(acc[k], blk[k]);
   }
-  if (MODE == kBwdOwned) add_owned<G, CPL>(row, own_ptr, own_slot, msg, c0, min(c1, nch), gl, acc);
+  if (MODE == kBwdOwned)
+    add_owned<G, CPL, 2>(row, own_ptr, own_slot, msg, c0, min(c1, nch), gl, group_mask(G, lane), acc);
   store_row<G, CPL>(row, acc, F, nch, nch_b, c0, c1, gl, M, ldm, Mb, ldmb, relu, hmask, ldhm);
 }
 
