@@ -338,8 +338,34 @@ __global__ void __launch_bounds__(GNN_GAT_SD_BLOCK, GNN_GAT_SD_MINB) gat_sddmm_k
     }
     const int cnt = (int)min((int64_t)32, end - base);
     constexpr int GP = 32 / U;  // lanes that end up holding one entry's sum
+    const uint32_t rmask = __ballot_sync(0xffffffffu, e < end && cc < 0);  // remote entries
     for (int k = 0; k < cnt; k += U) {
       float d[U];
+      if (((rmask >> k) & ((1u << U) - 1u)) == 0u) {
+        // all U entries local: their rows' loads go out together
+        float4 x[U][CPL];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int ck = __shfl_sync(0xffffffffu, cc, k + u < cnt ? k + u : k);
+#pragma unroll
+          for (int i = 0; i < CPL; ++i) {
+            const int c = lane + 32 * i;
+            x[u][i] = c < nch ? __ldg(Y4 + (int64_t)ck * ldy4 + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          float acc = 0.f;
+#pragma unroll
+          for (int i = 0; i < CPL; ++i) {
+            acc = fmaf(z[i].x, x[u][i].x, acc);
+            acc = fmaf(z[i].y, x[u][i].y, acc);
+            acc = fmaf(z[i].z, x[u][i].z, acc);
+            acc = fmaf(z[i].w, x[u][i].w, acc);
+          }
+          d[u] = acc;
+        }
+      } else {
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int src = k + u < cnt ? k + u : k;
@@ -367,6 +393,7 @@ __global__ void __launch_bounds__(GNN_GAT_SD_BLOCK, GNN_GAT_SD_MINB) gat_sddmm_k
           }
         }
         d[u] = acc;
+      }
       }
       const float t = reduce_scatter<U>(d, lane);
       const int idx = lane / GP;
