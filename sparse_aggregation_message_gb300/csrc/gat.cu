@@ -565,6 +565,69 @@ __global__ void gat_colsum_kernel(int64_t rows, int64_t rows_per_block, int F,
   part[(int64_t)blockIdx.x * F + j] = sum;
 }
 
+// part_l[b] / part_r[b] = the column sums of rows [b*rpb, (b+1)*rpb) of X
+// weighted by w_l and by w_r, in one pass over X.  Thread t covers chunk
+// t % nch of the rows t / nch + k*rp (rp = 256 / nch row phases), four rows
+// in flight; the row phases are then added in order through shared memory.
+__global__ void __launch_bounds__(256) gat_colsum2_kernel(int64_t rows, int64_t rpb, int F,
+                                                          const float* __restrict__ w_l,
+                                                          const float* __restrict__ w_r,
+                                                          const float* __restrict__ X, int64_t ldx,
+                                                          float* __restrict__ part_l,
+                                                          float* __restrict__ part_r) {
+  __shared__ float4 sl[256], sr[256];
+  const int nch = (F + 3) >> 2;
+  const int rp = 256 / nch;  // F <= 1024: at least one row phase
+  const int t = threadIdx.x;
+  const int c = t % nch, ph = t / nch;
+  const int64_t r0 = (int64_t)blockIdx.x * rpb;
+  const int64_t r1 = min(rows, r0 + rpb);
+  float4 al = make_float4(0.f, 0.f, 0.f, 0.f), ar = al;
+  if (ph < rp) {
+    int64_t r = r0 + ph;
+    for (; r + 3 * rp < r1; r += 4 * rp) {
+      float4 x[4];
+      float a[4], b[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int64_t rr = r + q * rp;
+        x[q] = __ldg(reinterpret_cast<const float4*>(X + rr * ldx) + c);
+        a[q] = __ldg(w_l + rr);
+        b[q] = __ldg(w_r + rr);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        fma4(al, a[q], x[q]);
+        fma4(ar, b[q], x[q]);
+      }
+    }
+    for (; r < r1; r += rp) {
+      const float4 x = __ldg(reinterpret_cast<const float4*>(X + r * ldx) + c);
+      fma4(al, __ldg(w_l + r), x);
+      fma4(ar, __ldg(w_r + r), x);
+    }
+  }
+  sl[t] = al;
+  sr[t] = ar;
+  __syncthreads();
+  if (t < nch) {
+    float4 sa = sl[t], sb = sr[t];
+    for (int q = 1; q < rp; ++q) {
+      add4(sa, sl[q * nch + t]);
+      add4(sb, sr[q * nch + t]);
+    }
+    float* pl = part_l + (int64_t)blockIdx.x * F + 4 * t;
+    float* pr = part_r + (int64_t)blockIdx.x * F + 4 * t;
+    const float va[4] = {sa.x, sa.y, sa.z, sa.w}, vb[4] = {sb.x, sb.y, sb.z, sb.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (4 * t + e < F) {
+        pl[e] = va[e];
+        pr[e] = vb[e];
+      }
+  }
+}
+
 __global__ void gat_colsum_reduce_kernel(int nparts, int F, const float* __restrict__ part,
                                          float* __restrict__ out) {
   const int j = blockIdx.x * blockDim.x + threadIdx.x;
@@ -853,13 +916,12 @@ extern "C" gnn_status gnn_gat_layer_bwd(
   GNN_CHECK_LAUNCH();
   // da_l = sum_v ds_l[v] Y_v;  da_r = sum_u ds_r[u] Y_u + sum_s r[s] Y~_s
   const int bn = colsum_blocks(n), bs = colsum_blocks(S);
-  gat_colsum_kernel<<<bn, 256, 0, st>>>(n, colsum_rows_per_block(n), F_out, w.ds_l, Y, ldy, nullptr,
-                                        nullptr, nullptr, nullptr, w.part_l);
-  GNN_CHECK_LAUNCH();
+  if (bn > 0) {
+    gat_colsum2_kernel<<<bn, 256, 0, st>>>(n, colsum_rows_per_block(n), F_out, w.ds_l, w.ds_r, Y, ldy,
+                                           w.part_l, w.part_r);
+    GNN_CHECK_LAUNCH();
+  }
   gat_colsum_reduce_kernel<<<1, 256, 0, st>>>(bn, F_out, w.part_l, da_l);
-  GNN_CHECK_LAUNCH();
-  gat_colsum_kernel<<<bn, 256, 0, st>>>(n, colsum_rows_per_block(n), F_out, w.ds_r, Y, ldy, nullptr,
-                                        nullptr, nullptr, nullptr, w.part_r);
   GNN_CHECK_LAUNCH();
   if (bs > 0) {
     gat_colsum_kernel<<<bs, 256, 0, st>>>(S, colsum_rows_per_block(S), F_out, w.r, nullptr, 0,
