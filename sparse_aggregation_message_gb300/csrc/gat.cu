@@ -525,46 +525,6 @@ __global__ void gat_score_terms_kernel(int64_t n, int F, const float* __restrict
   *p = v;
 }
 
-// part[blockIdx][j] = sum over the block's rows i (in order) of w[i] X_i[j],
-// X_i the row i of X or, with packed, the dequantised message of slot i.
-__global__ void gat_colsum_kernel(int64_t rows, int64_t rows_per_block, int F,
-                                  const float* __restrict__ w, const float* __restrict__ X,
-                                  int64_t ldx, const uint8_t* __restrict__ packed,
-                                  const float2* __restrict__ meta,
-                                  const int64_t* __restrict__ off,
-                                  const uint8_t* __restrict__ bits, float* __restrict__ part) {
-  const int j = threadIdx.x;
-  if (j >= F) return;
-  const int64_t r0 = (int64_t)blockIdx.x * rows_per_block;
-  const int64_t r1 = min(rows, r0 + rows_per_block);
-  // eight independent chains (row i feeds chain (i - r0) % 8), added in order
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  int64_t i = r0;
-  for (; i + 8 <= r1; i += 8) {
-    float x[8], wv[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int64_t r = i + q;
-      wv[q] = __ldg(w + r);
-      x[q] = packed ? dequant_elem(packed + __ldg(off + r), __ldg(bits + r), __ldg(meta + r).x,
-                                   __ldg(meta + r).y, j)
-                    : __ldg(X + r * ldx + j);
-    }
-#pragma unroll
-    for (int q = 0; q < 8; ++q) acc[q] = fmaf(wv[q], x[q], acc[q]);
-  }
-  for (int q = 0; i < r1; ++i, ++q) {
-    const float x = packed ? dequant_elem(packed + __ldg(off + i), __ldg(bits + i), __ldg(meta + i).x,
-                                          __ldg(meta + i).y, j)
-                           : __ldg(X + i * ldx + j);
-    acc[q] = fmaf(__ldg(w + i), x, acc[q]);
-  }
-  float sum = 0.f;
-#pragma unroll
-  for (int q = 0; q < 8; ++q) sum += acc[q];
-  part[(int64_t)blockIdx.x * F + j] = sum;
-}
-
 // part_l[b] / part_r[b] = the column sums of rows [b*rpb, (b+1)*rpb) of X
 // weighted by w_l and by w_r, in one pass over X.  Thread t covers chunk
 // t % nch of the rows t / nch + k*rp (rp = 256 / nch row phases), four rows
@@ -625,6 +585,58 @@ __global__ void __launch_bounds__(256) gat_colsum2_kernel(int64_t rows, int64_t 
         pl[e] = va[e];
         pr[e] = vb[e];
       }
+  }
+}
+
+// part[b] = sum over slots [b*rpb, (b+1)*rpb) of w[s] times slot s's
+// dequantised message (the receiver's values).  Thread t covers chunk
+// t % nch (four elements from one 32-bit word) of the slots t / nch + k*rp,
+// four slots in flight; row phases are added in order through shared memory.
+__global__ void __launch_bounds__(256) gat_colsum_slots_kernel(int64_t S, int64_t rpb, int F,
+                                                               const float* __restrict__ w,
+                                                               const uint8_t* __restrict__ packed,
+                                                               const float2* __restrict__ meta,
+                                                               const int64_t* __restrict__ off,
+                                                               const uint8_t* __restrict__ bits,
+                                                               float* __restrict__ part) {
+  __shared__ float4 sh[256];
+  const int nch = (F + 3) >> 2;
+  const int rp = 256 / nch;
+  const int t = threadIdx.x;
+  const int c = t % nch, ph = t / nch;
+  const int64_t r0 = (int64_t)blockIdx.x * rpb;
+  const int64_t r1 = min(S, r0 + rpb);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (ph < rp) {
+    int64_t s = r0 + ph;
+    for (; s + 3 * rp < r1; s += 4 * rp) {
+      float4 x[4];
+      float a[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int64_t ss = s + q * rp;
+        const float2 m = __ldg(meta + ss);
+        x[q] = dequant_chunk(packed + __ldg(off + ss), __ldg(bits + ss), m.x, m.y, c);
+        a[q] = __ldg(w + ss);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) fma4(acc, a[q], x[q]);
+    }
+    for (; s < r1; s += rp) {
+      const float2 m = __ldg(meta + s);
+      fma4(acc, __ldg(w + s), dequant_chunk(packed + __ldg(off + s), __ldg(bits + s), m.x, m.y, c));
+    }
+  }
+  sh[t] = acc;
+  __syncthreads();
+  if (t < nch) {
+    float4 sa = sh[t];
+    for (int q = 1; q < rp; ++q) add4(sa, sh[q * nch + t]);
+    float* pp = part + (int64_t)blockIdx.x * F + 4 * t;
+    const float va[4] = {sa.x, sa.y, sa.z, sa.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (4 * t + e < F) pp[e] = va[e];
   }
 }
 
@@ -924,9 +936,9 @@ extern "C" gnn_status gnn_gat_layer_bwd(
   gat_colsum_reduce_kernel<<<1, 256, 0, st>>>(bn, F_out, w.part_l, da_l);
   GNN_CHECK_LAUNCH();
   if (bs > 0) {
-    gat_colsum_kernel<<<bs, 256, 0, st>>>(S, colsum_rows_per_block(S), F_out, w.r, nullptr, 0,
-                                          packed_fwd, mf, bnd->slot_off, bnd->slot_bits,
-                                          w.part_r + (int64_t)bn * F_out);
+    gat_colsum_slots_kernel<<<bs, 256, 0, st>>>(S, colsum_rows_per_block(S), F_out, w.r, packed_fwd, mf,
+                                                bnd->slot_off, bnd->slot_bits,
+                                                w.part_r + (int64_t)bn * F_out);
     GNN_CHECK_LAUNCH();
   }
   gat_colsum_reduce_kernel<<<1, 256, 0, st>>>(bn + bs, F_out, w.part_r, da_r);
