@@ -339,9 +339,50 @@ __global__ void __launch_bounds__(GNN_GAT_SD_BLOCK, GNN_GAT_SD_MINB) gat_sddmm_k
     const int cnt = (int)min((int64_t)32, end - base);
     constexpr int GP = 32 / U;  // lanes that end up holding one entry's sum
     const uint32_t rmask = __ballot_sync(0xffffffffu, e < end && cc < 0);  // remote entries
+    const uint32_t raw = __ballot_sync(0xffffffffu, e < end && cc < 0 && sb == 32);
     for (int k = 0; k < cnt; k += U) {
       float d[U];
-      if (((rmask >> k) & ((1u << U) - 1u)) == 0u) {
+      const int lim = cnt - k;
+      const uint32_t vmask = lim >= U ? (1u << U) - 1u : (1u << lim) - 1u;  // the round's entries
+      if (((rmask >> k) & vmask) == vmask && ((raw >> k) & vmask) == 0u) {
+        // all entries remote and packed: each chunk's 32-bit word for every
+        // entry is loaded before any is decoded
+        uint32_t wd[U][CPL];
+        float mnk[U], sck[U];
+        int bk[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int src = k + u < cnt ? k + u : k;
+          bk[u] = __shfl_sync(0xffffffffu, sb, src);
+          const uint32_t ok = __shfl_sync(0xffffffffu, so16, src);
+          mnk[u] = __shfl_sync(0xffffffffu, sm.x, src);
+          sck[u] = __shfl_sync(0xffffffffu, sm.y, src);
+          const uint32_t* row = reinterpret_cast<const uint32_t*>(packed + ((size_t)ok << 4));
+#pragma unroll
+          for (int i = 0; i < CPL; ++i) {
+            const int c = lane + 32 * i;
+            wd[u][i] = c < nch ? __ldg(row + (((uint32_t)c * (uint32_t)bk[u]) >> 3)) : 0u;
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int b = bk[u];
+          const uint32_t m = (1u << b) - 1u;
+          float acc = 0.f;
+#pragma unroll
+          for (int i = 0; i < CPL; ++i) {
+            const int c = lane + 32 * i;
+            if (c < nch) {
+              const uint32_t bits4 = wd[u][i] >> (((uint32_t)c * (uint32_t)b * 4u) & 31u);
+              acc = fmaf(z[i].x, __fadd_rn(__fmul_rn(sck[u], (float)(bits4 & m)), mnk[u]), acc);
+              acc = fmaf(z[i].y, __fadd_rn(__fmul_rn(sck[u], (float)((bits4 >> b) & m)), mnk[u]), acc);
+              acc = fmaf(z[i].z, __fadd_rn(__fmul_rn(sck[u], (float)((bits4 >> (2 * b)) & m)), mnk[u]), acc);
+              acc = fmaf(z[i].w, __fadd_rn(__fmul_rn(sck[u], (float)((bits4 >> (3 * b)) & m)), mnk[u]), acc);
+            }
+          }
+          d[u] = acc;
+        }
+      } else if (((rmask >> k) & ((1u << U) - 1u)) == 0u) {
         // all U entries local: their rows' loads go out together
         float4 x[U][CPL];
 #pragma unroll
