@@ -251,12 +251,14 @@ struct Slices {
   int cs;
 };
 
-// Threads per block of the rows kernel.  Small blocks free their slot as soon
-// as their few rows finish, which keeps more warps resident when row lengths
-// vary.
-#ifndef GNN_ROWS_BLOCK
-#define GNN_ROWS_BLOCK 64
-#endif
+// Threads per block of the rows kernel: one warp with messages (forward
+// with remote rows, backward), two without.  Small blocks free their slot as
+// soon as their few rows finish, which keeps more warps resident when row
+// lengths vary.
+template <int MODE>
+constexpr int rows_block() {
+  return MODE == 0 ? 64 : 32;
+}
 // Entries gathered per round: local (U, by chunks per lane; the forward with
 // remote rows has its own) and remote (UR) entries, each measured best on the
 // power-law workloads; the 3-chunk layout gathers 2 local entries.
@@ -289,7 +291,7 @@ struct Slices {
 // 1024 resident threads per SM (64 registers each); the 3-chunk forward with
 // remote rows needs up to 80 and keeps 768.
 template <int G, int CPL, int MODE, int U, int UR>
-__global__ void __launch_bounds__(GNN_ROWS_BLOCK, ((MODE == 1 && CPL == 3) ? 768 : 1024) / GNN_ROWS_BLOCK)
+__global__ void __launch_bounds__(rows_block<MODE>(), ((MODE == 1 && CPL == 3) ? 768 : 1024) / rows_block<MODE>())
     spmm_rows_kernel(
     int n, const int64_t* __restrict__ rowptr, const int32_t* __restrict__ col,
     const float* __restrict__ val, const int32_t* __restrict__ local_cnt,
@@ -566,7 +568,7 @@ static gnn_status dispatch_rows(const gnn_csr& csr, const int32_t* colv, const f
     sl.cs = (need + sl.ns - 1) / sl.ns;
   }
   const int cpl = (sl.cs + 31) / 32;
-  const int block = GNN_ROWS_BLOCK;
+  constexpr int block = rows_block<MODE>();
 #define GNN_ROWS(G_, CPL_, U_, UR_)                                                            \
   do {                                                                                         \
     const int64_t groups = ((int64_t)csr.n + sp.n_pieces) * sl.ns;                             \
