@@ -406,35 +406,35 @@ __global__ void __launch_bounds__(GNN_GAT_SD_BLOCK, GNN_GAT_SD_MINB) gat_sddmm_k
           }
           d[u] = acc;
         }
-      } else {
+      } else {  // local and remote entries mixed: one entry at a time
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int src = k + u < cnt ? k + u : k;
-        const int32_t ck = __shfl_sync(0xffffffffu, cc, src);
-        int bk = 0;
-        uint32_t ok = 0;
-        float mnk = 0.f, sck = 0.f;
-        if (ck < 0) {  // uniform across the warp
-          bk = __shfl_sync(0xffffffffu, sb, src);
-          ok = __shfl_sync(0xffffffffu, so16, src);
-          mnk = __shfl_sync(0xffffffffu, sm.x, src);
-          sck = __shfl_sync(0xffffffffu, sm.y, src);
-        }
-        float acc = 0.f;
-#pragma unroll
-        for (int i = 0; i < CPL; ++i) {
-          const int c = lane + 32 * i;
-          if (c < nch) {
-            const float4 x = ck >= 0 ? __ldg(Y4 + (int64_t)ck * ldy4 + c)
-                                     : dequant_chunk(packed + ((size_t)ok << 4), bk, mnk, sck, c);
-            acc = fmaf(z[i].x, x.x, acc);
-            acc = fmaf(z[i].y, x.y, acc);
-            acc = fmaf(z[i].z, x.z, acc);
-            acc = fmaf(z[i].w, x.w, acc);
+        for (int u = 0; u < U; ++u) {
+          const int src = k + u < cnt ? k + u : k;
+          const int32_t ck = __shfl_sync(0xffffffffu, cc, src);
+          int bk = 0;
+          uint32_t ok = 0;
+          float mnk = 0.f, sck = 0.f;
+          if (ck < 0) {  // uniform across the warp
+            bk = __shfl_sync(0xffffffffu, sb, src);
+            ok = __shfl_sync(0xffffffffu, so16, src);
+            mnk = __shfl_sync(0xffffffffu, sm.x, src);
+            sck = __shfl_sync(0xffffffffu, sm.y, src);
           }
+          float acc = 0.f;
+#pragma unroll
+          for (int i = 0; i < CPL; ++i) {
+            const int c = lane + 32 * i;
+            if (c < nch) {
+              const float4 x = ck >= 0 ? __ldg(Y4 + (int64_t)ck * ldy4 + c)
+                                       : dequant_chunk(packed + ((size_t)ok << 4), bk, mnk, sck, c);
+              acc = fmaf(z[i].x, x.x, acc);
+              acc = fmaf(z[i].y, x.y, acc);
+              acc = fmaf(z[i].z, x.z, acc);
+              acc = fmaf(z[i].w, x.w, acc);
+            }
+          }
+          d[u] = acc;
         }
-        d[u] = acc;
-      }
       }
       const float t = reduce_scatter<U>(d, lane);
       const int idx = lane / GP;
