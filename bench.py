@@ -31,6 +31,8 @@ if ROOT not in sys.path:
 
 import numpy as np  # noqa: E402
 
+from synth.graphs import CONFIGS  # noqa: E402
+
 METRIC = "SpMM fwd+bwd GB/s & GFLOP/s, quant-pack GB/s; % of GB300 HBM roofline"
 UNIT = "GB/s"
 
@@ -40,6 +42,7 @@ WORKLOAD_TEXT = {
     "reddit": "Reddit-shaped DC-SBM: 232,965 nodes, 57.3M undirected edges, heavy tail capped at 20k, 50 communities, F=602, 2-layer GCN hidden 128, P=8, top-10% 8 bits else 2",
     "products": "ogbn-products-shaped DC-SBM: 2,449,029 nodes, 30,929,570 undirected edges, 128 communities, F=100, 4-layer GCN hidden 256, P=8, width quartiles {1,2,4,8}",
     "scale": "R-MAT scale 24 (16.8M nodes, 128M edge draws), BFS-ordered into 16 blocks, F=256, 3-layer GCN hidden 256, P=16, top-5% 8 bits else base 1",
+    "rmat20": "R-MAT scale 20 (1.05M nodes, 8M edge draws), BFS-ordered into 16 blocks, F=256, 3-layer GCN hidden 256, P=16, top-5% 8 bits else base 1 (the scale workload's generator at 1/16 size, for counter captures)",
 }
 
 
@@ -59,16 +62,33 @@ def rowbytes(b, F):
 
 # --------------------------------------------------------------- byte models
 def kernel_bytes(n, nnz, nnz_cut, S, F, slot_bits, slot_cut, out_bytes_per_row):
-    """Algorithmic bytes of the aggregation calls and the quantiser at width F.
-    slot_cut[s] = cut entries of slot s (forward remote reads per slot)."""
+    """Gather-model bytes of the aggregation calls and the quantiser at width
+    F: every gathered row counted at every use.  slot_cut[s] = cut entries of
+    slot s (forward remote reads per slot).  bwd = halo + local."""
     rb = rowbytes(slot_bits, F)
     Q = int(rb.sum())
     remote = int((slot_cut * (rb + 8)).sum())
     fwd = 8 * (n + 1) + 8 * nnz + (nnz - nnz_cut) * 4 * F + remote + out_bytes_per_row * n
     qp = 4 * S + 4 * F * S + Q + 8 * S + 1 * S + 8 * S
-    bwd = (8 * (S + 1) + 8 * nnz_cut + nnz_cut * 4 * F + Q + 8 * S          # halo partials + pack
-           + 8 * (n + 1) + 8 * nnz + (nnz - nnz_cut) * 4 * F + Q + 8 * S + 4 * F * n)  # local + owned
-    return dict(fwd=fwd, quant=qp, bwd=bwd, Q=Q)
+    halo = 8 * (S + 1) + 8 * nnz_cut + nnz_cut * 4 * F + Q + 8 * S          # halo partials + pack
+    local = 8 * (n + 1) + 8 * nnz + (nnz - nnz_cut) * 4 * F + Q + 8 * S + 4 * F * n  # local + owned
+    return dict(fwd=fwd, quant=qp, bwd=halo + local, halo=halo, local=local, Q=Q)
+
+
+def compulsory_bytes(n, nnz, nnz_cut, S, F, Q, n_pool, n_halo_src, out_fwd, out_bwd):
+    """Each array a kernel touches counted once (the least any schedule of the
+    same algorithm moves between HBM and the chip): CSR metadata, every
+    distinct source row, the messages and their per-slot tables, the outputs.
+    n_pool = distinct message nodes (rows the quantiser reads); n_halo_src =
+    distinct rows the halo partials read; out_* = output bytes per row."""
+    tables = 17 * S  # slot width (1), offset (8), meta (8)
+    return dict(
+        quant=4 * S + 4 * F * n_pool + Q + tables,
+        fwd=8 * (n + 1) + 8 * nnz + 4 * n + 4 * F * n + Q + tables + out_fwd * n,
+        halo=8 * (S + 1) + 8 * nnz_cut + 4 * F * n_halo_src + Q + tables,
+        local=8 * (n + 1) + 8 * nnz + 4 * n + 4 * F * n + 8 * (n + 1) + 4 * S + Q + tables
+        + out_bwd * n,
+    )
 
 
 def gemm_bytes(n, F_in, F_out):
@@ -81,25 +101,50 @@ def gemm_bytes(n, F_in, F_out):
     return dict(fwd=fwd, mask=mask, dM=dM, dW=dW)
 
 
-def committed_traffic():
-    """DRAM bytes per launch of the layer-1 forward aggregation from the
-    committed ncu summary, or None when the kernel source has changed since
-    those counters were taken (the summary records a hash of the source)."""
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.md")
+TRAFFIC_SOURCES = ("spmm.cu", "quant.cu", "device.cuh")
+
+
+def traffic_source_hash():
+    """Hash of the aggregation and quantiser kernel sources: committed DRAM
+    counters count only while the kernels they were taken on are unchanged."""
     import hashlib
+
+    csrc = os.path.join(ROOT, "sparse_aggregation_message_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in TRAFFIC_SOURCES:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(workload, base_bits=None, path=TRAFFIC_FILE):
+    """DRAM bytes (read + write) per launch of each aggregation-path kernel on
+    this workload, from the committed ncu summary: lines of the form
+    ``traffic workload=W base=B kind=K bytes_per_launch=N source=H``.  Kernels
+    whose source hash differs from today's sources are left out."""
     import re
 
-    path = os.path.join(ROOT, "profiles", "kernels_yelp_fullset.md")
     if not os.path.exists(path):
-        return None
-    text = open(path).read()
-    m_b = re.search(r"^traffic_bytes_per_launch:\s*(\d+)", text, re.M)
-    m_h = re.search(r"^traffic_source_sha256_16:\s*([0-9a-f]+)", text, re.M)
-    if not (m_b and m_h):
-        return None
-    csrc = os.path.join(ROOT, "sparse_aggregation_message_gb300", "csrc")
-    h = hashlib.sha256(open(os.path.join(csrc, "spmm.cu"), "rb").read() +
-                       open(os.path.join(csrc, "device.cuh"), "rb").read()).hexdigest()[:16]
-    return int(m_b.group(1)) if h == m_h.group(1) else None
+        return {}
+    want_h = traffic_source_hash()
+    out = {}
+    with open(path) as f:
+        for ln in f:
+            m = re.match(r"^traffic workload=(\S+) base=(\d+) kind=(\S+) bytes_per_launch=(\d+) "
+                         r"source=([0-9a-f]+)\s*$", ln.strip())
+            if not m or m.group(1) != workload or m.group(5) != want_h:
+                continue
+            if base_bits is not None and int(m.group(2)) != int(base_bits):
+                continue
+            out[m.group(3)] = int(m.group(4))
+    return out
+
+
+def default_variant(args):
+    """The aggregate-first GCN path with the row kernels (the counters in the
+    committed summary were taken on it)."""
+    return args.order == "af" and args.aggregator == "gcn" and not args.blocked
 
 
 def max_over_ranks(value, world, device="cpu"):
@@ -251,7 +296,7 @@ def run_gpu(args, rank, world, local_rank):
     slot_cut = (bnd.slot_rowptr[1:] - bnd.slot_rowptr[:-1]).cpu().numpy()
     slot_bits = bnd.slot_bits.cpu().numpy()
 
-    kinds = ["quant", "spmm_fwd", "gemm_fwd", "mask_dM_dW", "spmm_bwd", "tf_fwd", "tf_bwd"]
+    kinds = ["quant", "spmm_fwd", "gemm_fwd", "mask_dM_dW", "halo", "spmm_bwd", "tf_fwd", "tf_bwd"]
     ev = {}
 
     def rec(key):
@@ -369,17 +414,22 @@ def run_gpu(args, rank, world, local_rank):
             if timed:
                 rec(("mask_dM_dW", l, 1))
             if l > 0:
+                # the backward messages (halo partials, quantised and packed)
+                # and the owner-side aggregation are timed apart
+                if bl is None:
+                    G.gnn_halo_quant_pack(bnd, dMl, F, 2 * l + 1, packed, meta, slot_off=so)
+                if timed:
+                    rec(("halo", l, 1))
                 if fused and bl is not None:
                     dZ_in = dZbuf[F]
                     G.gnn_spmm_bwd_blocked(csr, bnd, bl, dMl, F, 2 * l + 1, packed, meta, H_mask=Hs[l],
                                            dZ=dZ_in, slot_off=so, ws=blk_ws)
                 elif fused:
                     dZ_in = dZbuf[F]
-                    G.gnn_spmm_bwd_masked(csr, bnd, dMl, F, 2 * l + 1, packed, meta, Hs[l], dZ_in,
-                                          slot_off=so, ws=wss)
+                    G.gnn_spmm_bwd_local_masked(csr, bnd, dMl, F, packed, meta, Hs[l], dZ_in,
+                                                slot_off=so, ws=wss)
                 else:
-                    G.gnn_spmm_bwd(csr, bnd, dMl, F, 2 * l + 1, packed, meta, dHs[l], slot_off=so,
-                                   ws=wss)
+                    G.gnn_spmm_bwd_local(csr, bnd, dMl, F, packed, meta, dHs[l], slot_off=so, ws=wss)
                 if timed:
                     rec(("spmm_bwd", l, 1))
 
@@ -422,18 +472,23 @@ def run_gpu(args, rank, world, local_rank):
         if which != 1:
             continue
         start_key = {"quant": ("quant", l, 0), "spmm_fwd": ("quant", l, 1), "gemm_fwd": ("spmm_fwd", l, 1),
-                     "mask_dM_dW": ("mask_dM_dW", l, 0), "spmm_bwd": ("mask_dM_dW", l, 1),
+                     "mask_dM_dW": ("mask_dM_dW", l, 0), "halo": ("mask_dM_dW", l, 1),
+                     "spmm_bwd": ("halo", l, 1),
                      "tf_fwd": ("tf_fwd", l, 0), "tf_bwd": ("tf_bwd", l, 0)}[kind]
         starts = ev[start_key]
         tot = sum(a.elapsed_time(b) for a, b in zip(starts, lst)) / args.steps
         per[kind] += tot
         per_layer[f"{kind}_l{l + 1}"] = tot
 
-    # algorithmic bytes per step
+    # algorithmic bytes per step: the gather model (every gathered row at
+    # every use) and the compulsory bytes (every array once)
     nnz, nc = csr.nnz, bnd.nnz_cut
     byt = {k: 0 for k in kinds}
+    comp = {k: 0 for k in kinds}
+    launches_k = {k: 0 for k in kinds}
+    n_pool = int(torch.unique(bnd.slot_node).numel()) if S else 0
+    n_halo_src = int(torch.unique(bnd.slot_col).numel()) if nc else 0
     flops = {"spmm": 0.0, "gemm": 0.0}
-    spmm_fwd_bytes_l = {}
     for l in range(L):
         F, Fo = dims[l], dims[l + 1]
         gb = gemm_bytes(n, F, Fo)
@@ -456,29 +511,35 @@ def run_gpu(args, rank, world, local_rank):
         kb = kernel_bytes(n, nnz, nc, S, F, slot_bits, slot_cut, 2 * ldb[l])
         byt["quant"] += kb["quant"]
         byt["spmm_fwd"] += kb["fwd"]
-        spmm_fwd_bytes_l[l] = kb["fwd"]
         byt["gemm_fwd"] += gb["fwd"]
         byt["mask_dM_dW"] += gb["mask"] + gb["dW"] + (gb["dM"] if l > 0 else 0)
         flops["spmm"] += 2.0 * nnz * F
         flops["gemm"] += 2.0 * n * F * Fo * (3 if l > 0 else 2)
+        cb = compulsory_bytes(n, nnz, nc, S, F, kb["Q"], n_pool, n_halo_src, 2 * ldb[l],
+                              4 * F + 2 * G.ldz_for(F) if fused else 4 * F)
+        comp["quant"] += cb["quant"]
+        comp["spmm_fwd"] += cb["fwd"]
+        launches_k["quant"] += 1
+        launches_k["spmm_fwd"] += 1
         if l > 0:
             kb4 = kernel_bytes(n, nnz, nc, S, F, slot_bits, slot_cut, 4 * F)
             # fused: the store reads the gate row (4F) in place of writing fp32
             # dH (4F) and writes the bf16 gradient; the layer below skips its mask
-            byt["spmm_bwd"] += kb4["bwd"] + (2 * G.ldz_for(F) * n if fused else 0)
+            extra = 2 * G.ldz_for(F) * n if fused else 0
+            if bl is None:
+                byt["halo"] += kb4["halo"]
+                byt["spmm_bwd"] += kb4["local"] + extra
+                comp["halo"] += cb["halo"]
+                comp["spmm_bwd"] += cb["local"]
+                launches_k["halo"] += 1
+            else:
+                byt["spmm_bwd"] += kb4["bwd"] + extra
+                comp["spmm_bwd"] += cb["halo"] + cb["local"]
+            launches_k["spmm_bwd"] += 1
             flops["spmm"] += 2.0 * nnz * F
         if fused and l < L - 1:
             byt["mask_dM_dW"] -= gb["mask"]
     total_bytes = sum(byt.values())
-    # every array of an aggregate-first forward aggregation touched once: CSR
-    # metadata, each source row, the messages with their meta, bf16 output
-    compulsory = {}
-    for l in range(L):
-        if not tf[l]:
-            Fl = dims[l]
-            Ql = int(offs[Fl][-1].item())
-            compulsory[l] = (8 * (n + 1) + 8 * nnz + 4 * n + 4 * Fl * n + Ql + 17 * S
-                             + 2 * ldb[l] * n)
 
     # an asynchronous epoch (SYLVIE guide section 10) through the layer API:
     # each layer aggregates with the previous step's messages while this
@@ -594,65 +655,139 @@ def run_gpu(args, rank, world, local_rank):
         e2e = dict(ms=e2e_ms, h2d=h2d, d2h=d2h, issue_ms=1e3 * t_issue / args.e2e_steps,
                    pinned=bool(h_in.is_pinned() and g_in.is_pinned()))
 
-    return dict(ms=ms, per=per, per_layer=per_layer, byt=byt, flops=flops, total_bytes=total_bytes,
+    return dict(ms=ms, per=per, per_layer=per_layer, byt=byt, comp=comp, launches_k=launches_k,
+                flops=flops, total_bytes=total_bytes,
                 launches=launches, clocks=clk.summary(), e2e=e2e, asy=asy, S=S, nnz=nnz, nnz_cut=nc, n=n,
-                Q=int(offs[mwid[0]][-1].item()), spmm_fwd_bytes_l=spmm_fwd_bytes_l, n_long=csr.n_long,
-                n_pieces=csr.n_pieces, dims=dims, P=P, tf=tf, compulsory=compulsory)
+                Q=int(offs[mwid[0]][-1].item()), n_long=csr.n_long,
+                n_pieces=csr.n_pieces, dims=dims, P=P, tf=tf, n_pool=n_pool, n_halo_src=n_halo_src,
+                base=base)
 
 
 # --------------------------------------------------------------- oracle (CPU) arm
 class OracleBaseline:
-    """The oracle, as it stands, on bounded samples of the workload's rows:
-    forward aggregation (with quantisation of the remote rows it reads) and
-    backward aggregation (halo partials, quantisation, owner adds) at the
-    first layer width.  Rates use the same algorithmic byte model as the GPU
-    arm, scaled by the fraction of rows processed."""
+    """The oracle, as it stands, on bounded samples of the workload: its C
+    routines (one OpenMP loop over rows or slots, timed on every host core
+    and on one) run the first layer's forward messages, forward aggregation,
+    backward messages and backward aggregation over a block of slots and a
+    block of rows of one partition per sample.  The GCN/mean aggregations use
+    the same routines; for attention layers the GCN-weighted aggregation is
+    timed (the attention oracle is plain numpy and not sampled).  Rates use
+    the GPU arm's gather-model bytes per slot and per row."""
 
     def __init__(self, workload, aggregator="gcn"):
         import oracle as O
+        from oracle import coracle as C
         from synth import make_workload
 
-        self.O = O
+        self.C = C
         self.aggregator = aggregator
         wl = make_workload(workload)
         self.n = n = wl.n
         flags = O.FLAGS_GCN | (O.FLAG_MEAN if aggregator == "mean" else 0)
-        self.rp, self.col, self.val = O.csr_build(n, wl.src, wl.dst, flags)
-        vt = O.transpose_values(n, self.rp, self.col, self.val) if aggregator == "mean" else None
-        self.b = O.boundary_index(n, self.rp, self.col, self.val, wl.P, vt)
-        nb = O.node_bits(n, self.rp, self.b, wl.rule_pct, wl.rule_bits, wl.base_bits[0])
-        self.sb = nb[self.b["slot_node"]]
-        self.F = F = wl.dims[0]
-        rng = np.random.default_rng(wl.seed + 1)
-        self.H = rng.standard_normal((n, F)).astype(np.float32)
-        self.Gm = rng.standard_normal((n, F)).astype(np.float32)
-        slot_cut = np.diff(self.b["slot_rowptr"])
-        kb = kernel_bytes(n, len(self.col), self.b["nnz_cut"], self.b["n_slots"], F, self.sb, slot_cut, 4 * F)
-        self.per_row_bytes = (kb["fwd"] + kb["quant"] + kb["bwd"]) / n
-        self.order = rng.permutation(n)
-        self.pos = 0
+        self.rp, col, val = O.csr_build(n, wl.src, wl.dst, flags)
+        vt = O.transpose_values(n, self.rp, col, val) if aggregator == "mean" else None
+        self.b = b = O.boundary_index(n, self.rp, col, val, wl.P, vt)
+        del wl
+        nb = O.node_bits(n, self.rp, b, wl_rule(workload)[0], wl_rule(workload)[1],
+                         CONFIGS[workload]["base_bits"][0])
+        self.sb = nb[b["slot_node"]].astype(np.uint8)
+        self.F = F = CONFIGS[workload]["F"]
+        self.off = O.slot_offsets(self.sb, F)
+        self.S = S = b["n_slots"]
+        self.P = wl_P = CONFIGS[workload]["P"]
+        self.H = normal_f32(n, F, CONFIGS[workload]["index"] + 0x5EED0001)
+        self.Gm = normal_f32(n, F, CONFIGS[workload]["index"] + 0x5EED1001)
+        # the message buffers the aggregations read (set up once, untimed)
+        self.fp, self.fm = C.quant_pack(self.H, F, b["slot_node"], self.sb, self.off, 0)
+        self.hp, self.hm = C.halo_quant_pack(b, self.Gm, F, self.sb, self.off, 1)
+        # gather-model bytes of each row's two aggregations and each slot's two
+        # message rows (the GPU arm's byte model, split by row and by slot)
+        rb = rowbytes(self.sb, F).astype(np.int64)
+        slot_cut = np.diff(b["slot_rowptr"])
+        self.slot_bytes = (4 + 4 * F + rb + 17) + (8 + slot_cut * (8 + 4 * F) + rb + 8)
+        cr = b["col_remap"]
+        rem = cr < 0
+        ent = np.where(rem, 8 + np.concatenate([rb, [0]])[np.where(rem, ~cr, S)] + 8, 8 + 4 * F)
+        ent_local = np.where(rem, 8, 8 + 4 * F)
+        own = np.zeros(n, np.int64)
+        np.add.at(own, b["slot_node"], rb + 8)
+        rows_of = np.repeat(np.arange(n), np.diff(self.rp))
+        self.row_bytes = (np.bincount(rows_of, weights=ent + ent_local, minlength=n)
+                          + 16 + 8 * F + own)
+        del rows_of, ent, ent_local, rem
+        self.part = O.partition_starts(n, wl_P)
+        self.q = 0
+        self.rng = np.random.default_rng(CONFIGS[workload]["index"] + 0x5EED2001)
 
-    def sample(self, budget_s):
-        O, n = self.O, self.n
-        rows_done, t_used, chunk = 0, 0.0, 256
+    def _one(self, budget_s, threads):
+        """Samples until budget_s has passed: per sample one partition's block
+        of slots and block of rows.  Returns (GB/s, seconds, slots, rows)."""
+        C, b, F = self.C, self.b, self.F
+        C.set_threads(threads)
+        done_b, t_used, slots_done, rows_done = 0.0, 0.0, 0, 0
+        k_rows, k_slots = 2048, 4096
         t0 = time.perf_counter()
-        while t_used < budget_s and rows_done < n:
-            if self.pos >= n:
-                self.pos = 0
-            rows = np.sort(self.order[self.pos:self.pos + chunk])
-            self.pos += rows.size
-            O.spmm_fwd(n, self.rp, self.col, self.val, self.H, self.F, self.b, self.sb, seed=0, rows=rows)
-            O.spmm_bwd(n, self.rp, self.col, self.val, self.Gm, self.F, self.b, self.sb, seed=1, rows=rows)
+        while t_used < budget_s:
+            q = self.q % self.P
+            self.q += 1
+            # a seeded random block of the partition's rows (all degrees mixed)
+            p0, p1 = int(self.part[q]), int(self.part[q + 1])
+            rows = np.sort(self.rng.choice(p1 - p0, min(k_rows, p1 - p0), replace=False)) + p0
+            # a block of the partition's slots from a seeded random start
+            a0, a1 = int(b["send_start"][q]), int(b["send_start"][q + 1])
+            s0 = a0 + int(self.rng.integers(0, max(1, a1 - a0 - k_slots + 1)))
+            s1 = min(a1, s0 + k_slots)
+            if s1 > s0:
+                C.quant_pack(self.H, F, b["slot_node"][s0:s1], self.sb[s0:s1],
+                             self.off[s0:s1 + 1] - self.off[s0], 0, key0=s0)
+                C.halo_quant_pack(b, self.Gm, F, self.sb, self.off, 1, s0, s1)
+            C.spmm_fwd_rows(self.rp, b, self.H, F, self.fp, self.fm, self.sb, self.off, rows)
+            C.spmm_bwd_rows(self.rp, b, self.Gm, F, self.hp, self.hm, self.sb, self.off, rows)
+            slots_done += s1 - s0
             rows_done += rows.size
+            done_b += float(self.slot_bytes[s0:s1].sum()) + float(self.row_bytes[rows].sum())
             t_used = time.perf_counter() - t0
-            chunk = min(chunk * 2, 1 << 14)
-        gbs = self.per_row_bytes * rows_done / t_used / 1e9
+            k_rows, k_slots = min(k_rows * 2, 1 << 16), min(k_slots * 2, 1 << 17)
+        return done_b / t_used / 1e9, t_used, slots_done, rows_done
+
+    def sample(self, budget_s, single_thread_share=0.3):
+        """All host cores for (1 - share) of the budget, one core for the rest."""
+        C = self.C
+        cores = C.max_threads()
+        gbs, secs, ns, nr = self._one(budget_s * (1 - single_thread_share), cores)
+        gbs1, secs1, ns1, nr1 = self._one(budget_s * single_thread_share, 1)
+        C.set_threads(cores)
         what = ("GCN-weighted aggregation; the attention oracle is not sampled"
-                if self.aggregator == "gat" else "forward + backward aggregation with quantised "
-                                                 "boundary rows")
-        return dict(value=gbs, unit=UNIT, cores=1, kind="oracle",  # numpy/scipy run on one thread here
-                    sample=f"{rows_done} of {n} rows ({what}, F={self.F}), {t_used:.1f} s",
-                    seconds=t_used, rows=rows_done)
+                if self.aggregator == "gat" else "forward and backward messages and aggregations")
+        return dict(value=gbs, unit=UNIT, cores=cores, kind="oracle",
+                    sample=f"{ns} of {self.S} slots and {nr} of {self.n} rows ({what}, F={self.F}), "
+                           f"{secs:.1f} s on {cores} threads (the oracle's C routines, OpenMP)",
+                    single_thread={"value": gbs1, "unit": UNIT, "cores": 1, "seconds": secs1,
+                                   "sample": f"{ns1} slots and {nr1} rows"},
+                    seconds=secs)
+
+
+def normal_f32(n, F, seed, chunk=1 << 18):
+    """fp32 N(0,1) [n, F], drawn in row chunks by independent seeded streams
+    on several threads (numpy releases the GIL while it fills)."""
+    import concurrent.futures as cf
+
+    out = np.empty((n, F), np.float32)
+    starts = list(range(0, n, chunk))
+    seqs = np.random.SeedSequence(seed).spawn(len(starts))
+
+    def fill(i):
+        r0 = starts[i]
+        np.random.default_rng(seqs[i]).standard_normal(out=out[r0:r0 + chunk], dtype=np.float32)
+
+    with cf.ThreadPoolExecutor(max_workers=os.cpu_count() or 1) as ex:
+        list(ex.map(fill, range(len(starts))))
+    return out
+
+
+def wl_rule(workload):
+    r = CONFIGS[workload]["rule"]
+    return r["pct"], r["bits"]
 
 
 def main():
@@ -660,7 +795,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="yelp", choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--workload", default="scale", choices=sorted(WORKLOAD_TEXT))
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--order", default="af", choices=["af", "tf", "auto"],
                     help="aggregate first (the message is H), transform first where F_out < F_in "
@@ -695,7 +830,7 @@ def main():
 
     config = {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload,
               "aggregator": args.aggregator, "order": args.order, "blocked": args.blocked or None,
-              "base_bits": args.base_bits or None,
+              "base_bits": args.base_bits or CONFIGS[args.workload]["base_bits"][0],
               "timing": "inputs larger than L2 (no flush); CUDA events on the launching stream",
               "parallelism": f"replicas x{world}"}
 
@@ -716,7 +851,7 @@ def main():
                     "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                     "config": config,
                     "cpu_baseline": {"value": val, "unit": UNIT, "cores": cb["cores"], "kind": "oracle",
-                                     "sample": cb["sample"]},
+                                     "sample": cb["sample"], "single_thread": cb["single_thread"]},
                     "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
             print(json.dumps(line), flush=True)
         if world > 1:
@@ -733,40 +868,73 @@ def main():
     def rate(k):
         return r["byt"][k] / (per[k] * 1e-3) / 1e9 if per[k] > 0 else None
 
-    spmm_ms = per["spmm_fwd"] + per["spmm_bwd"]
+    spmm_ms = per["spmm_fwd"] + per["halo"] + per["spmm_bwd"]
     gemm_ms = per["gemm_fwd"] + per["mask_dM_dW"]
-    # dominant kernel: the forward aggregation of the first aggregate-first layer
-    L0 = next((l for l, t in enumerate(r["tf"]) if not t), None)
-    t_dom = r["per_layer"].get(f"spmm_fwd_l{L0 + 1}") if L0 is not None else None
-    dom_bytes = r["spmm_fwd_bytes_l"].get(L0) if L0 is not None else None
-    achieved = dom_bytes / (t_dom * 1e-3) / 1e9 if t_dom else None
-    default_path = (args.workload == "yelp" and args.order == "af" and args.aggregator == "gcn"
-                    and not args.base_bits and not args.blocked)
-    traffic = committed_traffic() if default_path else None
+    names = {"quant": "quant_pack_kernel (gnn_quant_pack: forward messages)",
+             "spmm_fwd": "spmm_rows_kernel (gnn_spmm_fwd: aggregation with in-gather dequantisation)",
+             "halo": "halo_quant_pack_kernel (gnn_halo_quant_pack: backward halo partials, "
+                     "quantised and packed)",
+             "spmm_bwd": "spmm_rows_kernel (gnn_spmm_bwd_local_masked: local transpose aggregation, "
+                         "owned messages, ReLU gate)"}
+    agg = [k for k in names if r["launches_k"][k] > 0 and per[k] > 0]
+    traffic_tab = (committed_traffic(args.workload, r["base"]) if default_variant(args) else {})
+
+    def kstats(k):
+        t = per[k] * 1e-3  # s per step
+        nl = r["launches_k"][k]
+        d = {"ms_per_step": per[k], "launches_per_step": nl,
+             "gather_model_GBs": r["byt"][k] / t / 1e9,
+             "compulsory_GBs": r["comp"][k] / t / 1e9,
+             "compulsory_frac_of_hbm": r["comp"][k] / t / 1e9 / hbm}
+        tr = traffic_tab.get(k)
+        if tr is not None:
+            d["dram_GBs"] = tr * nl / t / 1e9
+            d["dram_frac_of_hbm"] = d["dram_GBs"] / hbm
+        return d
+
+    kstat = {k: kstats(k) for k in agg}
+    # dominant kernel: the aggregation-path kernel with the most time per step
+    dom = max(agg, key=lambda k: per[k]) if agg else None
+    roof = None
+    if dom is not None:
+        st = kstat[dom]
+        nl = r["launches_k"][dom]
+        t_launch = per[dom] / nl * 1e-3
+        traffic = traffic_tab.get(dom)
+        comp_launch = r["comp"][dom] / nl
+        if traffic is not None:
+            achieved, basis = traffic / t_launch / 1e9, "dram bytes (ncu, same kernel source and workload)"
+        else:
+            achieved, basis = comp_launch / t_launch / 1e9, "compulsory bytes (every array once)"
+        roof = {"kernel": names[dom], "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "traffic": traffic, "basis": basis,
+                "launch_ms": t_launch * 1e3, "launches_per_step": nl,
+                "compulsory": {"bytes_per_launch": comp_launch, "GBs": comp_launch / t_launch / 1e9,
+                               "frac": comp_launch / t_launch / 1e9 / hbm},
+                "gather_model": {"bytes_per_launch": r["byt"][dom] / nl, "GBs": st["gather_model_GBs"],
+                                 "note": "every gathered row counted at every use; L2 serves the "
+                                         "repeats, so this is not an HBM figure"},
+                "peak_source": peak_src + " (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+                else peak_src}
     line = {
         "metric": METRIC, "value": gbs, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "fp32 aggregation, bf16 transform, 1-8 bit messages",
         "data": "synthetic (seeded generator; no dataset)",
         "config": config,
+        "value_basis": "gather-model bytes of every kernel of the step / step time",
         "kernels": {
-            "spmm_fwd_GBs": rate("spmm_fwd"), "spmm_bwd_GBs": rate("spmm_bwd"),
-            "quant_pack_GBs": rate("quant"),
             "spmm_GFLOPs": r["flops"]["spmm"] / (spmm_ms * 1e-3) / 1e9 if spmm_ms else None,
             "gemm_TFLOPs": r["flops"]["gemm"] / (gemm_ms * 1e-3) / 1e12 if gemm_ms else None,
             "ms": per, "ms_per_layer": r["per_layer"], "transform_first_layers": r["tf"],
-            "hbm_frac": {k: (rate(k) / hbm if rate(k) else None) for k in ["spmm_fwd", "spmm_bwd", "quant"]},
+            **kstat,
         },
         "graph": {"n": r["n"], "nnz": r["nnz"], "nnz_cut": r["nnz_cut"], "slots": r["S"],
                   "packed_bytes_layer1": r["Q"], "meta_bytes_layer1": 8 * r["S"],
+                  "message_nodes": r["n_pool"], "halo_source_rows": r["n_halo_src"],
                   "long_rows": r["n_long"], "pieces": r["n_pieces"],
                   "dims": r["dims"], "P": r["P"]},
-        "roofline": {"kernel": f"gnn_spmm_fwd, layer {(L0 or 0) + 1} (aggregation with in-gather "
-                               "dequantisation)",
-                     "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": (achieved / hbm) if achieved else None, "traffic": traffic,
-                     "compulsory_bytes": r["compulsory"].get(L0) if L0 is not None else None,
-                     "peak_source": peak_src},
+        "roofline": roof,
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
     }
@@ -785,7 +953,8 @@ def main():
                                        "step's are packed on a second stream meanwhile"}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cb = OracleBaseline(args.workload, args.aggregator).sample(args.cpu_budget)
-        line["cpu_baseline"] = {k: cb[k] for k in ["value", "unit", "cores", "kind", "sample"]}
+        line["cpu_baseline"] = {k: cb[k] for k in ["value", "unit", "cores", "kind", "sample",
+                                                    "single_thread"]}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -396,6 +396,21 @@ gnn_status gnn_spmm_bwd_masked(const gnn_csr* csr, const gnn_boundary* bnd, cons
                                float* meta_ws, const float* H_mask, int64_t ldhm, uint16_t* dZ,
                                int64_t ldz, void* ws, size_t ws_bytes, gnn_stream_t stream);
 
+/* The owner-side half of gnn_spmm_bwd_masked, for callers that form the
+ * backward messages themselves (gnn_halo_quant_pack) or time the two halves
+ * apart: dZ = bf16((local A^T G + the dequantised messages in packed/meta of
+ * the slots each row owns) * 1[H_mask > 0]), as gnn_spmm_bwd_local sums them
+ * (SYLVIE guide, section 3: backward gradients return along the forward
+ * dependencies; section 11: dequantise, then aggregate).  Layout, workspace
+ * and checks as gnn_spmm_bwd_masked; gnn_spmm_bwd_masked(G) equals
+ * gnn_halo_quant_pack(G) followed by this call with the same buffers. */
+gnn_status gnn_spmm_bwd_local_masked(const gnn_csr* csr, const gnn_boundary* bnd,
+                                     const float* G, int64_t ldg, int32_t F,
+                                     const uint8_t* packed, const float* meta,
+                                     const float* H_mask, int64_t ldhm, uint16_t* dZ,
+                                     int64_t ldz, void* ws, size_t ws_bytes,
+                                     gnn_stream_t stream);
+
 /* gnn_dense_bwd from a given bf16 dZ (as gnn_spmm_bwd_masked writes it; row
  * stride ldz >= round_up(F_out, 64), columns F_out..ldz-1 zero):
  * dM = dZ W^T and dW = Mb^T dZ.  Either output may be NULL. */

@@ -7,7 +7,7 @@
  * host core.  It is called only by the test suite and by the benchmark's CPU
  * baseline, never by the GPU library, and shares no code with it.
  *
- * Build: gcc -O2 -ffp-contract=off -fopenmp -shared -fPIC (oracle/cbuild.py).
+ * Build: gcc -O2 -ffp-contract=off -fopenmp -shared -fPIC (oracle/coracle.py).
  * -ffp-contract=off keeps every fp32 multiply and add separately rounded, as
  * the definitions below state; fp32 arithmetic is IEEE round-to-nearest.  The
  * only parallelism is one OpenMP loop over independent rows or slots; each
@@ -118,14 +118,16 @@ static void quant_pack_row(const float* x, int F, int b, uint32_t key, uint32_t 
 }
 
 /* Rows X[row_idx[r]] (row_idx NULL: X[r]) for r < n_rows, width bits[r], row
- * key r, packed at packed + off[r]; meta[2r], meta[2r+1] = (min, scale). */
+ * key key0 + r, packed at packed + off[r]; meta[2r], meta[2r+1] = (min,
+ * scale).  key0 lets a long list of slots be processed in pieces. */
 void orc_quant_pack(const float* X, int64_t ldx, int F, const int32_t* row_idx, int64_t n_rows,
-                    const uint8_t* bits, const int64_t* off, uint32_t seed, uint8_t* packed,
-                    float* meta) {
+                    const uint8_t* bits, const int64_t* off, uint32_t seed, int64_t key0,
+                    uint8_t* packed, float* meta) {
 #pragma omp parallel for schedule(dynamic, 1024)
   for (int64_t r = 0; r < n_rows; ++r) {
     const int64_t src = row_idx ? (int64_t)row_idx[r] : r;
-    quant_pack_row(X + src * ldx, F, bits[r], (uint32_t)r, seed, packed + off[r], meta + 2 * r);
+    quant_pack_row(X + src * ldx, F, bits[r], (uint32_t)(key0 + r), seed, packed + off[r],
+                   meta + 2 * r);
   }
 }
 
@@ -148,14 +150,16 @@ static float dequant(const uint8_t* row, int b, float mn, float scale, int j) {
 /* Backward messages (section 3): for every slot s, the halo copy's partial
  * gradient P_s[j] = sum over the slot's entries e (ascending v) of
  * sval[e] * G[scol[e]][j] in fp32 -- start at +0, each product rounded, then
- * each sum rounded -- quantised with row key s and packed at off[s]. */
+ * each sum rounded -- quantised with row key key0 + s and packed at off[s]
+ * (srp, bits, off and meta may start at slot key0 of a longer list). */
 void orc_halo_quant_pack(int64_t S, const int64_t* srp, const int32_t* scol, const float* sval,
                          const float* G, int64_t ldg, int F, const uint8_t* bits,
-                         const int64_t* off, uint32_t seed, uint8_t* packed, float* meta) {
+                         const int64_t* off, uint32_t seed, int64_t key0, uint8_t* packed,
+                         float* meta) {
 #pragma omp parallel
   {
     float* acc = (float*)malloc((size_t)F * sizeof(float));
-#pragma omp for schedule(dynamic, 256)
+#pragma omp for schedule(dynamic, 16)
     for (int64_t s = 0; s < S; ++s) {
       for (int j = 0; j < F; ++j) acc[j] = 0.0f;
       for (int64_t e = srp[s]; e < srp[s + 1]; ++e) {
@@ -166,7 +170,7 @@ void orc_halo_quant_pack(int64_t S, const int64_t* srp, const int32_t* scol, con
           acc[j] = acc[j] + p;
         }
       }
-      quant_pack_row(acc, F, bits[s], (uint32_t)s, seed, packed + off[s], meta + 2 * s);
+      quant_pack_row(acc, F, bits[s], (uint32_t)(key0 + s), seed, packed + off[s], meta + 2 * s);
     }
     free(acc);
   }
@@ -181,7 +185,7 @@ void orc_spmm_fwd_rows(const int64_t* rowptr, const int32_t* col_remap, const fl
                        const float* H, int64_t ldh, int F, const uint8_t* packed,
                        const float* meta, const uint8_t* slot_bits, const int64_t* slot_off,
                        const int64_t* rows, int64_t n_rows, double* M, double* T) {
-#pragma omp parallel for schedule(dynamic, 64)
+#pragma omp parallel for schedule(dynamic, 4)
   for (int64_t i = 0; i < n_rows; ++i) {
     const int64_t v = rows[i];
     double* m = M + i * F;
@@ -221,7 +225,7 @@ void orc_spmm_bwd_rows(const int64_t* rowptr, const int32_t* col_remap, const fl
                        const int32_t* own_slot, const uint8_t* packed, const float* meta,
                        const uint8_t* slot_bits, const int64_t* slot_off, const int64_t* rows,
                        int64_t n_rows, double* dH, double* T) {
-#pragma omp parallel for schedule(dynamic, 64)
+#pragma omp parallel for schedule(dynamic, 4)
   for (int64_t i = 0; i < n_rows; ++i) {
     const int64_t u = rows[i];
     double* d = dH + i * F;

@@ -53,8 +53,8 @@ def lib():
         L.orc_hash32.argtypes = [u32, u32, u32]
         L.orc_rowbytes.restype = i64
         L.orc_rowbytes.argtypes = [i32, i32]
-        L.orc_quant_pack.argtypes = [vp, i64, i32, vp, i64, vp, vp, u32, vp, vp]
-        L.orc_halo_quant_pack.argtypes = [i64, vp, vp, vp, vp, i64, i32, vp, vp, u32, vp, vp]
+        L.orc_quant_pack.argtypes = [vp, i64, i32, vp, i64, vp, vp, u32, i64, vp, vp]
+        L.orc_halo_quant_pack.argtypes = [i64, vp, vp, vp, vp, i64, i32, vp, vp, u32, i64, vp, vp]
         L.orc_spmm_fwd_rows.argtypes = [vp, vp, vp, vp, i64, i32, vp, vp, vp, vp, vp, i64, vp, vp]
         L.orc_spmm_bwd_rows.argtypes = [vp, vp, vp, vp, i64, i32, vp, vp, vp, vp, vp, vp, vp, i64,
                                         vp, vp]
@@ -84,40 +84,46 @@ def hash32(seed: int, s: int, j: int) -> int:
     return int(lib().orc_hash32(seed & 0xFFFFFFFF, s & 0xFFFFFFFF, j & 0xFFFFFFFF))
 
 
-def quant_pack(X, F, row_idx, bits, off, seed, total=None):
+def quant_pack(X, F, row_idx, bits, off, seed, total=None, key0=0):
     """Rows X[row_idx[r], :F] (row_idx None: X[r]) quantised with width
-    bits[r] and row key r, packed at off[r].  Returns (packed uint8 buffer,
-    meta fp32 [R, 2] = (min, scale))."""
+    bits[r] and row key key0 + r, packed at off[r] (off[R], when given, is
+    the buffer size).  Returns (packed uint8 buffer, meta fp32 [R, 2] =
+    (min, scale))."""
     X, px = _c(X, np.float32)
     bits, pb = _c(bits, np.uint8)
     off, po = _c(off, np.int64)
     R = bits.size
     if total is None:
-        total = int(off[R]) if off.size > R else int(max((off[r] + int(lib().orc_rowbytes(int(bits[r]), F))
-                                                            for r in range(R)), default=0))
+        if off.size > R:
+            total = int(off[R])
+        else:
+            total = max((int(off[r]) + int(lib().orc_rowbytes(int(bits[r]), F)) for r in range(R)),
+                        default=0)
     packed = np.zeros(max(total, 1), np.uint8)
     meta = np.zeros((R, 2), np.float32)
     ri, pr = (None, None) if row_idx is None else _c(row_idx, np.int32)
-    lib().orc_quant_pack(px, X.shape[1], F, pr, R, pb, po, seed & 0xFFFFFFFF, packed.ctypes.data,
-                         meta.ctypes.data)
+    lib().orc_quant_pack(px, X.shape[1], F, pr, R, pb, po, seed & 0xFFFFFFFF, int(key0),
+                         packed.ctypes.data, meta.ctypes.data)
     return packed[:total], meta
 
 
-def halo_quant_pack(bnd, G, F, slot_bits, slot_off, seed):
-    """Backward messages of every slot: the fixed-order fp32 halo partial of
-    G, quantised with key s and packed at slot_off[s]."""
+def halo_quant_pack(bnd, G, F, slot_bits, slot_off, seed, s0=0, s1=None):
+    """Backward messages of slots [s0, s1) (default all): the fixed-order fp32
+    halo partial of G, quantised with key s and packed at
+    slot_off[s] - slot_off[s0]."""
     S = int(bnd["n_slots"])
+    s1 = S if s1 is None else s1
     G, pg = _c(G, np.float32)
-    srp, p1 = _c(bnd["slot_rowptr"], np.int64)
+    srp, p1 = _c(bnd["slot_rowptr"][s0:s1 + 1], np.int64)
     scol, p2 = _c(bnd["slot_col"], np.int32)
     sval, p3 = _c(bnd["slot_val"], np.float32)
-    bits, pb = _c(slot_bits, np.uint8)
-    off, po = _c(slot_off, np.int64)
-    total = int(off[S])
+    bits, pb = _c(slot_bits[s0:s1], np.uint8)
+    off, po = _c(np.asarray(slot_off[s0:s1 + 1], np.int64) - int(slot_off[s0]), np.int64)
+    total = int(off[-1])
     packed = np.zeros(max(total, 1), np.uint8)
-    meta = np.zeros((S, 2), np.float32)
-    lib().orc_halo_quant_pack(S, p1, p2, p3, pg, G.shape[1], F, pb, po, seed & 0xFFFFFFFF,
-                              packed.ctypes.data, meta.ctypes.data)
+    meta = np.zeros((s1 - s0, 2), np.float32)
+    lib().orc_halo_quant_pack(s1 - s0, p1, p2, p3, pg, G.shape[1], F, pb, po, seed & 0xFFFFFFFF,
+                              int(s0), packed.ctypes.data, meta.ctypes.data)
     return packed[:total], meta
 
 

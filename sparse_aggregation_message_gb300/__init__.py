@@ -26,7 +26,7 @@ __all__ = [
     "LdrState", "gnn_ldr_init", "gnn_ldr_update", "gnn_quant_divide",
     "gnn_layer_tf_workspace", "gnn_layer_fwd_tf", "gnn_layer_bwd_tf",
     "gnn_gat_index", "gnn_gat_workspace", "gnn_gat_layer_fwd", "gnn_gat_layer_bwd",
-    "gnn_spmm_bwd_masked", "gnn_dense_bwd_z", "ldz_for",
+    "gnn_spmm_bwd_masked", "gnn_spmm_bwd_local_masked", "gnn_dense_bwd_z", "ldz_for",
     "Blocked", "gnn_blocked_build", "gnn_spmm_fwd_blocked", "gnn_spmm_bwd_blocked",
 ]
 
@@ -379,6 +379,18 @@ def gnn_spmm_bwd_masked(csr: Csr, bnd: Optional[Boundary], G, F: int, seed: int,
          _ptr(G), G.stride(0), F, seed & 0xFFFFFFFF, _ptr(packed_ws), _ptr(meta_ws), _ptr(H_mask),
          H_mask.stride(0) if H_mask is not None else 0, _ptr(dZ), dZ.stride(0), wp, wn,
          _stream(stream))
+
+
+def gnn_spmm_bwd_local_masked(csr: Csr, bnd: Boundary, G, F: int, packed, meta, H_mask, dZ,
+                              slot_off=None, ws=None, stream=None) -> None:
+    """The owner-side half of gnn_spmm_bwd_masked: dZ = bf16((local A^T G +
+    the dequantised messages in packed/meta) * 1[H_mask > 0])."""
+    c = csr.c()
+    cb = bnd.c(slot_off, F if slot_off is not None else None)
+    wp, wn = _ws_args(csr, F, ws, G.device)
+    call("gnn_spmm_bwd_local_masked", ctypes.byref(c), ctypes.byref(cb), _ptr(G), G.stride(0), F,
+         _ptr(packed), _ptr(meta), _ptr(H_mask), H_mask.stride(0) if H_mask is not None else 0,
+         _ptr(dZ), dZ.stride(0), wp, wn, _stream(stream))
 
 
 def gnn_kernel_launches() -> int:

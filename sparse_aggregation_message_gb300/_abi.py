@@ -126,6 +126,8 @@ PROTOTYPES = {
                                          c_vp, c_size, c_vp]),
     "gnn_spmm_bwd_masked": (ctypes.c_int, [P_csr, P_bnd, c_vp, c_i64, c_i32, c_u32, c_vp, c_vp, c_vp, c_i64,
                                            c_vp, c_i64, c_vp, c_size, c_vp]),
+    "gnn_spmm_bwd_local_masked": (ctypes.c_int, [P_csr, P_bnd, c_vp, c_i64, c_i32, c_vp, c_vp, c_vp,
+                                                 c_i64, c_vp, c_i64, c_vp, c_size, c_vp]),
     "gnn_dense_bwd_z": (ctypes.c_int, [c_vp, c_i64, c_i64, c_i32, c_vp, c_i32, c_vp, c_i64, c_vp, c_i64, c_vp,
                                        c_vp, c_size, c_vp]),
     "gnn_blocked_workspace": (ctypes.c_int, [P_csr, P_bnd, c_i32, c_i32, P_size]),

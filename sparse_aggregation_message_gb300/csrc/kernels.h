@@ -67,6 +67,13 @@ gnn_status launch_spmm_bwd_masked(const gnn_csr& csr, const gnn_boundary* bnd, c
                                   float2* meta_ws, const float* hmask, int64_t ldhm, uint16_t* dZ,
                                   int64_t ldz, float* partial, cudaStream_t st);
 
+// The owner-side half of launch_spmm_bwd_masked: local A^T entries plus the
+// owned messages in packed/meta, gated and stored as bf16.
+gnn_status launch_spmm_bwd_local_masked(const gnn_csr& csr, const gnn_boundary& bnd,
+                                        const float* Gm, int64_t ldg, int F, const uint8_t* packed,
+                                        const float2* meta, const float* hmask, int64_t ldhm,
+                                        uint16_t* dZ, int64_t ldz, float* partial, cudaStream_t st);
+
 size_t spmm_workspace_bytes(const gnn_csr& csr, int F);
 
 // gnn_spmm_fwd with its argument checks, the output ReLU'd when relu != 0.

@@ -628,10 +628,21 @@ gnn_status launch_spmm_bwd_masked(const gnn_csr& csr, const gnn_boundary* bnd, c
   }
   gnn_status s = launch_halo_quant_pack(*bnd, Gm, ldg, F, seed, packed_ws, meta_ws, st);
   if (s != GNN_OK) return s;
-  SlotMsgs msg{packed_ws, meta_ws, bnd->slot_off, bnd->slot_bits};
-  const float* wt = bnd->val_remap_t ? bnd->val_remap_t : bnd->val_remap;
-  return dispatch_rows<kBwdOwned>(csr, bnd->col_remap, wt, bnd->local_cnt, Gm, ldg, F, msg,
-                                  bnd->own_ptr, bnd->own_slot, partial, nullptr, 0, zb, ldz, st, 0,
+  return launch_spmm_bwd_local_masked(csr, *bnd, Gm, ldg, F, packed_ws, meta_ws, hmask, ldhm, dZ,
+                                      ldz, partial, st);
+}
+
+gnn_status launch_spmm_bwd_local_masked(const gnn_csr& csr, const gnn_boundary& bnd,
+                                        const float* Gm, int64_t ldg, int F, const uint8_t* packed,
+                                        const float2* meta, const float* hmask, int64_t ldhm,
+                                        uint16_t* dZ, int64_t ldz, float* partial,
+                                        cudaStream_t st) {
+  if (csr.n == 0) return GNN_OK;
+  auto* zb = reinterpret_cast<__nv_bfloat16*>(dZ);
+  SlotMsgs msg{packed, meta, bnd.slot_off, bnd.slot_bits};
+  const float* wt = bnd.val_remap_t ? bnd.val_remap_t : bnd.val_remap;
+  return dispatch_rows<kBwdOwned>(csr, bnd.col_remap, wt, bnd.local_cnt, Gm, ldg, F, msg,
+                                  bnd.own_ptr, bnd.own_slot, partial, nullptr, 0, zb, ldz, st, 0,
                                   hmask, ldhm, (int)ldz);
 }
 
@@ -893,6 +904,39 @@ extern "C" gnn_status gnn_spmm_bwd_masked(const gnn_csr* csr, const gnn_boundary
   return launch_spmm_bwd_masked(*csr, bnd, G, ldg, F, seed, packed_ws,
                                 reinterpret_cast<float2*>(meta_ws), H_mask, ldhm, dZ, ldz,
                                 static_cast<float*>(ws), as_stream(stream));
+}
+
+extern "C" gnn_status gnn_spmm_bwd_local_masked(const gnn_csr* csr, const gnn_boundary* bnd,
+                                                const float* G, int64_t ldg, int32_t F,
+                                                const uint8_t* packed, const float* meta,
+                                                const float* H_mask, int64_t ldhm, uint16_t* dZ,
+                                                int64_t ldz, void* ws, size_t ws_bytes,
+                                                gnn_stream_t stream) {
+  gnn_status st = check_csr(csr, "gnn_spmm_bwd_local_masked");
+  if (st != GNN_OK) return st;
+  GNN_REQUIRE(bnd, "gnn_spmm_bwd_local_masked: boundary is NULL (use gnn_spmm_bwd_masked)");
+  GNN_REQUIRE(F >= 1, "gnn_spmm_bwd_local_masked: F must be >= 1");
+  if (F > kMaxF) return fail(GNN_ERR_UNSUPPORTED, "gnn_spmm_bwd_local_masked: F=%d > %d", F, kMaxF);
+  if (!csr->symmetric && !csr->val_t)
+    return fail(GNN_ERR_UNSUPPORTED,
+                "gnn_spmm_bwd_local_masked: needs A^T (a symmetric CSR or val_t)");
+  if ((st = check_bnd(csr, bnd, F, true, "gnn_spmm_bwd_local_masked")) != GNN_OK) return st;
+  if ((st = check_ws(csr, F, ws, ws_bytes, "gnn_spmm_bwd_local_masked")) != GNN_OK) return st;
+  if (csr->n == 0) return GNN_OK;
+  GNN_REQUIRE(G && dZ, "gnn_spmm_bwd_local_masked: NULL G or dZ");
+  GNN_REQUIRE(ldg >= F && ldg % 4 == 0 && ((uintptr_t)G & 15) == 0,
+              "gnn_spmm_bwd_local_masked: ldg must be >= F, a multiple of 4, G 16-byte aligned");
+  GNN_REQUIRE(ldz >= (F + 63) / 64 * 64 && ldz % 8 == 0 && ((uintptr_t)dZ & 15) == 0,
+              "gnn_spmm_bwd_local_masked: ldz must be >= round_up(F, 64), a multiple of 8, dZ "
+              "16-byte aligned");
+  GNN_REQUIRE(!H_mask || (ldhm >= F && ldhm % 4 == 0 && ((uintptr_t)H_mask & 15) == 0),
+              "gnn_spmm_bwd_local_masked: ldhm must be >= F, a multiple of 4, H_mask 16-byte "
+              "aligned");
+  GNN_REQUIRE(bnd->n_slots == 0 || (packed && meta && ((uintptr_t)packed & 15) == 0),
+              "gnn_spmm_bwd_local_masked: packed (16-byte aligned) and meta required");
+  return launch_spmm_bwd_local_masked(*csr, *bnd, G, ldg, F, packed,
+                                      reinterpret_cast<const float2*>(meta), H_mask, ldhm, dZ, ldz,
+                                      static_cast<float*>(ws), as_stream(stream));
 }
 
 // ---------------------------------------------------------------- no-allocation forward

@@ -50,6 +50,13 @@ CONFIGS = {
         abcd=(0.57, 0.19, 0.19, 0.05), communities=16, F=256, hidden=256,
         layers=3, P=16, rule=dict(pct=[95], bits=[1, 8]), base_bits=[1, 2, 4, 8],
     ),
+    # the scale workload's generator at 1/16 of its size (same edge factor),
+    # small enough for hardware-counter captures
+    "rmat20": dict(
+        index=5, kind="rmat", scale=20, draws=8 << 20,
+        abcd=(0.57, 0.19, 0.19, 0.05), communities=16, F=256, hidden=256,
+        layers=3, P=16, rule=dict(pct=[95], bits=[1, 8]), base_bits=[1, 2, 4, 8],
+    ),
 }
 
 

@@ -175,3 +175,33 @@ def test_thread_count_does_not_change_results():
     finally:
         C.set_threads(t0)
     assert np.array_equal(a[0], z[0]) and np.array_equal(a[1], z[1])
+
+
+def test_quant_pack_in_pieces_equals_whole():
+    """Rows processed in pieces with key0 = first row give the same buffer."""
+    rng = np.random.default_rng(3)
+    R, F = 100, 40
+    X = rng.standard_normal((R, F)).astype(np.float32)
+    bits = rng.choice([1, 2, 4, 8], R).astype(np.uint8)
+    off = O.slot_offsets(bits, F)
+    whole_p, whole_m = C.quant_pack(X, F, None, bits, off, 11)
+    for a, b in [(0, 37), (37, 64), (64, 100)]:
+        p, m = C.quant_pack(X[a:b], F, None, bits[a:b], off[a:b + 1] - off[a], 11, key0=a)
+        assert np.array_equal(p, whole_p[off[a]:off[b]])
+        assert np.array_equal(m, whole_m[a:b])
+
+
+def test_halo_in_pieces_equals_whole():
+    n, s, d = _graph("planted")
+    F, P = 24, 4
+    rp, col, val = O.csr_build(n, s, d)
+    b = O.boundary_index(n, rp, col, val, P)
+    sb = np.random.default_rng(5).choice([1, 2, 4, 8], b["n_slots"]).astype(np.uint8)
+    off = O.slot_offsets(sb, F)
+    G = np.random.default_rng(6).standard_normal((n, F)).astype(np.float32)
+    wp, wm = C.halo_quant_pack(b, G, F, sb, off, 2)
+    S = b["n_slots"]
+    cut = [0, S // 3, S // 2, S]
+    for a, z in zip(cut[:-1], cut[1:]):
+        p, m = C.halo_quant_pack(b, G, F, sb, off, 2, a, z)
+        assert np.array_equal(p, wp[off[a]:off[z]]) and np.array_equal(m, wm[a:z])

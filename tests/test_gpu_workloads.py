@@ -1,19 +1,26 @@
 """The five synthetic workloads at full size, in the launch configuration
 bench.py times (row-split plan of 128 entries, long-slot list of 128
-entries, slot offsets per layer width).
+entries, slot offsets per layer width, the backward as halo messages then the
+gated owner-side aggregation).
 
-Per workload: CSR, boundary index, widths and offsets bit-exact against the
-oracle in full; quantised messages (forward and backward) bit-exact on a
-seeded sample of slots; forward and backward aggregation on a seeded sample of
-rows plus the longest (split) rows, within |d| <= 1e-5*sum|terms| + 1e-7; the
-first layer's transform on the sampled rows against fp64 products of the same
-bf16 inputs."""
+Per workload, against the oracle:
+  * CSR, boundary index, widths and offsets: bit-exact, every array in full;
+  * forward and backward messages: the ENTIRE packed buffer (padding
+    included) and every slot's meta bit-exact, from the oracle's C routines;
+  * forward aggregation, backward aggregation and the gated bf16 backward on
+    a seeded sample of 2^16 rows plus every row with more than 1,000 entries,
+    within |d| <= 1e-5*sum|terms| + 1e-7 (bf16: plus half a bf16 step);
+  * the transform at each width on sampled rows against fp64 products of the
+    oracle's aggregation rounded to bf16.
+The R-MAT scale workload runs every base width of its schedule (1, 2, 4, 8),
+the widths recomputed by gnn_boundary_set_bits."""
 import os
 
 import numpy as np
 import pytest
 
 import oracle as O
+from oracle import coracle as C
 from synth import make_workload
 from synth.graphs import CONFIGS, make_weight_bf16
 from tests.helpers import assert_close_agg, dev, host, oracle_boundary
@@ -24,14 +31,52 @@ G = pytest.importorskip("sparse_aggregation_message_gb300")
 
 SPLIT_LEN = 128
 LONG_SLOT_LEN = 128
-N_SAMPLE_ROWS = 2048
-N_SAMPLE_SLOTS = 4096
+N_SAMPLE_ROWS = 1 << 16
+LONG_ROW = 1000
+CHUNK_SLOTS = 1 << 22
 
 WORKLOADS = os.environ.get("GNN_TEST_WORKLOADS", "tiny,yelp,products,reddit,scale").split(",")
 
 
-def _bits_to_f32(b):
-    return (b.astype(np.uint32) << 16).view(np.float32)
+def _f32(bits):
+    return (np.asarray(bits).astype(np.uint32) << 16).view(np.float32)
+
+
+def sample_rows(n, rowptr, seed):
+    """2^16 seeded random rows (all rows when fewer) plus every row with more
+    than 1,000 entries."""
+    rng = np.random.default_rng(seed)
+    deg = np.diff(rowptr)
+    rnd = rng.choice(n, min(n, N_SAMPLE_ROWS), replace=False)
+    return np.unique(np.concatenate([rnd, np.nonzero(deg > LONG_ROW)[0]])).astype(np.int64)
+
+
+def compare_messages(packed_d, meta_d, want_packed, want_meta, off, what):
+    """GPU packed buffer and meta against the oracle's, in slot chunks (bit
+    for bit, padding included)."""
+    S = want_meta.shape[0]
+    for s0 in range(0, S, CHUNK_SLOTS):
+        s1 = min(S, s0 + CHUNK_SLOTS)
+        a, b = int(off[s0]), int(off[s1])
+        got_p = host(packed_d[a:b])
+        if not np.array_equal(got_p, want_packed[a:b]):
+            bad = np.nonzero(got_p != want_packed[a:b])[0][0] + a
+            s = int(np.searchsorted(off, bad, side="right") - 1)
+            raise AssertionError(f"{what}: packed byte {bad} (slot {s}) differs")
+        got_m = host(meta_d[s0:s1])
+        if not np.array_equal(got_m.view(np.uint32), want_meta[s0:s1].view(np.uint32)):
+            s = s0 + int(np.nonzero((got_m != want_meta[s0:s1]).any(1))[0][0])
+            raise AssertionError(f"{what}: meta of slot {s} differs: {got_m[s - s0]} vs {want_meta[s]}")
+
+
+def assert_close_bf16(got_bits, ref, T, gate, where):
+    """bf16 outputs: zero where the gate is off; elsewhere within the fp32
+    bound plus half a bf16 step (2^-8 relative)."""
+    g = _f32(got_bits).astype(np.float64)
+    assert np.all(g[~gate] == 0), f"{where}: gated-off element not zero"
+    bound = 2.0 ** -8 * np.abs(ref) + 1.1e-5 * T + 2e-7
+    bad = (np.abs(g - ref) > bound) & gate
+    assert not bad.any(), f"{where}: {bad.sum()} elements out of bound"
 
 
 @pytest.mark.parametrize("name", WORKLOADS)
@@ -42,7 +87,6 @@ def test_workload_parity(name):
         pytest.skip("no CUDA device")
     wl = make_workload(name)
     n, P, dims = wl.n, wl.P, wl.dims
-    rng = np.random.default_rng(wl.seed + 99)
 
     # ---- a1: CSR (full)
     csr = G.gnn_csr_build(n, dev(wl.src), dev(wl.dst))
@@ -57,9 +101,10 @@ def test_workload_parity(name):
     # ---- a2: boundary, widths, offsets (full), at the first base width
     F0 = dims[0]
     cfg = CONFIGS[name]
-    cfg_pct, cfg_bits, base = cfg["rule"]["pct"], cfg["rule"]["bits"], cfg["base_bits"][0]
-    bnd = G.gnn_boundary_index(csr, P, G.BitRule(cfg_pct, cfg_bits), base, F0)
-    ob = oracle_boundary(n, rp, col, val, P, cfg_pct, cfg_bits, base, F0)
+    pct, bits_rule, bases = cfg["rule"]["pct"], cfg["rule"]["bits"], cfg["base_bits"]
+    rule = G.BitRule(pct, bits_rule)
+    bnd = G.gnn_boundary_index(csr, P, rule, bases[0], F0)
+    ob = oracle_boundary(n, rp, col, val, P, pct, bits_rule, bases[0], F0)
     assert (bnd.n_slots, bnd.nnz_cut) == (ob["n_slots"], ob["nnz_cut"])
     for k in ("part_start", "send_start", "slot_node", "col_remap", "local_cnt", "slot_rowptr",
               "slot_col", "own_ptr", "own_slot", "node_bits", "slot_bits", "slot_off"):
@@ -68,102 +113,104 @@ def test_workload_parity(name):
     assert np.array_equal(host(bnd.slot_val).view(np.uint32), ob["slot_val"].view(np.uint32))
     assert np.array_equal(host(bnd.val_remap).view(np.uint32), ob["val_remap"].view(np.uint32))
     S = bnd.n_slots
-    sb = ob["slot_bits"]
     G.gnn_boundary_long_slots(csr, bnd, LONG_SLOT_LEN)
+    rows = sample_rows(n, rp, CONFIGS[name]["index"] + 99)
+    rows_d = t.from_numpy(rows).cuda()
 
-    # sampled rows: random plus the longest rows (those are split into pieces)
-    deg = np.diff(rp)
-    longest = np.argsort(-deg, kind="stable")[:32]
-    rows = np.unique(np.concatenate([rng.choice(n, min(n, N_SAMPLE_ROWS), replace=False), longest]))
-    slots = np.unique(rng.choice(S, min(S, N_SAMPLE_SLOTS), replace=False)) if S else np.zeros(0, np.int64)
-
-    for li, F in enumerate(sorted(set(dims[:-1]), reverse=True)):
-        ld = G.ld_for(F)
-        off = ob["slot_off"] if F == F0 else O.slot_offsets(sb, F)
-        off_d = bnd.slot_off if F == F0 else G.gnn_slot_offsets(bnd.slot_bits, S, F)
-        assert np.array_equal(host(off_d), off)
-        Q = int(off[-1])
-        # layer inputs: N(0,1) features for the first width, ReLU'd N(0,1) otherwise
+    widths = sorted(set(dims[:-1]), reverse=True)
+    inputs = {}
+    for li, F in enumerate(widths):
+        # layer inputs: N(0,1) features at the first width, ReLU'd N(0,1) otherwise
         g = t.Generator(device="cuda")
         g.manual_seed(1000 + F)
-        Hd = t.zeros((n, ld), device="cuda")
+        Hd = t.zeros((n, G.ld_for(F)), device="cuda")
         Hd[:, :F] = t.randn((n, F), generator=g, device="cuda")
         if F != F0:
             Hd.clamp_(min=0)
-        seed_f, seed_b = 2 * li, 2 * li + 1
-        packed = t.zeros(max(Q, 16), dtype=t.uint8, device="cuda")
-        meta = t.zeros((max(S, 1), 2), device="cuda")
-        G.gnn_quant_pack(Hd, F, bnd.slot_node, S, bnd.slot_bits, off_d, seed_f, packed, meta)
-        M = t.empty((n, ld), device="cuda")
-        G.gnn_spmm_fwd(csr, bnd, Hd, F, packed, meta, M=M, slot_off=off_d)
-        G.gnn_sync_check()
-        # forward messages on sampled slots
-        ph, mh = host(packed), host(meta)
-        Hrows = host(Hd[t.from_numpy(ob["slot_node"][slots]).long().cuda()])[:, :F] if S else None
-        if S:
-            codes, wmeta = O.quantize(Hrows, sb[slots], slots, seed_f)
-            assert np.array_equal(mh[slots].view(np.uint32), wmeta.view(np.uint32))
-            for b in np.unique(sb[slots]):
-                sel = slots[sb[slots] == b]
-                rb = int(O.rowbytes(b, F))
-                got = ph[off[sel][:, None] + np.arange(rb)[None, :]]
-                want = O.pack(codes[sb[slots] == b], np.full(sel.size, b), F,
-                              np.arange(sel.size) * rb, sel.size * rb).reshape(sel.size, rb)
-                assert np.array_equal(got, want), f"packed bytes F={F} b={b}"
-        # forward aggregation on sampled rows (the oracle quantises what they read)
-        need = np.unique(np.concatenate([col[rp[r]:rp[r + 1]] for r in rows] + [rows]))
-        Hh = np.zeros((n, F), np.float32)
-        Hh[need] = host(Hd[t.from_numpy(need).long().cuda()])[:, :F]
-        ref, T = O.spmm_fwd(n, rp, col, val, Hh, F, ob, sb, seed_f, rows=rows)
-        assert_close_agg(host(M[t.from_numpy(rows).long().cuda()])[:, :F], ref, T, f"{name} fwd F={F}")
+        inputs[F] = Hd
 
-        # backward: G = the forward output (any dense matrix serves)
-        dH = t.empty((n, ld), device="cuda")
-        pw = t.zeros_like(packed)
-        mw = t.zeros_like(meta)
-        G.gnn_spmm_bwd(csr, bnd, M, F, seed_b, pw, mw, dH, slot_off=off_d)
-        G.gnn_sync_check()
-        ob_F = dict(ob)
-        ob_F["slot_off"] = off
-        # rows the sampled slots' partials and the sampled rows' owned slots read
-        own = np.concatenate([ob["own_slot"][ob["own_ptr"][r]:ob["own_ptr"][r + 1]] for r in rows])
-        chk = np.unique(np.concatenate([slots, own])).astype(np.int64)
-        srp, scol = ob["slot_rowptr"], ob["slot_col"]
-        needv = np.unique(np.concatenate([scol[srp[s]:srp[s + 1]] for s in chk] + [need])) if chk.size else need
-        Gh = np.zeros((n, F), np.float32)
-        Gh[needv] = host(M[t.from_numpy(needv).long().cuda()])[:, :F]
-        if S:
-            part = O.slot_partials(ob, Gh, F, slots)
-            codes, wmeta = O.quantize(part, sb[slots], slots, seed_b)
-            assert np.array_equal(host(mw)[slots].view(np.uint32), wmeta.view(np.uint32))
-            pwh = host(pw)
-            for b in np.unique(sb[slots]):
-                sel = slots[sb[slots] == b]
-                rb = int(O.rowbytes(b, F))
-                got = pwh[off[sel][:, None] + np.arange(rb)[None, :]]
-                want = O.pack(codes[sb[slots] == b], np.full(sel.size, b), F,
-                              np.arange(sel.size) * rb, sel.size * rb).reshape(sel.size, rb)
-                assert np.array_equal(got, want), f"backward packed bytes F={F} b={b}"
-        dref, T2 = O.spmm_bwd(n, rp, col, val, Gh, F, ob, sb, seed_b, rows=rows)
-        assert_close_agg(host(dH[t.from_numpy(rows).long().cuda()])[:, :F], dref, T2, f"{name} bwd F={F}")
-        del pw, mw, dH
+    # every base width of the workload's schedule (one epoch each)
+    for bi, base in enumerate(bases if name == "scale" else bases[:1]):
+        if bi > 0:
+            G.gnn_boundary_set_bits(csr, bnd, rule, base, F0)
+            nb = O.node_bits(n, rp, ob, pct, bits_rule, base)
+            ob["node_bits"] = nb
+            ob["slot_bits"] = nb[ob["slot_node"]].astype(np.uint8)
+            ob["slot_off"] = O.slot_offsets(ob["slot_bits"], F0)
+            for k in ("node_bits", "slot_bits", "slot_off"):
+                assert np.array_equal(host(bnd.arrays[k]), np.asarray(ob[k])), f"base {base}: {k}"
+        sb = ob["slot_bits"]
+        for li, F in enumerate(widths):
+            tag = f"{name} base {base} F={F}"
+            ld = G.ld_for(F)
+            off = ob["slot_off"] if F == F0 else O.slot_offsets(sb, F)
+            off_d = bnd.slot_off if F == F0 else G.gnn_slot_offsets(bnd.slot_bits, S, F)
+            assert np.array_equal(host(off_d), off)
+            Q = int(off[-1])
+            Hd = inputs[F]
+            Hh = host(Hd)
+            seed_f, seed_b = 2 * li + 8 * bi, 2 * li + 1 + 8 * bi
 
-        # the transform of this width on the sampled rows, teacher-forced on Mb
-        Fo = dims[1]
-        Mb = t.empty((n, G.ldb_for(F)), dtype=t.bfloat16, device="cuda")
-        packed = t.zeros(max(Q, 16), dtype=t.uint8, device="cuda")
-        meta = t.zeros((max(S, 1), 2), device="cuda")
-        G.gnn_quant_pack(Hd, F, bnd.slot_node, S, bnd.slot_bits, off_d, seed_f, packed, meta)
-        G.gnn_spmm_fwd(csr, bnd, Hd, F, packed, meta, Mb=Mb, slot_off=off_d)
-        W = make_weight_bf16(F, Fo, 1234, li)
-        Ho = t.empty((n, G.ld_for(Fo)), device="cuda")
-        G.gnn_dense_fwd(Mb, n, F, dev(W.view(np.int16)), Fo, True, Ho)
-        G.gnn_sync_check()
-        A = _bits_to_f32(host(Mb[t.from_numpy(rows).long().cuda()].view(t.int16)).view(np.uint16))[:, :F]
-        B = _bits_to_f32(W)
-        _, Href = O.dense_fwd(A, B, True)
-        got = host(Ho[t.from_numpy(rows).long().cuda()])[:, :Fo]
-        scale = O.gemm_abs(A, B)
-        assert np.all(np.abs(got - Href) <= 1e-4 * scale + 1e-6), f"{name} transform F={F}"
-        del Hd, M, Mb, Ho, packed, meta
-        t.cuda.empty_cache()
+            # ---- a3: forward messages, the whole buffer
+            packed = t.zeros(max(Q, 16), dtype=t.uint8, device="cuda")
+            meta = t.zeros((max(S, 1), 2), device="cuda")
+            G.gnn_quant_pack(Hd, F, bnd.slot_node, S, bnd.slot_bits, off_d, seed_f, packed, meta)
+            G.gnn_sync_check()
+            fp, fm = C.quant_pack(Hh, F, ob["slot_node"], sb, off, seed_f)
+            compare_messages(packed, meta, fp, fm, off, f"{tag} forward messages")
+
+            # ---- a4: forward aggregation on the sampled rows
+            M = t.empty((n, ld), device="cuda")
+            G.gnn_spmm_fwd(csr, bnd, Hd, F, packed, meta, M=M, slot_off=off_d)
+            G.gnn_sync_check()
+            ref, T = C.spmm_fwd_rows(rp, ob, Hh, F, fp, fm, sb, off, rows)
+            assert_close_agg(host(M[rows_d])[:, :F], ref, T, f"{tag} fwd")
+
+            # ---- a5: the transform of this width (first base): the bench's
+            # bf16 aggregation output feeds tcgen05; on the sampled rows the
+            # result is checked against fp64 products of the oracle's own
+            # aggregation rounded to bf16 (an input may sit one bf16 step from
+            # the GPU's: inside the transform's 2e-2 tolerance)
+            if bi == 0:
+                Fo = dims[1]
+                Mb = t.empty((n, G.ldb_for(F)), dtype=t.bfloat16, device="cuda")
+                G.gnn_spmm_fwd(csr, bnd, Hd, F, packed, meta, Mb=Mb, slot_off=off_d)
+                W = make_weight_bf16(F, Fo, 1234, li)
+                Ho = t.empty((n, G.ld_for(Fo)), device="cuda")
+                G.gnn_dense_fwd(Mb, n, F, dev(W.view(np.int16)), Fo, True, Ho)
+                G.gnn_sync_check()
+                k = min(rows.size, 4096)
+                A = O.bf16_round(ref[:k].astype(np.float32))
+                B = _f32(W)
+                _, Href = O.dense_fwd(A, B, True)
+                got = host(Ho[rows_d[:k]])[:, :Fo]
+                scale = O.gemm_abs(A, B)
+                assert np.all(np.abs(got - Href) <= 2e-2 * scale + 1e-6), f"{tag} transform"
+                del Mb, Ho
+            del ref, T, packed
+
+            # ---- a7: backward messages from G = M, the whole buffer
+            Gh = host(M)
+            pw = t.zeros(max(Q, 16), dtype=t.uint8, device="cuda")
+            mw = t.zeros((max(S, 1), 2), device="cuda")
+            G.gnn_halo_quant_pack(bnd, M, F, seed_b, pw, mw, slot_off=off_d)
+            G.gnn_sync_check()
+            hp, hm = C.halo_quant_pack(ob, Gh, F, sb, off, seed_b)
+            compare_messages(pw, mw, hp, hm, off, f"{tag} backward messages")
+
+            # ---- a8: backward aggregation, plain (fp32) and gated (bf16)
+            dH = t.empty((n, ld), device="cuda")
+            G.gnn_spmm_bwd_local(csr, bnd, M, F, pw, mw, dH, slot_off=off_d)
+            ldz = G.ldz_for(F)
+            dZ = t.full((n, ldz), float("nan"), dtype=t.bfloat16, device="cuda")
+            G.gnn_spmm_bwd_local_masked(csr, bnd, M, F, pw, mw, Hd, dZ, slot_off=off_d)
+            G.gnn_sync_check()
+            dref, T2 = C.spmm_bwd_rows(rp, ob, Gh, F, hp, hm, sb, off, rows)
+            assert_close_agg(host(dH[rows_d])[:, :F], dref, T2, f"{tag} bwd")
+            zb = host(dZ[rows_d].view(t.int16)).view(np.uint16)
+            assert np.all(zb[:, F:] == 0), f"{tag}: dZ padding"
+            assert_close_bf16(zb[:, :F], dref, T2, Hh[rows, :F] > 0, f"{tag} gated bwd")
+            del dH, dZ, pw, mw, dref, T2, Gh
+
+            del M, meta, Hh, fp, fm, hp, hm
+            t.cuda.empty_cache()
