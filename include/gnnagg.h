@@ -176,6 +176,12 @@ typedef struct gnn_boundary {
    * gnn_boundary_index when both it and csr->val_t are non-NULL, and then
    * used by the backward calls in place of val_remap (NULL: A symmetric).   */
   float* val_remap_t;
+  /* Optional visiting order of the backward halo kernel (filled by
+   * gnn_boundary_long_slots when non-NULL; NULL = slot order): the slots
+   * sorted by their first backward entry v, ties by s.  Slots that read the
+   * same gradient rows then run at the same time and share those rows in L2.
+   * It changes no result: every slot's sum keeps its own fixed order.      */
+  int32_t* halo_order;  /* [n_slots]                                        */
 } gnn_boundary;
 
 /* Workspace bytes for gnn_boundary_count / _index / _set_bits on this CSR. */
@@ -211,6 +217,8 @@ gnn_status gnn_boundary_long_slots_count(const gnn_boundary* bnd, int32_t long_s
                                          gnn_stream_t stream);
 gnn_status gnn_boundary_long_slots(gnn_boundary* bnd, void* ws, size_t ws_bytes,
                                    gnn_stream_t stream);
+/* gnn_boundary_long_slots also fills bnd->halo_order when it is non-NULL
+ * (n_slots int32 entries, caller-allocated). */
 
 /* slot_off[s] = sum_{t<s} rowbytes(slot_bits[t], F), slot_off[S] = total,
  * rowbytes(b,F) = 16*ceil(F*b/128) (b=32: 16*ceil(4F/16)).  Every row starts
@@ -378,6 +386,23 @@ gnn_status gnn_layer_bwd(const gnn_csr* csr, const gnn_boundary* bnd, const floa
  * with the same buffers. */
 gnn_status gnn_halo_quant_pack(const gnn_boundary* bnd, const float* G, int64_t ldg, int32_t F,
                                uint32_t seed, uint8_t* packed, float* meta, gnn_stream_t stream);
+/* Slot-range forms for a rank that holds some partitions of a multi-GPU
+ * job (SYLVIE guide, section 5: every worker quantises the boundary rows it
+ * owns and sends them; section 11: backward messages return to the owners).
+ * gnn_quant_pack_slots quantises and packs the message rows of slots
+ * s0..s1-1 only (row X[slot_node[s]], width slot_bits[s], row key s, bytes
+ * at packed + slot_off[s], meta[2s..2s+1]): the bytes a full gnn_quant_pack
+ * over every slot writes there.  gnn_halo_quant_pack_slots forms the
+ * backward messages of slots s0..s1-1 only (bytes as gnn_halo_quant_pack
+ * writes them).  Neither touches the rows of other slots.  Checks as
+ * gnn_quant_pack / gnn_halo_quant_pack; 0 <= s0 <= s1 (<= n_slots). */
+gnn_status gnn_quant_pack_slots(const float* X, int64_t ldx, int32_t F, const int32_t* slot_node,
+                                int64_t s0, int64_t s1, const uint8_t* slot_bits,
+                                const int64_t* slot_off, uint32_t seed, uint8_t* packed,
+                                float* meta, gnn_stream_t stream);
+gnn_status gnn_halo_quant_pack_slots(const gnn_boundary* bnd, const float* G, int64_t ldg,
+                                     int32_t F, int64_t s0, int64_t s1, uint32_t seed,
+                                     uint8_t* packed, float* meta, gnn_stream_t stream);
 gnn_status gnn_spmm_bwd_local(const gnn_csr* csr, const gnn_boundary* bnd, const float* G,
                               int64_t ldg, int32_t F, const uint8_t* packed, const float* meta,
                               float* dH, int64_t ldh, void* ws, size_t ws_bytes,
@@ -613,9 +638,11 @@ gnn_status gnn_ldr_init(gnn_ldr_state* st, double lambda, int32_t delta, int32_t
 gnn_status gnn_ldr_update(gnn_ldr_state* st, const double* partition_loss, int32_t n_parts,
                           double epoch_seconds);
 
-/* Synchronise `stream` and report device-side failures (GNN_ERR_CUDA for a
- * CUDA error, GNN_ERR_DEVICE_CHECK / GNN_ERR_TIMEOUT for flags the kernels
- * raised).  Clears the flags. */
+/* Synchronise `stream`, then the whole device (a flag can come from a kernel
+ * on another stream, e.g. the aux stream of the asynchronous layers), and
+ * report device-side failures (GNN_ERR_CUDA for a CUDA error,
+ * GNN_ERR_DEVICE_CHECK / GNN_ERR_TIMEOUT for flags the kernels raised).
+ * Clears the flags. */
 gnn_status gnn_sync_check(gnn_stream_t stream);
 
 #ifdef __cplusplus

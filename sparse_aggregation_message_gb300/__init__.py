@@ -22,7 +22,7 @@ __all__ = [
     "gnn_quant_pack", "gnn_dequant_unpack", "gnn_spmm_fwd", "gnn_spmm_bwd", "gnn_sync_check", "gnn_kernel_launches",
     "rowbytes", "ld_for", "ldb_for", "gnn_dense_workspace", "gnn_dense_fwd", "gnn_dense_bwd",
     "gnn_layer_workspace", "gnn_layer_fwd", "gnn_layer_bwd",
-    "gnn_halo_quant_pack", "gnn_spmm_bwd_local", "gnn_layer_fwd_async", "gnn_layer_bwd_async",
+    "gnn_halo_quant_pack", "gnn_spmm_bwd_local", "gnn_quant_pack_slots", "gnn_halo_quant_pack_slots", "gnn_layer_fwd_async", "gnn_layer_bwd_async",
     "LdrState", "gnn_ldr_init", "gnn_ldr_update", "gnn_quant_divide",
     "gnn_layer_tf_workspace", "gnn_layer_fwd_tf", "gnn_layer_bwd_tf",
     "gnn_gat_index", "gnn_gat_workspace", "gnn_gat_layer_fwd", "gnn_gat_layer_bwd",
@@ -142,6 +142,7 @@ class Boundary:
         b.long_slot_len, b.n_long_slots = self.long_slot_len, self.n_long_slots
         b.long_slots = _ptr(a.get("long_slots"))
         b.val_remap_t = _ptr(a.get("val_remap_t"))
+        b.halo_order = _ptr(a.get("halo_order"))
         return b
 
 
@@ -248,9 +249,12 @@ def gnn_boundary_index(csr: Csr, P: int, rule: BitRule, base_bits: int, F: int,
     return b
 
 
-def gnn_boundary_long_slots(csr: Csr, bnd: Boundary, long_slot_len: int = 128, stream=None) -> None:
+def gnn_boundary_long_slots(csr: Csr, bnd: Boundary, long_slot_len: int = 128, stream=None,
+                            halo_order: bool = True) -> None:
     """Attach the list of slots with more than long_slot_len backward entries
-    (their halo partials are then summed by a whole thread block each)."""
+    (their halo partials are then summed by a whole thread block each) and,
+    with halo_order, the halo kernel's visiting order (slots by first
+    backward entry)."""
     torch = _torch()
     dev = csr.rowptr.device
     c = csr.c()
@@ -264,6 +268,10 @@ def gnn_boundary_long_slots(csr: Csr, bnd: Boundary, long_slot_len: int = 128, s
          ws.numel(), st)
     bnd.arrays["long_slots"] = torch.empty(max(nl.value, 1), dtype=torch.int32, device=dev)
     bnd.long_slot_len, bnd.n_long_slots = long_slot_len, nl.value
+    if halo_order:
+        bnd.arrays["halo_order"] = torch.empty(max(bnd.n_slots, 1), dtype=torch.int32, device=dev)
+    else:
+        bnd.arrays.pop("halo_order", None)
     cb = bnd.c()
     call("gnn_boundary_long_slots", ctypes.byref(cb), _ptr(ws), ws.numel(), st)
 
@@ -356,6 +364,23 @@ def gnn_halo_quant_pack(bnd: Boundary, G, F: int, seed: int, packed, meta, slot_
     cb = bnd.c(slot_off, F if slot_off is not None else None)
     call("gnn_halo_quant_pack", ctypes.byref(cb), _ptr(G), G.stride(0), F, seed & 0xFFFFFFFF,
          _ptr(packed), _ptr(meta), _stream(stream))
+
+
+def gnn_quant_pack_slots(X, F: int, slot_node, s0: int, s1: int, slot_bits, slot_off, seed: int,
+                         packed, meta, stream=None) -> None:
+    """Forward messages of slots s0..s1-1 only (row key s), at their places in
+    the slot-ordered buffer."""
+    call("gnn_quant_pack_slots", _ptr(X), X.stride(0), F, _ptr(slot_node), int(s0), int(s1),
+         _ptr(slot_bits), _ptr(slot_off), seed & 0xFFFFFFFF, _ptr(packed), _ptr(meta),
+         _stream(stream))
+
+
+def gnn_halo_quant_pack_slots(bnd: Boundary, G, F: int, s0: int, s1: int, seed: int, packed, meta,
+                              slot_off=None, stream=None) -> None:
+    """Backward messages of slots s0..s1-1 only."""
+    cb = bnd.c(slot_off, F if slot_off is not None else None)
+    call("gnn_halo_quant_pack_slots", ctypes.byref(cb), _ptr(G), G.stride(0), F, int(s0), int(s1),
+         seed & 0xFFFFFFFF, _ptr(packed), _ptr(meta), _stream(stream))
 
 
 def gnn_spmm_bwd_local(csr: Csr, bnd: Boundary, G, F: int, packed, meta, dH, slot_off=None,

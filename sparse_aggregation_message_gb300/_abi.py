@@ -38,7 +38,7 @@ class GnnBoundary(ctypes.Structure):
                 ("slot_col", c_vp), ("slot_val", c_vp), ("own_ptr", c_vp), ("own_slot", c_vp),
                 ("node_bits", c_vp), ("slot_bits", c_vp), ("slot_off", c_vp),
                 ("long_slot_len", c_i32), ("n_long_slots", c_i32), ("long_slots", c_vp),
-                ("val_remap_t", c_vp)]
+                ("val_remap_t", c_vp), ("halo_order", c_vp)]
 
 
 class GnnBlocked(ctypes.Structure):
@@ -100,6 +100,10 @@ PROTOTYPES = {
                                      c_i32, c_i32, c_u32, c_vp, c_vp, c_vp, c_vp, c_i64, c_vp, c_size,
                                      c_vp]),
     "gnn_halo_quant_pack": (ctypes.c_int, [P_bnd, c_vp, c_i64, c_i32, c_u32, c_vp, c_vp, c_vp]),
+    "gnn_quant_pack_slots": (ctypes.c_int, [c_vp, c_i64, c_i32, c_vp, c_i64, c_i64, c_vp, c_vp, c_u32,
+                                            c_vp, c_vp, c_vp]),
+    "gnn_halo_quant_pack_slots": (ctypes.c_int, [P_bnd, c_vp, c_i64, c_i32, c_i64, c_i64, c_u32, c_vp,
+                                                 c_vp, c_vp]),
     "gnn_spmm_bwd_local": (ctypes.c_int, [P_csr, P_bnd, c_vp, c_i64, c_i32, c_vp, c_vp, c_vp, c_i64, c_vp,
                                           c_size, c_vp]),
     "gnn_layer_fwd_async": (ctypes.c_int, [P_csr, P_bnd, c_vp, c_i64, c_i32, c_vp, c_i32, c_i32, c_u32,

@@ -72,6 +72,55 @@ __device__ __forceinline__ float div_rn(float a, const Divisor& d) {
   return __fmaf_rn(__fmaf_rn(-d.b, q, a), d.y, q);  // correctly rounded
 }
 
+// Paired fp32 arithmetic: each lane of a float2 rounded exactly as the
+// scalar operation (sm_100's packed FMA/MUL/ADD issue two IEEE operations
+// per instruction).  A paired multiply whose result feeds a paired add may be
+// contracted into one fused multiply-add by the code generator even with an
+// explicit .rn (measured), so they are used only where no multiply feeds an
+// add: fused multiply-adds, sums of loaded values, and the quantiser's
+// subtract / multiply / fused-correction chain.
+__device__ __forceinline__ float2 dup2(float a) { return make_float2(a, a); }
+
+__device__ __forceinline__ unsigned long long pack2(float2 v) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(v.x), "f"(v.y));
+  return r;
+}
+
+__device__ __forceinline__ float2 unpack2(unsigned long long r) {
+  float2 v;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+  return v;
+}
+
+__device__ __forceinline__ float2 add2_rn(float2 a, float2 b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pack2(a)), "l"(pack2(b)));
+  return unpack2(d);
+}
+
+__device__ __forceinline__ float2 mul2_rn(float2 a, float2 b) {
+  unsigned long long d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pack2(a)), "l"(pack2(b)));
+  return unpack2(d);
+}
+
+__device__ __forceinline__ float2 fma2_rn(float2 a, float2 b, float2 c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(pack2(a)), "l"(pack2(b)), "l"(pack2(c)));
+  return unpack2(d);
+}
+
+// div_rn on a pair of dividends.
+template <bool FAST>
+__device__ __forceinline__ float2 div2_rn(float2 a, const Divisor& d) {
+  if (!FAST) return make_float2(__fdiv_rn(a.x, d.b), __fdiv_rn(a.y, d.b));
+  const float2 y = dup2(d.y), nb = dup2(-d.b);
+  float2 q = mul2_rn(a, y);
+  q = fma2_rn(fma2_rn(nb, q, a), y, q);     // faithful
+  return fma2_rn(fma2_rn(nb, q, a), y, q);  // correctly rounded
+}
+
 // The rest of fmix32 after its first step h ^= h >> 16.
 __device__ __forceinline__ uint32_t fmix32_tail(uint32_t h) {
   h *= 0x85ebca6bu;
@@ -106,14 +155,20 @@ __device__ __forceinline__ void pack_codes(const float4 (&v)[CPL], int F, float 
       // gives those elements in-row values, so no element is special-cased)
       const uint32_t kc = key ^ (uint32_t)(4 * c);
       const uint32_t a = kc ^ (kc >> 16);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float t = div_rn<FAST>(__fsub_rn(elem(v[i], k), mn), dv);
-        const float m = static_cast<float>(fmix32_tail(a ^ (uint32_t)k) >> 8);
-        // floor(t + u) >= 0 and below 2^24: round down while converting
-        const uint32_t q = min(__float2uint_rd(__fmaf_rn(m, 5.9604644775390625e-08f, t)), TOP);
-        part += q << (k * B);  // disjoint fields: + is |
-      }
+      // x - min (as x + (-min): the same IEEE result), then the division
+      const float2 nmn = dup2(-mn);
+      const float2 t01 = div2_rn<FAST>(add2_rn(make_float2(v[i].x, v[i].y), nmn), dv);
+      const float2 t23 = div2_rn<FAST>(add2_rn(make_float2(v[i].z, v[i].w), nmn), dv);
+      const float2 m01 = make_float2(static_cast<float>(fmix32_tail(a) >> 8),
+                                     static_cast<float>(fmix32_tail(a ^ 1u) >> 8));
+      const float2 m23 = make_float2(static_cast<float>(fmix32_tail(a ^ 2u) >> 8),
+                                     static_cast<float>(fmix32_tail(a ^ 3u) >> 8));
+      const float2 e24 = dup2(5.9604644775390625e-08f);
+      const float2 r01 = fma2_rn(m01, e24, t01), r23 = fma2_rn(m23, e24, t23);
+      // floor(t + u) >= 0 and below 2^24: round down while converting
+      part = min(__float2uint_rd(r01.x), TOP) | (min(__float2uint_rd(r01.y), TOP) << B) |
+             (min(__float2uint_rd(r23.x), TOP) << (2 * B)) |
+             (min(__float2uint_rd(r23.y), TOP) << (3 * B));
       const int nv = F - 4 * c;  // elements of chunk c below F, >= 1
       if (nv < 4) part &= (1u << (B * nv)) - 1u;
     }
@@ -201,13 +256,9 @@ __device__ __forceinline__ void quantize_pack_row(const float4 (&v)[CPL], int F,
   if (gl == 0) *meta = make_float2(mn, scale);
 }
 
-// The 4 dequantised values of chunk c of a packed row (width b, meta m).
-__device__ __forceinline__ float4 dequant_chunk(const uint8_t* __restrict__ row, int b,
-                                                float mn, float scale, int c) {
-  if (b == 32) return __ldg(reinterpret_cast<const float4*>(row) + c);
-  const uint32_t bitpos = (uint32_t)(4 * c * b);
-  const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(row) + (bitpos >> 5));
-  const uint32_t bits4 = w >> (bitpos & 31u);
+// The 4 dequantised values fl(fl(scale * code) + min) of the codes in the low
+// 4b bits of bits4 (width b < 32).
+__device__ __forceinline__ float4 dequant4(uint32_t bits4, int b, float mn, float scale) {
   const uint32_t m = (1u << b) - 1u;
   float4 r;
   r.x = __fadd_rn(__fmul_rn(scale, (float)(bits4 & m)), mn);
@@ -217,18 +268,38 @@ __device__ __forceinline__ float4 dequant_chunk(const uint8_t* __restrict__ row,
   return r;
 }
 
+// The 4 dequantised values of chunk c of a packed row (width b, meta m).
+__device__ __forceinline__ float4 dequant_chunk(const uint8_t* __restrict__ row, int b,
+                                                float mn, float scale, int c) {
+  if (b == 32) return __ldg(reinterpret_cast<const float4*>(row) + c);
+  const uint32_t bitpos = (uint32_t)(4 * c * b);
+  const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(row) + (bitpos >> 5));
+  const uint32_t bits4 = w >> (bitpos & 31u);
+  return dequant4(bits4, b, mn, scale);
+}
+
 __device__ __forceinline__ void fma4(float4& acc, float w, const float4& x) {
-  acc.x = fmaf(w, x.x, acc.x);
-  acc.y = fmaf(w, x.y, acc.y);
-  acc.z = fmaf(w, x.z, acc.z);
-  acc.w = fmaf(w, x.w, acc.w);
+  const float2 ww = dup2(w);
+  const float2 lo = fma2_rn(ww, make_float2(x.x, x.y), make_float2(acc.x, acc.y));
+  const float2 hi = fma2_rn(ww, make_float2(x.z, x.w), make_float2(acc.z, acc.w));
+  acc = make_float4(lo.x, lo.y, hi.x, hi.y);
 }
 
 __device__ __forceinline__ void add4(float4& acc, const float4& x) {
-  acc.x += x.x;
-  acc.y += x.y;
-  acc.z += x.z;
-  acc.w += x.w;
+  const float2 lo = add2_rn(make_float2(acc.x, acc.y), make_float2(x.x, x.y));
+  const float2 hi = add2_rn(make_float2(acc.z, acc.w), make_float2(x.z, x.w));
+  acc = make_float4(lo.x, lo.y, hi.x, hi.y);
+}
+
+// acc = fl(acc + fl(w * x)) element by element (product and sum each
+// rounded: the fixed-order halo partial sums).  Scalar: the paired multiply
+// and add can be contracted into one fused operation by the code generator,
+// the scalar _rn forms never are.
+__device__ __forceinline__ void mul_add4(float4& acc, float w, const float4& x) {
+  acc.x = __fadd_rn(acc.x, __fmul_rn(w, x.x));
+  acc.y = __fadd_rn(acc.y, __fmul_rn(w, x.y));
+  acc.z = __fadd_rn(acc.z, __fmul_rn(w, x.z));
+  acc.w = __fadd_rn(acc.w, __fmul_rn(w, x.w));
 }
 
 // Stores chunk c of an fp32 row, zeroing elements >= F.

@@ -12,6 +12,11 @@ namespace gnn {
 gnn_status launch_quant_pack(const float* X, int64_t ldx, int F, const int32_t* row_idx,
                              int64_t n_rows, const uint8_t* bits, const int64_t* off,
                              uint32_t seed, uint8_t* packed, float2* meta, cudaStream_t st);
+// Rows [r0, r0 + n_rows) of the row lists (row key = row index).
+gnn_status launch_quant_pack_range(const float* X, int64_t ldx, int F, const int32_t* row_idx,
+                                   int64_t r0, int64_t n_rows, const uint8_t* bits,
+                                   const int64_t* off, uint32_t seed, uint8_t* packed,
+                                   float2* meta, cudaStream_t st);
 
 gnn_status launch_dequant_unpack(const uint8_t* packed, const float2* meta, const int64_t* off,
                                  const uint8_t* bits, int64_t n_rows, int F, float* out,
@@ -42,10 +47,11 @@ gnn_status launch_halo_quant_pack(const gnn_boundary& b, const float* Gm, int64_
 // The halo quant-pack with other entry weights (sval, slot-CSR order) and,
 // when score_r is given, the score term fl(P + fl(score_r[s] * a_r[j])) added
 // to each slot's partial before it is quantised.
+// Slots [s_lo, s_hi) only (s_hi < 0: every slot).
 gnn_status launch_halo_quant_pack_ex(const gnn_boundary& b, const float* Gm, int64_t ldg, int F,
                                      uint32_t seed, uint8_t* packed_ws, float2* meta_ws,
                                      const float* sval, const float* score_r, const float* a_r,
-                                     cudaStream_t st);
+                                     cudaStream_t st, int64_t s_lo = 0, int64_t s_hi = -1);
 
 // Aggregations with caller weights in place of the CSR's (CSR order without
 // a boundary, col_remap order with one): the forward (fp32 out, optional

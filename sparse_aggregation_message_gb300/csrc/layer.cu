@@ -290,23 +290,24 @@ extern "C" gnn_status gnn_layer_fwd_async(const gnn_csr* csr, const gnn_boundary
               "gnn_layer_fwd_async: message buffers required with a boundary");
   GNN_REQUIRE(ldh >= F_in && ldh % 4 == 0 && H_in && ((uintptr_t)H_in & 15) == 0,
               "gnn_layer_fwd_async: bad H_in");
+  GNN_REQUIRE(bnd->n_slots == 0 || (packed_prev != packed_next && meta_prev != meta_next),
+              "gnn_layer_fwd_async: the previous and next message buffers must differ");
   bool ok;
   LayerWs w = layer_ws_layout(ws, ws_bytes, *csr, F_in, F_out, &ok);
   GNN_REQUIRE(ws && ok, "gnn_layer_fwd_async: workspace too small (%zu < %zu)", ws_bytes, w.bytes);
   cudaStream_t st = as_stream(stream), ax = as_stream(aux);
   Fork f;
   if ((s = fork_to(f, st, ax)) != GNN_OK) return s;
-  if (bnd->n_slots > 0) {
+  // from here on `stream` always waits for `aux` before returning, error or not
+  if (bnd->n_slots > 0)
     s = launch_quant_pack(H_in, ldh, F_in, bnd->slot_node, bnd->n_slots, bnd->slot_bits,
                           bnd->slot_off, seed, packed_next, reinterpret_cast<float2*>(meta_next), ax);
-    if (s != GNN_OK) return s;
-  }
-  s = gnn_spmm_fwd(csr, bnd, H_in, ldh, F_in, packed_prev, meta_prev, nullptr, 0, Mb, ldmb, w.spmm,
-                   spmm_workspace_bytes(*csr, F_in), stream);
-  if (s != GNN_OK) return s;
-  if ((s = dense_fwd_impl(Mb, ldmb, csr->n, F_in, W, F_out, relu, H_out, ldo, w.dense, st)) != GNN_OK)
-    return s;
-  return join_from(f, st, ax);
+  if (s == GNN_OK)
+    s = gnn_spmm_fwd(csr, bnd, H_in, ldh, F_in, packed_prev, meta_prev, nullptr, 0, Mb, ldmb,
+                     w.spmm, spmm_workspace_bytes(*csr, F_in), stream);
+  if (s == GNN_OK) s = dense_fwd_impl(Mb, ldmb, csr->n, F_in, W, F_out, relu, H_out, ldo, w.dense, st);
+  const gnn_status j = join_from(f, st, ax);
+  return s != GNN_OK ? s : j;
 }
 
 extern "C" gnn_status gnn_layer_bwd_async(const gnn_csr* csr, const gnn_boundary* bnd,
@@ -326,6 +327,8 @@ extern "C" gnn_status gnn_layer_bwd_async(const gnn_csr* csr, const gnn_boundary
   LayerWs w = layer_ws_layout(ws, ws_bytes, *csr, F_in, F_out, &ok);
   GNN_REQUIRE(ws && ok, "gnn_layer_bwd_async: workspace too small (%zu < %zu)", ws_bytes, w.bytes);
   GNN_REQUIRE(dW, "gnn_layer_bwd_async: dW is NULL");
+  GNN_REQUIRE(!dH_in || bnd->n_slots == 0 || (packed_prev != packed_next && meta_prev != meta_next),
+              "gnn_layer_bwd_async: the previous and next message buffers must differ");
   const int64_t ldm = round_up(F_in, 4);
   s = gnn_dense_bwd(Mb, ldmb, csr->n, F_in, W, F_out, dH_out, ldg, H_out, ldo, relu,
                     dH_in ? w.dM : nullptr, ldm, dW, w.dense.wt, w.dense.bytes, stream);
@@ -333,12 +336,13 @@ extern "C" gnn_status gnn_layer_bwd_async(const gnn_csr* csr, const gnn_boundary
   cudaStream_t st = as_stream(stream), ax = as_stream(aux);
   Fork f;
   if ((s = fork_to(f, st, ax)) != GNN_OK) return s;
-  if ((s = gnn_halo_quant_pack(bnd, w.dM, ldm, F_in, seed, packed_next, meta_next, aux)) != GNN_OK)
-    return s;
-  s = gnn_spmm_bwd_local(csr, bnd, w.dM, ldm, F_in, packed_prev, meta_prev, dH_in, ldh, w.spmm,
-                         spmm_workspace_bytes(*csr, F_in), stream);
-  if (s != GNN_OK) return s;
-  return join_from(f, st, ax);
+  // from here on `stream` always waits for `aux` before returning, error or not
+  s = gnn_halo_quant_pack(bnd, w.dM, ldm, F_in, seed, packed_next, meta_next, aux);
+  if (s == GNN_OK)
+    s = gnn_spmm_bwd_local(csr, bnd, w.dM, ldm, F_in, packed_prev, meta_prev, dH_in, ldh, w.spmm,
+                           spmm_workspace_bytes(*csr, F_in), stream);
+  const gnn_status j = join_from(f, st, ax);
+  return s != GNN_OK ? s : j;
 }
 
 // ------------------------------------------------------------------ transform-first layers

@@ -12,11 +12,12 @@ template <int G, int CPL>
 __global__ void __launch_bounds__(256) quant_pack_kernel(
     const float* __restrict__ X, int64_t ldx, int F, const int32_t* __restrict__ row_idx,
     int64_t n_rows, const uint8_t* __restrict__ row_bits, const int64_t* __restrict__ row_off,
-    uint32_t seed, uint8_t* __restrict__ packed, float2* __restrict__ meta) {
+    uint32_t seed, uint8_t* __restrict__ packed, float2* __restrict__ meta, int64_t r0) {
   const int lane = threadIdx.x & 31;
   const int gl = lane & (G - 1);
-  const int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / G;
-  if (r >= n_rows) return;  // uniform across the group
+  const int64_t idx = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / G;
+  if (idx >= n_rows) return;  // uniform across the group
+  const int64_t r = r0 + idx;  // row (and row key) of this group
   const uint32_t gmask = group_mask(G, lane);
   const int64_t src = row_idx ? (int64_t)__ldg(row_idx + r) : r;
   const float4* x = reinterpret_cast<const float4*>(X + src * ldx);
@@ -66,31 +67,38 @@ static int quant_chunk_slots(int F) { return 32 * ((F + 127) / 128) > (F + 3) / 
 template <int G, int CPL>
 static void launch_qp(const float* X, int64_t ldx, int F, const int32_t* row_idx, int64_t n_rows,
                       const uint8_t* bits, const int64_t* off, uint32_t seed, uint8_t* packed,
-                      float2* meta, cudaStream_t st) {
+                      float2* meta, cudaStream_t st, int64_t r0) {
   const int64_t threads = n_rows * G;
   const int block = 256;
   const int64_t grid = (threads + block - 1) / block;
   quant_pack_kernel<G, CPL><<<(unsigned)grid, block, 0, st>>>(X, ldx, F, row_idx, n_rows, bits,
-                                                               off, seed, packed, meta);
+                                                               off, seed, packed, meta, r0);
 }
 
 gnn_status launch_quant_pack(const float* X, int64_t ldx, int F, const int32_t* row_idx,
                              int64_t n_rows, const uint8_t* bits, const int64_t* off,
                              uint32_t seed, uint8_t* packed, float2* meta, cudaStream_t st) {
+  return launch_quant_pack_range(X, ldx, F, row_idx, 0, n_rows, bits, off, seed, packed, meta, st);
+}
+
+gnn_status launch_quant_pack_range(const float* X, int64_t ldx, int F, const int32_t* row_idx,
+                                   int64_t r0, int64_t n_rows, const uint8_t* bits,
+                                   const int64_t* off, uint32_t seed, uint8_t* packed,
+                                   float2* meta, cudaStream_t st) {
   if (n_rows == 0) return GNN_OK;
   const int slots = quant_chunk_slots(F);
   if (slots <= 32) {
-    launch_qp<8, 4>(X, ldx, F, row_idx, n_rows, bits, off, seed, packed, meta, st);
+    launch_qp<8, 4>(X, ldx, F, row_idx, n_rows, bits, off, seed, packed, meta, st, r0);
   } else {
     switch ((slots + 31) / 32) {
-      case 1: launch_qp<32, 1>(X, ldx, F, row_idx, n_rows, bits, off, seed, packed, meta, st); break;
-      case 2: launch_qp<32, 2>(X, ldx, F, row_idx, n_rows, bits, off, seed, packed, meta, st); break;
-      case 3: launch_qp<32, 3>(X, ldx, F, row_idx, n_rows, bits, off, seed, packed, meta, st); break;
-      case 4: launch_qp<32, 4>(X, ldx, F, row_idx, n_rows, bits, off, seed, packed, meta, st); break;
-      case 5: launch_qp<32, 5>(X, ldx, F, row_idx, n_rows, bits, off, seed, packed, meta, st); break;
-      case 6: launch_qp<32, 6>(X, ldx, F, row_idx, n_rows, bits, off, seed, packed, meta, st); break;
-      case 7: launch_qp<32, 7>(X, ldx, F, row_idx, n_rows, bits, off, seed, packed, meta, st); break;
-      case 8: launch_qp<32, 8>(X, ldx, F, row_idx, n_rows, bits, off, seed, packed, meta, st); break;
+      case 1: launch_qp<32, 1>(X, ldx, F, row_idx, n_rows, bits, off, seed, packed, meta, st, r0); break;
+      case 2: launch_qp<32, 2>(X, ldx, F, row_idx, n_rows, bits, off, seed, packed, meta, st, r0); break;
+      case 3: launch_qp<32, 3>(X, ldx, F, row_idx, n_rows, bits, off, seed, packed, meta, st, r0); break;
+      case 4: launch_qp<32, 4>(X, ldx, F, row_idx, n_rows, bits, off, seed, packed, meta, st, r0); break;
+      case 5: launch_qp<32, 5>(X, ldx, F, row_idx, n_rows, bits, off, seed, packed, meta, st, r0); break;
+      case 6: launch_qp<32, 6>(X, ldx, F, row_idx, n_rows, bits, off, seed, packed, meta, st, r0); break;
+      case 7: launch_qp<32, 7>(X, ldx, F, row_idx, n_rows, bits, off, seed, packed, meta, st, r0); break;
+      case 8: launch_qp<32, 8>(X, ldx, F, row_idx, n_rows, bits, off, seed, packed, meta, st, r0); break;
       default: return fail(GNN_ERR_UNSUPPORTED, "quant_pack: F=%d exceeds %d", F, kMaxF);
     }
   }
@@ -135,6 +143,24 @@ extern "C" gnn_status gnn_quant_pack(const float* X, int64_t ldx, int32_t F, con
               "gnn_quant_pack: X and packed must be 16-byte aligned, meta 8-byte aligned");
   return launch_quant_pack(X, ldx, F, row_idx, n_rows, row_bits, row_off, seed, packed,
                            reinterpret_cast<float2*>(meta), as_stream(stream));
+}
+
+extern "C" gnn_status gnn_quant_pack_slots(const float* X, int64_t ldx, int32_t F,
+                                           const int32_t* slot_node, int64_t s0, int64_t s1,
+                                           const uint8_t* slot_bits, const int64_t* slot_off,
+                                           uint32_t seed, uint8_t* packed, float* meta,
+                                           gnn_stream_t stream) {
+  GNN_REQUIRE(s0 >= 0 && s1 >= s0, "gnn_quant_pack_slots: need 0 <= s0 <= s1");
+  GNN_REQUIRE(F >= 1, "gnn_quant_pack_slots: F must be >= 1");
+  if (F > kMaxF) return fail(GNN_ERR_UNSUPPORTED, "gnn_quant_pack_slots: F=%d > %d", F, kMaxF);
+  if (s1 == s0) return GNN_OK;
+  GNN_REQUIRE(X && slot_node && slot_bits && slot_off && packed && meta,
+              "gnn_quant_pack_slots: NULL pointer");
+  GNN_REQUIRE(ldx >= F && ldx % 4 == 0, "gnn_quant_pack_slots: ldx must be >= F and a multiple of 4");
+  GNN_REQUIRE(((uintptr_t)X & 15) == 0 && ((uintptr_t)packed & 15) == 0 && ((uintptr_t)meta & 7) == 0,
+              "gnn_quant_pack_slots: X and packed must be 16-byte aligned, meta 8-byte aligned");
+  return launch_quant_pack_range(X, ldx, F, slot_node, s0, s1 - s0, slot_bits, slot_off, seed,
+                                 packed, reinterpret_cast<float2*>(meta), as_stream(stream));
 }
 
 extern "C" gnn_status gnn_quant_divide(const float* a, const float* b, float* q, int64_t n,

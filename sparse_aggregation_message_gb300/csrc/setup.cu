@@ -520,10 +520,11 @@ extern "C" gnn_status gnn_csr_build(int32_t n, int64_t n_edges, const int32_t* s
   GNN_REQUIRE(ws, "gnn_csr_build: NULL workspace");
   const bool sym = flags & GNN_CSR_SYMMETRIZE, loops = flags & GNN_CSR_SELF_LOOPS;
   const int shift = bits_for((uint64_t)(n > 0 ? n : 1));
-  unsigned* dflags = device_flags();
-  if (!dflags) return fail(GNN_ERR_CUDA, "gnn_csr_build: device flag word unavailable");
+  // the build's own bad-endpoint flag lives in its workspace (count[3]), so
+  // a flag another kernel raised in the library-wide word is left for
+  // gnn_sync_check to report
+  unsigned* dflags = reinterpret_cast<unsigned*>(w.count + 3);
   GNN_CUDA(cudaMemsetAsync(w.count, 0, 4 * sizeof(unsigned long long), st));
-  GNN_CUDA(cudaMemsetAsync(dflags, 0, sizeof(unsigned), st));
   if (n_edges > 0)
     emit_edge_keys<<<GRID1(n_edges), 0, st>>>(n_edges, src, dst, n, shift, sym, loops, w.a,
                                               w.count, dflags);
@@ -537,11 +538,7 @@ extern "C" gnn_status gnn_csr_build(int32_t n, int64_t n_edges, const int32_t* s
   GNN_CUDA(cudaMemcpyAsync(&cnt, w.count, sizeof(cnt), cudaMemcpyDeviceToHost, st));
   GNN_CUDA(cudaMemcpyAsync(&bad, dflags, sizeof(bad), cudaMemcpyDeviceToHost, st));
   GNN_CUDA(cudaStreamSynchronize(st));
-  if (bad) {
-    const unsigned zero = 0;
-    GNN_CUDA(cudaMemcpy(dflags, &zero, sizeof(zero), cudaMemcpyHostToDevice));
-    return fail(GNN_ERR_INVALID_ARG, "gnn_csr_build: an edge endpoint is outside [0, n)");
-  }
+  if (bad) return fail(GNN_ERR_INVALID_ARG, "gnn_csr_build: an edge endpoint is outside [0, n)");
   const int64_t total = (int64_t)cnt + (loops ? n : 0);
   const int end_bit = 2 * shift;
   uint64_t* sorted = w.a;
@@ -813,6 +810,41 @@ extern "C" gnn_status gnn_boundary_long_slots_count(const gnn_boundary* bnd, int
                          as_stream(stream));
 }
 
+// Halo visiting order: key (first backward entry v) << 32 | s, sorted.
+__global__ void halo_key_kernel(int64_t S, const int64_t* __restrict__ srp,
+                                const int32_t* __restrict__ scol, uint64_t* __restrict__ key) {
+  const int64_t s = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (s >= S) return;
+  const int64_t b = srp[s];
+  const uint32_t v = b < srp[s + 1] ? (uint32_t)scol[b] : 0xffffffffu;
+  key[s] = ((uint64_t)v << 32) | (uint64_t)s;
+}
+
+__global__ void halo_order_kernel(int64_t S, const uint64_t* __restrict__ key,
+                                  int32_t* __restrict__ order) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < S) order[i] = (int32_t)(key[i] & 0xffffffffu);
+}
+
+static gnn_status halo_order_fill(const gnn_boundary& b, void* ws, size_t ws_bytes,
+                                  cudaStream_t st) {
+  const int64_t S = b.n_slots;
+  if (S == 0) return GNN_OK;
+  size_t t = 0;
+  GNN_CUDA(cub::DeviceRadixSort::SortKeys(nullptr, t, (uint64_t*)nullptr, (uint64_t*)nullptr, S, 0, 64));
+  Arena ar(ws, ws_bytes);
+  uint64_t* k0 = ar.take<uint64_t>((size_t)S);
+  uint64_t* k1 = ar.take<uint64_t>((size_t)S);
+  void* temp = ar.take_bytes(t);
+  if (!ar.ok()) return fail(GNN_ERR_INVALID_ARG, "halo order: workspace too small");
+  halo_key_kernel<<<GRID1(S), 0, st>>>(S, b.slot_rowptr, b.slot_col, k0);
+  GNN_CHECK_LAUNCH();
+  GNN_CUDA(cub::DeviceRadixSort::SortKeys(temp, t, k0, k1, S, 0, 64, st));
+  halo_order_kernel<<<GRID1(S), 0, st>>>(S, k1, b.halo_order);
+  GNN_CHECK_LAUNCH();
+  return GNN_OK;
+}
+
 extern "C" gnn_status gnn_boundary_long_slots(gnn_boundary* bnd, void* ws, size_t ws_bytes,
                                               gnn_stream_t stream) {
   GNN_REQUIRE(bnd && ws && bnd->long_slot_len >= 32 && bnd->slot_rowptr &&
@@ -830,5 +862,11 @@ extern "C" gnn_status gnn_boundary_long_slots(gnn_boundary* bnd, void* ws, size_
     GNN_CHECK_LAUNCH();
   }
   GNN_CUDA(cudaStreamSynchronize(st));
+  if (bnd->halo_order && bnd->n_slots > 0) {
+    if (bnd->nnz_cut > 0 && !bnd->slot_col)
+      return fail(GNN_ERR_INVALID_ARG, "gnn_boundary_long_slots: slot_col is NULL");
+    if ((s = halo_order_fill(*bnd, ws, ws_bytes, st)) != GNN_OK) return s;
+    GNN_CUDA(cudaStreamSynchronize(st));
+  }
   return GNN_OK;
 }

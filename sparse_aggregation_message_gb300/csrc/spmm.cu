@@ -15,6 +15,7 @@
 // cut into pieces of split_len entries.  Pieces run as their own groups at
 // the front of the grid and leave fp32 partial rows in the workspace; a fixup
 // kernel adds a row's pieces in piece order (deterministic) and writes it.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -45,6 +46,34 @@ struct RowSplit {
   const int64_t* piece_beg;
 };
 
+// Prefetch hints for the rows a batch will gather: each lane asks L2 for the
+// 128-byte lines of its own entry's byte range [lo, hi) as soon as the
+// batch's entry data arrive, so the later rounds of the batch (which load
+// only a few entries at a time) find their rows in L2 instead of waiting on
+// HBM one round after another.  0: off; 1: L2; 2: L1.
+#ifndef GNN_PF_REMOTE
+#define GNN_PF_REMOTE 0
+#endif
+#ifndef GNN_PF_LOCAL
+#define GNN_PF_LOCAL 0
+#endif
+#ifndef GNN_PF_HALO
+#define GNN_PF_HALO 0
+#endif
+
+template <int LEVEL>
+__device__ __forceinline__ void prefetch_lines(const void* base, uint32_t lo, uint32_t hi) {
+  if (LEVEL == 0 || hi <= lo) return;
+  const uintptr_t a0 = (reinterpret_cast<uintptr_t>(base) + lo) & ~uintptr_t(127);
+  const uintptr_t a1 = reinterpret_cast<uintptr_t>(base) + hi;
+  for (uintptr_t a = a0; a < a1; a += 128) {
+    if (LEVEL == 1)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+    else
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(a));
+  }
+}
+
 // acc += sum over local entries [beg, end) of val * H[col].  The group covers
 // chunks c0 + gl + i*G (i < CPL) below c_end.  One accumulator per chunk; U
 // entries are gathered before they are added, so U*CPL 16-byte loads per lane
@@ -61,6 +90,7 @@ __device__ __forceinline__ void gather_local(int64_t beg, int64_t end, const int
     if (e < end) {
       cc = __ldg(col + e);
       w = __ldg(val + e);
+      prefetch_lines<GNN_PF_LOCAL>(H4 + (int64_t)cc * ldh4, 16u * c0, 16u * c_end);
     }
     const int cnt = (int)min((int64_t)G, end - base);
     for (int k = 0; k < cnt; k += U) {
@@ -116,6 +146,10 @@ __device__ __forceinline__ void gather_remote(int64_t beg, int64_t end,
       sb = __ldg(msg.bits + s);
       so16 = (uint32_t)(__ldg(msg.off + s) >> 4);
       sm = __ldg(msg.meta + s);
+      // bytes of the row the group's chunks [c0, c_end) read
+      const uint32_t lo = sb == 32 ? 16u * c0 : ((uint32_t)(4 * c0 * sb) >> 5) << 2;
+      const uint32_t hi = sb == 32 ? 16u * c_end : (((uint32_t)(4 * c_end * sb) + 31u) >> 5) << 2;
+      prefetch_lines<GNN_PF_REMOTE>(msg.packed + ((size_t)so16 << 4), lo, hi);
     }
     const int cnt = (int)min((int64_t)G, end - base);
     for (int k = 0; k < cnt; k += UR) {
@@ -164,22 +198,195 @@ __device__ __forceinline__ void gather_remote(int64_t beg, int64_t end,
 #pragma unroll
       for (int u = 0; u < UR; ++u) {
         const int b = bk[u];
-        const uint32_t m = (1u << b) - 1u;
 #pragma unroll
         for (int i = 0; i < CPL; ++i) {
           const int c = c0 + gl + i * G;
           const uint32_t bits4 = wd[u][i] >> ((uint32_t)(4 * c * b) & 31u);
-          float4 x;
-          x.x = __fadd_rn(__fmul_rn(sck[u], (float)(bits4 & m)), mnk[u]);
-          x.y = __fadd_rn(__fmul_rn(sck[u], (float)((bits4 >> b) & m)), mnk[u]);
-          x.z = __fadd_rn(__fmul_rn(sck[u], (float)((bits4 >> (2 * b)) & m)), mnk[u]);
-          x.w = __fadd_rn(__fmul_rn(sck[u], (float)((bits4 >> (3 * b)) & m)), mnk[u]);
-          fma4(acc[i], wk[u], x);
+          fma4(acc[i], wk[u], dequant4(bits4, b, mnk[u], sck[u]));
         }
       }
     }
   }
 }
+
+// The same sum with the round split in two phases: first the packed words of
+// UR entries are requested (each entry's width and offset taken from its
+// lane by shuffle), then each entry's weight, width and meta are taken again
+// and its words decoded.  Only the words are held across the phase, so far
+// more entries are in flight per lane than when every entry's five values
+// are kept (latency of the random message reads is what bounds this loop
+// when most sources are remote).
+template <int G, int CPL, int UR, bool OWNED = false>
+__device__ __forceinline__ void gather_remote_split(int64_t beg, int64_t end,
+                                                    const int32_t* __restrict__ col,
+                                                    const float* __restrict__ val, int c0,
+                                                    int c_end, const SlotMsgs& msg, int gl,
+                                                    uint32_t gmask, float4 (&acc)[CPL]) {
+  for (int64_t base = beg; base < end; base += G) {
+    const int64_t e = base + gl;
+    float w = 0.f;
+    int sb = 0;
+    uint32_t so16 = 0;
+    float2 sm = make_float2(0.f, 0.f);
+    if (e < end) {
+      const int s = OWNED ? __ldg(col + e) : ~__ldg(col + e);
+      w = OWNED ? 1.f : __ldg(val + e);
+      sb = __ldg(msg.bits + s);
+      so16 = (uint32_t)(__ldg(msg.off + s) >> 4);
+      sm = __ldg(msg.meta + s);
+      const uint32_t lo = sb == 32 ? 16u * c0 : ((uint32_t)(4 * c0 * sb) >> 5) << 2;
+      const uint32_t hi = sb == 32 ? 16u * c_end : (((uint32_t)(4 * c_end * sb) + 31u) >> 5) << 2;
+      prefetch_lines<GNN_PF_REMOTE>(msg.packed + ((size_t)so16 << 4), lo, hi);
+    }
+    const int cnt = (int)min((int64_t)G, end - base);
+    for (int k = 0; k < cnt; k += UR) {
+      uint32_t wd[UR][CPL];
+      bool raw = false;
+#pragma unroll
+      for (int u = 0; u < UR; ++u) {
+        const bool valid = k + u < cnt;
+        const int src = valid ? k + u : k;
+        const int b = __shfl_sync(gmask, sb, src, G);
+        const uint32_t o16 = __shfl_sync(gmask, so16, src, G);
+        raw |= valid && b == 32;
+        const uint32_t* rowp = reinterpret_cast<const uint32_t*>(msg.packed + ((size_t)o16 << 4));
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) {
+          const int c = c0 + gl + i * G;
+          wd[u][i] = 0u;
+          if (valid && c < c_end && b != 32) wd[u][i] = __ldg(rowp + ((uint32_t)(4 * c * b) >> 5));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < UR; ++u) {
+        const bool valid = k + u < cnt;
+        const int src = valid ? k + u : k;
+        const float wk = valid ? __shfl_sync(gmask, w, src, G) : 0.f;
+        const int b = __shfl_sync(gmask, sb, src, G);
+        const float mn = __shfl_sync(gmask, sm.x, src, G);
+        const float sc = __shfl_sync(gmask, sm.y, src, G);
+        if (b == 32) continue;  // raw rows: below
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) {
+          const int c = c0 + gl + i * G;
+          const uint32_t bits4 = wd[u][i] >> ((uint32_t)(4 * c * b) & 31u);
+          fma4(acc[i], wk, dequant4(bits4, b, mn, sc));
+        }
+      }
+      if (raw) {  // fp32 pass-through rows (width 32), read as float4 chunks
+#pragma unroll
+        for (int u = 0; u < UR; ++u) {
+          const bool valid = k + u < cnt;
+          const int src = valid ? k + u : k;
+          const float wk = __shfl_sync(gmask, w, src, G);
+          const int b = __shfl_sync(gmask, sb, src, G);
+          const uint32_t o16 = __shfl_sync(gmask, so16, src, G);
+          if (!valid || b != 32) continue;
+#pragma unroll
+          for (int i = 0; i < CPL; ++i) {
+            const int c = c0 + gl + i * G;
+            if (c < c_end) fma4(acc[i], wk, dequant_chunk(msg.packed + ((size_t)o16 << 4), 32, 0.f, 0.f, c));
+          }
+        }
+      }
+    }
+  }
+}
+
+// The same sum with each batch's per-entry values -- (slot offset, weight,
+// min, scale) and the width -- staged in shared memory instead of held in
+// registers and broadcast by shuffles: a round then requests the packed words
+// of UR entries (reading each entry's offset and width back with broadcast
+// shared loads), and decodes them after all UR requests are in flight.  Only
+// the words stay in registers across the round, so UR can be large.
+// rec/recb: this warp's 32 records (index = lane).
+template <int G, int CPL, int UR, bool OWNED = false>
+__device__ __forceinline__ void gather_remote_smem(int64_t beg, int64_t end,
+                                                   const int32_t* __restrict__ col,
+                                                   const float* __restrict__ val, int c0,
+                                                   int c_end, const SlotMsgs& msg, int gl,
+                                                   uint32_t gmask, float4 (&acc)[CPL],
+                                                   uint4* rec, int* recb) {
+  const int lane = threadIdx.x & 31;
+  const int g0 = lane & ~(G - 1);  // the group's first record
+  for (int64_t base = beg; base < end; base += G) {
+    const int64_t e = base + gl;
+    if (e < end) {
+      const int s = OWNED ? __ldg(col + e) : ~__ldg(col + e);
+      const float w = OWNED ? 1.f : __ldg(val + e);
+      const int sb = __ldg(msg.bits + s);
+      const uint32_t so16 = (uint32_t)(__ldg(msg.off + s) >> 4);
+      const float2 sm = __ldg(msg.meta + s);
+      rec[lane] = make_uint4(so16, __float_as_uint(w), __float_as_uint(sm.x), __float_as_uint(sm.y));
+      recb[lane] = sb;
+    }
+    __syncwarp(gmask);
+    const int cnt = (int)min((int64_t)G, end - base);
+    for (int k = 0; k < cnt; k += UR) {
+      uint32_t wd[UR][CPL];
+      int bk[UR];
+      bool raw = false;
+#pragma unroll
+      for (int u = 0; u < UR; ++u) {
+        const bool valid = k + u < cnt;
+        const int idx = g0 + (valid ? k + u : k);
+        const int b = recb[idx];
+        bk[u] = b;
+        raw |= valid && b == 32;
+        const uint32_t* rowp =
+            reinterpret_cast<const uint32_t*>(msg.packed + ((size_t)rec[idx].x << 4));
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) {
+          const int c = c0 + gl + i * G;
+          wd[u][i] = 0u;
+          if (valid && c < c_end && b != 32) wd[u][i] = __ldg(rowp + ((uint32_t)(4 * c * b) >> 5));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < UR; ++u) {
+        const bool valid = k + u < cnt;
+        const uint4 r = rec[g0 + (valid ? k + u : k)];
+        const float wk = valid ? __uint_as_float(r.y) : 0.f;
+        const int b = bk[u];
+        if (b == 32) continue;  // raw rows: below
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) {
+          const int c = c0 + gl + i * G;
+          const uint32_t bits4 = wd[u][i] >> ((uint32_t)(4 * c * b) & 31u);
+          fma4(acc[i], wk, dequant4(bits4, b, __uint_as_float(r.z), __uint_as_float(r.w)));
+        }
+      }
+      if (raw) {  // fp32 pass-through rows (width 32), read as float4 chunks
+#pragma unroll
+        for (int u = 0; u < UR; ++u) {
+          if (k + u >= cnt || bk[u] != 32) continue;
+          const uint4 r = rec[g0 + k + u];
+#pragma unroll
+          for (int i = 0; i < CPL; ++i) {
+            const int c = c0 + gl + i * G;
+            if (c < c_end)
+              fma4(acc[i], __uint_as_float(r.y),
+                   dequant_chunk(msg.packed + ((size_t)r.x << 4), 32, 0.f, 0.f, c));
+          }
+        }
+      }
+    }
+    __syncwarp(gmask);  // every lane is done with this batch's records
+  }
+}
+
+#ifndef GNN_REMOTE_SPLIT
+#define GNN_REMOTE_SPLIT 0
+#endif
+#ifndef GNN_REMOTE_SMEM
+#define GNN_REMOTE_SMEM 0
+#endif
+#ifndef GNN_REMOTE_SMEM_UR
+#define GNN_REMOTE_SMEM_UR 8
+#endif
+#ifndef GNN_REMOTE_SPLIT_UR
+#define GNN_REMOTE_SPLIT_UR 8
+#endif
 
 // acc += dequantised messages of the slots row r owns (backward), in the
 // owner list's order; the slots' widths, offsets and meta are loaded for G
@@ -331,8 +538,20 @@ __global__ void __launch_bounds__(rows_block<MODE>(), ((MODE == 1 && CPL == 3) ?
   const int64_t mid =
       MODE == kPlain ? end : (piece ? __ldg(rowptr + row) : beg) + __ldg(local_cnt + row);
   gather_local<G, CPL, U>(beg, min(end, mid), col, val, H4, ldh4, c0, min(c1, nch), gl, gmask, acc);
-  if constexpr (MODE == kFwdRemote)
-    gather_remote<G, CPL, UR>(max(beg, mid), end, col, val, c0, min(c1, nch), msg, gl, gmask, acc);
+  if constexpr (MODE == kFwdRemote) {
+    if (GNN_REMOTE_SMEM) {
+      __shared__ uint4 srec[rows_block<MODE>()];
+      __shared__ int sbits[rows_block<MODE>()];
+      gather_remote_smem<G, CPL, GNN_REMOTE_SMEM_UR>(max(beg, mid), end, col, val, c0,
+                                                     min(c1, nch), msg, gl, gmask, acc,
+                                                     srec + (threadIdx.x & ~31),
+                                                     sbits + (threadIdx.x & ~31));
+    } else if (GNN_REMOTE_SPLIT)
+      gather_remote_split<G, CPL, GNN_REMOTE_SPLIT_UR>(max(beg, mid), end, col, val, c0,
+                                                        min(c1, nch), msg, gl, gmask, acc);
+    else
+      gather_remote<G, CPL, UR>(max(beg, mid), end, col, val, c0, min(c1, nch), msg, gl, gmask, acc);
+  }
   if (piece) {
     float4* prow = reinterpret_cast<float4*>(partial) + unit * nch;
 #pragma unroll
@@ -412,14 +631,125 @@ __device__ __forceinline__ void add_score_term(float4& p, float r, const float* 
 // so the result is the same as one sequential loop.  Rows of up to three
 // chunks per lane keep 64 registers (four blocks per SM: the loads of a slot
 // are few and short, so more slots in flight pay more than deeper unrolling).
-template <int G, int CPL, int U>
+// Ordinary slots, HK > 1: each group of G lanes walks HK consecutive slots of
+// the visiting order.  The bounds of all HK slots are read at once, and the
+// first batch of the next slot's entries is requested before the current
+// slot is quantised, so only the row gathers are left on each slot's chain
+// of dependent loads.  Every slot's sum keeps its fixed order.
+template <int G, int CPL, int U, int HK>
+__device__ __forceinline__ void halo_group_slots(
+    int64_t block, const int64_t* __restrict__ srp, const int32_t* __restrict__ scol,
+    const float* __restrict__ sval, const float4* __restrict__ G4, int64_t ldg4, int F,
+    const uint8_t* __restrict__ slot_bits, const int64_t* __restrict__ slot_off, uint32_t seed,
+    uint8_t* __restrict__ packed, float2* __restrict__ meta, int long_len,
+    const float* __restrict__ score_r, const float* __restrict__ a_r,
+    const int32_t* __restrict__ order, int64_t s_lo, int64_t s_hi) {
+  const int lane = threadIdx.x & 31;
+  const int gl = lane & (G - 1);
+  const uint32_t gmask = group_mask(G, lane);
+  const int nch = (F + 3) >> 2;
+  const int64_t count = s_hi - s_lo;
+  const int64_t i0 = ((block * blockDim.x + threadIdx.x) / G) * HK;
+  if (i0 >= count) return;  // uniform across the group
+  long long my_s = 0, my_b = 0, my_e = 0;
+  if (gl < HK && i0 + gl < count) {
+    my_s = order ? (long long)__ldg(order + i0 + gl) : (long long)(s_lo + i0 + gl);
+    my_b = __ldg(srp + my_s);
+    my_e = __ldg(srp + my_s + 1);
+  }
+  // the first entry batch of the group's first slot
+  int v_next = 0;
+  float w_next = 0.f;
+  {
+    const int64_t b0 = __shfl_sync(gmask, my_b, 0, G), e0 = __shfl_sync(gmask, my_e, 0, G);
+    if (b0 + gl < e0) {
+      v_next = __ldg(scol + b0 + gl);
+      w_next = __ldg(sval + b0 + gl);
+    }
+  }
+#pragma unroll 1
+  for (int j = 0; j < HK; ++j) {
+    if (i0 + j >= count) break;  // uniform
+    const int64_t s = __shfl_sync(gmask, my_s, j, G);
+    const int64_t beg = __shfl_sync(gmask, my_b, j, G), end = __shfl_sync(gmask, my_e, j, G);
+    const bool skip = long_len > 0 && end - beg > long_len;  // summed by a long-slot block
+    float4 acc[CPL];
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (!skip) {
+      for (int64_t base = beg; base < end; base += G) {
+        const int64_t e = base + gl;
+        int v = v_next;
+        float w = w_next;
+        if (base != beg) {
+          v = 0;
+          w = 0.f;
+          if (e < end) {
+            v = __ldg(scol + e);
+            w = __ldg(sval + e);
+          }
+        }
+        const int cnt = (int)min((int64_t)G, end - base);
+        for (int k = 0; k < cnt; k += U) {
+          float4 x[U][CPL];
+          float wk[U];
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const int src = (k + u < cnt) ? k + u : k;
+            const int vk = __shfl_sync(gmask, v, src, G);
+            wk[u] = __shfl_sync(gmask, w, src, G);
+#pragma unroll
+            for (int i = 0; i < CPL; ++i) {
+              const int c = gl + i * G;
+              if (c < nch) x[u][i] = __ldg(G4 + (int64_t)vk * ldg4 + c);
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            if (k + u < cnt) {
+#pragma unroll
+              for (int i = 0; i < CPL; ++i) {
+                if (gl + i * G < nch) mul_add4(acc[i], wk[u], x[u][i]);
+              }
+            }
+          }
+        }
+      }
+    }
+    // the next slot's first entry batch, requested before this slot is quantised
+    v_next = 0;
+    w_next = 0.f;
+    if (j + 1 < HK && i0 + j + 1 < count) {
+      const int64_t nb = __shfl_sync(gmask, my_b, j + 1, G), ne = __shfl_sync(gmask, my_e, j + 1, G);
+      if (nb + gl < ne) {
+        v_next = __ldg(scol + nb + gl);
+        w_next = __ldg(sval + nb + gl);
+      }
+    }
+    if (skip) continue;
+    if (score_r) {
+      const float r = __ldg(score_r + s);
+#pragma unroll
+      for (int i = 0; i < CPL; ++i)
+        if (gl + i * G < nch) add_score_term(acc[i], r, a_r, gl + i * G, F);
+    }
+    quantize_pack_row<G, CPL>(acc, F, __ldg(slot_bits + s), row_key(seed, (uint32_t)s),
+                              packed + __ldg(slot_off + s), meta + s, gl, gmask);
+  }
+}
+
+#ifndef GNN_HALO_MULTI
+#define GNN_HALO_MULTI 1
+#endif
+
+template <int G, int CPL, int U, int HK = GNN_HALO_MULTI>
 __global__ void __launch_bounds__(256, (G == 32 && CPL <= 3) ? 4 : 1) halo_quant_pack_kernel(
     int64_t S, const int64_t* __restrict__ srp, const int32_t* __restrict__ scol,
     const float* __restrict__ sval, const float* __restrict__ Gm, int64_t ldg, int F,
     const uint8_t* __restrict__ slot_bits, const int64_t* __restrict__ slot_off, uint32_t seed,
     uint8_t* __restrict__ packed, float2* __restrict__ meta, int n_long,
     const int32_t* __restrict__ long_slots, int long_len, int E, const float* __restrict__ score_r,
-    const float* __restrict__ a_r) {
+    const float* __restrict__ a_r, const int32_t* __restrict__ order, int64_t s_lo, int64_t s_hi) {
   constexpr int CPLQ = (G * CPL + 31) / 32;  // chunks per lane when one warp quantises
   extern __shared__ float4 tile[];
   const int lane = threadIdx.x & 31;
@@ -431,6 +761,7 @@ __global__ void __launch_bounds__(256, (G == 32 && CPL <= 3) ? 4 : 1) halo_quant
     __shared__ int sv[32];
     __shared__ float sw[32];
     const int64_t s = __ldg(long_slots + blockIdx.x);
+    if (s < s_lo || s >= s_hi) return;  // outside the requested slot range (block-uniform)
     const int64_t beg = __ldg(srp + s), end = __ldg(srp + s + 1);
     const int t = threadIdx.x;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -447,14 +778,7 @@ __global__ void __launch_bounds__(256, (G == 32 && CPL <= 3) ? 4 : 1) halo_quant
       }
       __syncthreads();
       if (t < nch) {
-        for (int e = 0; e < cnt; ++e) {
-          const float4 x = tile[e * nch + t];
-          const float w = sw[e];
-          acc.x = __fadd_rn(acc.x, __fmul_rn(w, x.x));
-          acc.y = __fadd_rn(acc.y, __fmul_rn(w, x.y));
-          acc.z = __fadd_rn(acc.z, __fmul_rn(w, x.z));
-          acc.w = __fadd_rn(acc.w, __fmul_rn(w, x.w));
-        }
+        for (int e = 0; e < cnt; ++e) mul_add4(acc, sw[e], tile[e * nch + t]);
       }
       __syncthreads();
     }
@@ -477,8 +801,16 @@ __global__ void __launch_bounds__(256, (G == 32 && CPL <= 3) ? 4 : 1) halo_quant
   }
 
   const int gl = lane & (G - 1);
-  const int64_t s = ((int64_t)(blockIdx.x - n_long) * blockDim.x + threadIdx.x) / G;
-  if (s >= S) return;
+  if constexpr (HK > 1) {
+    halo_group_slots<G, CPL, U, HK>(blockIdx.x - n_long, srp, scol, sval, G4, ldg4, F, slot_bits,
+                                    slot_off, seed, packed, meta, long_len, score_r, a_r, order,
+                                    s_lo, s_hi);
+    return;
+  }
+  const int64_t i = ((int64_t)(blockIdx.x - n_long) * blockDim.x + threadIdx.x) / G;
+  if (i >= s_hi - s_lo) return;
+  // visiting order (no effect on results), or the slots of [s_lo, s_hi) in turn
+  const int64_t s = order ? (int64_t)__ldg(order + i) : s_lo + i;
   const int64_t beg = __ldg(srp + s), end = __ldg(srp + s + 1);
   if (long_len > 0 && end - beg > long_len) return;  // summed by a long-slot block
   const uint32_t gmask = group_mask(G, lane);
@@ -492,6 +824,7 @@ __global__ void __launch_bounds__(256, (G == 32 && CPL <= 3) ? 4 : 1) halo_quant
     if (e < end) {
       v = __ldg(scol + e);
       w = __ldg(sval + e);
+      prefetch_lines<GNN_PF_HALO>(G4 + (int64_t)v * ldg4, 0u, 16u * nch);
     }
     const int cnt = (int)min((int64_t)G, end - base);
     for (int k = 0; k < cnt; k += U) {
@@ -513,12 +846,7 @@ __global__ void __launch_bounds__(256, (G == 32 && CPL <= 3) ? 4 : 1) halo_quant
         if (k + u < cnt) {
 #pragma unroll
           for (int i = 0; i < CPL; ++i) {
-            if (gl + i * G < nch) {
-              acc[i].x = __fadd_rn(acc[i].x, __fmul_rn(wk[u], x[u][i].x));
-              acc[i].y = __fadd_rn(acc[i].y, __fmul_rn(wk[u], x[u][i].y));
-              acc[i].z = __fadd_rn(acc[i].z, __fmul_rn(wk[u], x[u][i].z));
-              acc[i].w = __fadd_rn(acc[i].w, __fmul_rn(wk[u], x[u][i].w));
-            }
+            if (gl + i * G < nch) mul_add4(acc[i], wk[u], x[u][i]);
           }
         }
       }
@@ -687,9 +1015,13 @@ gnn_status launch_halo_quant_pack(const gnn_boundary& b, const float* Gm, int64_
 gnn_status launch_halo_quant_pack_ex(const gnn_boundary& b, const float* Gm, int64_t ldg, int F,
                                      uint32_t seed, uint8_t* packed_ws, float2* meta_ws,
                                      const float* sval, const float* score_r, const float* a_r,
-                                     cudaStream_t st) {
+                                     cudaStream_t st, int64_t s_lo, int64_t s_hi) {
   const int64_t S = b.n_slots;
-  if (S == 0) return GNN_OK;
+  if (s_hi < 0) s_hi = S;
+  if (S == 0 || s_hi <= s_lo) return GNN_OK;
+  // the visiting order covers every slot: a partial range walks its slots in turn
+  const int32_t* order = (s_lo == 0 && s_hi == S) ? b.halo_order : nullptr;
+  const int64_t count = s_hi - s_lo;
   const int slots = quant_chunk_slots(F);
   const int nch = (F + 3) / 4;
   const int block = 256;
@@ -705,10 +1037,10 @@ gnn_status launch_halo_quant_pack_ex(const gnn_boundary& b, const float* Gm, int
   const size_t dyn = smem > smem_q ? smem : (use_long ? smem_q : 0);
 #define GNN_HALO(G_, CPL_, U_)                                                                   \
   do {                                                                                           \
-    const int64_t grid = n_long + (S * G_ + block - 1) / block;                                  \
+    const int64_t grid = n_long + (((count + GNN_HALO_MULTI - 1) / GNN_HALO_MULTI) * G_ + block - 1) / block; \
     halo_quant_pack_kernel<G_, CPL_, U_><<<(unsigned)grid, block, dyn, st>>>(                    \
         S, b.slot_rowptr, b.slot_col, sval, Gm, ldg, F, b.slot_bits, b.slot_off, seed,           \
-        packed_ws, meta_ws, n_long, b.long_slots, long_len, E, score_r, a_r);                    \
+        packed_ws, meta_ws, n_long, b.long_slots, long_len, E, score_r, a_r, order, s_lo, s_hi); \
   } while (0)
   if (slots <= 32) GNN_HALO(8, 4, 2);
   else {
@@ -953,21 +1285,48 @@ constexpr int kNoAllocMaxDevices = 64;
 static __device__ __align__(256) float g_noalloc_partials[kNoAllocScratchBytes / sizeof(float)];
 std::mutex g_noalloc_mu;
 float* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+CUcontext g_noalloc_ctx[kNoAllocMaxDevices] = {};
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+// The driver's cuCtxGetCurrent, fetched once through the runtime (the
+// library links no driver library).
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPoint("cuCtxGetCurrent", &p, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  return fn;
+}
 }  // namespace
 
 // Device address of the array on the current device.  Host code only knows a
-// host-side stand-in for the symbol, so the address is looked up once per
-// device (with that device current) and cached.
+// host-side stand-in for the symbol, so the address is looked up with that
+// device current and cached together with the context it was found in: a
+// new context on the device (after cudaDeviceReset, or once the primary
+// context was released and created again) is seen and the address looked up
+// afresh, so a stale address from a dead context is never used.
 static gnn_status noalloc_scratch(float** out) {
   int dev = 0;
   GNN_CUDA(cudaGetDevice(&dev));
   if (dev < 0 || dev >= kNoAllocMaxDevices)
     return fail(GNN_ERR_UNSUPPORTED, "gnn_spmm_fwd_noalloc: device %d out of range", dev);
+  GNN_CUDA(cudaSetDevice(dev));  // makes the device's primary context current on this thread
+  CUcontext ctx = nullptr;
+  CtxGetCurrentFn get = ctx_get_current();
+  if (!get || get(&ctx) != CUDA_SUCCESS)
+    return fail(GNN_ERR_CUDA, "gnn_spmm_fwd_noalloc: cannot read the current context");
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
+  if (!g_noalloc_ptr[dev] || g_noalloc_ctx[dev] != ctx) {
     void* p = nullptr;
     GNN_CUDA(cudaGetSymbolAddress(&p, g_noalloc_partials));
     g_noalloc_ptr[dev] = static_cast<float*>(p);
+    g_noalloc_ctx[dev] = ctx;
   }
   *out = g_noalloc_ptr[dev];
   return GNN_OK;
@@ -1027,6 +1386,33 @@ extern "C" gnn_status gnn_halo_quant_pack(const gnn_boundary* bnd, const float* 
               "gnn_halo_quant_pack: packed (16-byte aligned) and meta required");
   return launch_halo_quant_pack(*bnd, G, ldg, F, seed, packed, reinterpret_cast<float2*>(meta),
                                 as_stream(stream));
+}
+
+extern "C" gnn_status gnn_halo_quant_pack_slots(const gnn_boundary* bnd, const float* G,
+                                                int64_t ldg, int32_t F, int64_t s0, int64_t s1,
+                                                uint32_t seed, uint8_t* packed, float* meta,
+                                                gnn_stream_t stream) {
+  GNN_REQUIRE(bnd, "gnn_halo_quant_pack_slots: boundary is NULL");
+  GNN_REQUIRE(s0 >= 0 && s0 <= s1 && s1 <= bnd->n_slots,
+              "gnn_halo_quant_pack_slots: need 0 <= s0 <= s1 <= n_slots");
+  GNN_REQUIRE(F >= 1, "gnn_halo_quant_pack_slots: F must be >= 1");
+  if (F > kMaxF) return fail(GNN_ERR_UNSUPPORTED, "gnn_halo_quant_pack_slots: F=%d > %d", F, kMaxF);
+  GNN_REQUIRE(bnd->F == F, "gnn_halo_quant_pack_slots: boundary offsets are for F=%d, call has F=%d",
+              bnd->F, F);
+  if (s1 == s0) return GNN_OK;
+  GNN_REQUIRE(bnd->slot_rowptr && bnd->slot_bits && bnd->slot_off &&
+                  (bnd->nnz_cut == 0 || (bnd->slot_col && bnd->slot_val)),
+              "gnn_halo_quant_pack_slots: boundary arrays are NULL");
+  GNN_REQUIRE(bnd->long_slot_len == 0 ||
+                  (bnd->long_slot_len >= 32 && bnd->n_long_slots >= 0 &&
+                   (bnd->n_long_slots == 0 || bnd->long_slots)),
+              "gnn_halo_quant_pack_slots: incomplete long-slot list");
+  GNN_REQUIRE(G && ldg >= F && ldg % 4 == 0 && ((uintptr_t)G & 15) == 0,
+              "gnn_halo_quant_pack_slots: ldg must be >= F, a multiple of 4, G 16-byte aligned");
+  GNN_REQUIRE(packed && meta && ((uintptr_t)packed & 15) == 0 && ((uintptr_t)meta & 7) == 0,
+              "gnn_halo_quant_pack_slots: packed (16-byte aligned) and meta required");
+  return launch_halo_quant_pack_ex(*bnd, G, ldg, F, seed, packed, reinterpret_cast<float2*>(meta),
+                                   bnd->slot_val, nullptr, nullptr, as_stream(stream), s0, s1);
 }
 
 extern "C" gnn_status gnn_spmm_bwd_local(const gnn_csr* csr, const gnn_boundary* bnd,

@@ -43,7 +43,10 @@ extern "C" unsigned long long gnn_kernel_launches(void) {
 }
 
 extern "C" gnn_status gnn_sync_check(gnn_stream_t stream) {
+  // every stream: a flag may come from a kernel on a second stream (the
+  // asynchronous layers' aux stream)
   GNN_CUDA(cudaStreamSynchronize(gnn::as_stream(stream)));
+  GNN_CUDA(cudaDeviceSynchronize());
   unsigned flags = 0;
   GNN_CUDA(cudaMemcpyFromSymbol(&flags, gnn::g_device_flags, sizeof(flags)));
   if (flags) {
