@@ -8,29 +8,63 @@
 
 namespace gnn {
 
+// Rows per group: a group walks QK consecutive rows and loads the next row
+// (and its width and offset) before it quantises the current one, so the
+// row's HBM latency overlaps the quantiser's arithmetic.
+#ifndef GNN_QUANT_ROWS
+#define GNN_QUANT_ROWS 1
+#endif
+
 template <int G, int CPL>
+__device__ __forceinline__ void load_row(const float* __restrict__ X, int64_t ldx,
+                                         const int32_t* __restrict__ row_idx, int64_t r, int nch,
+                                         int gl, float4 (&v)[CPL]) {
+  const int64_t src = row_idx ? (int64_t)__ldg(row_idx + r) : r;
+  const float4* x = reinterpret_cast<const float4*>(X + src * ldx);
+#pragma unroll
+  for (int i = 0; i < CPL; ++i) {
+    const int c = gl + i * G;
+    v[i] = c < nch ? __ldg(x + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+template <int G, int CPL, int QK = GNN_QUANT_ROWS>
 __global__ void __launch_bounds__(256) quant_pack_kernel(
     const float* __restrict__ X, int64_t ldx, int F, const int32_t* __restrict__ row_idx,
     int64_t n_rows, const uint8_t* __restrict__ row_bits, const int64_t* __restrict__ row_off,
     uint32_t seed, uint8_t* __restrict__ packed, float2* __restrict__ meta, int64_t r0) {
   const int lane = threadIdx.x & 31;
   const int gl = lane & (G - 1);
-  const int64_t idx = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / G;
-  if (idx >= n_rows) return;  // uniform across the group
-  const int64_t r = r0 + idx;  // row (and row key) of this group
+  const int64_t i0 = (((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / G) * QK;
+  if (i0 >= n_rows) return;  // uniform across the group
   const uint32_t gmask = group_mask(G, lane);
-  const int64_t src = row_idx ? (int64_t)__ldg(row_idx + r) : r;
-  const float4* x = reinterpret_cast<const float4*>(X + src * ldx);
   const int nch = (F + 3) >> 2;
   float4 v[CPL];
+  load_row<G, CPL>(X, ldx, row_idx, r0 + i0, nch, gl, v);
+  int b = __ldg(row_bits + r0 + i0);
+  int64_t off = __ldg(row_off + r0 + i0);
+#pragma unroll 1
+  for (int j = 0; j < QK; ++j) {
+    const int64_t idx = i0 + j;
+    if (idx >= n_rows) break;  // uniform
+    const int64_t r = r0 + idx;  // row (and row key) of this step
+    float4 nv[CPL];
+    int nb = 0;
+    int64_t noff = 0;
+    if (QK > 1 && j + 1 < QK && idx + 1 < n_rows) {
+      load_row<G, CPL>(X, ldx, row_idx, r + 1, nch, gl, nv);
+      nb = __ldg(row_bits + r + 1);
+      noff = __ldg(row_off + r + 1);
+    }
+    quantize_pack_row<G, CPL>(v, F, b, row_key(seed, (uint32_t)r), packed + off, meta + r, gl,
+                              gmask);
+    if (QK > 1) {
 #pragma unroll
-  for (int i = 0; i < CPL; ++i) {
-    const int c = gl + i * G;
-    v[i] = c < nch ? __ldg(x + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int i = 0; i < CPL; ++i) v[i] = nv[i];
+      b = nb;
+      off = noff;
+    }
   }
-  const int b = __ldg(row_bits + r);
-  quantize_pack_row<G, CPL>(v, F, b, row_key(seed, (uint32_t)r), packed + __ldg(row_off + r),
-                            meta + r, gl, gmask);
 }
 
 template <int G>
@@ -68,7 +102,7 @@ template <int G, int CPL>
 static void launch_qp(const float* X, int64_t ldx, int F, const int32_t* row_idx, int64_t n_rows,
                       const uint8_t* bits, const int64_t* off, uint32_t seed, uint8_t* packed,
                       float2* meta, cudaStream_t st, int64_t r0) {
-  const int64_t threads = n_rows * G;
+  const int64_t threads = ((n_rows + GNN_QUANT_ROWS - 1) / GNN_QUANT_ROWS) * G;
   const int block = 256;
   const int64_t grid = (threads + block - 1) / block;
   quant_pack_kernel<G, CPL><<<(unsigned)grid, block, 0, st>>>(X, ldx, F, row_idx, n_rows, bits,

@@ -379,10 +379,10 @@ __device__ __forceinline__ void gather_remote_smem(int64_t beg, int64_t end,
 #define GNN_REMOTE_SPLIT 0
 #endif
 #ifndef GNN_REMOTE_SMEM
-#define GNN_REMOTE_SMEM 0
+#define GNN_REMOTE_SMEM 1
 #endif
 #ifndef GNN_REMOTE_SMEM_UR
-#define GNN_REMOTE_SMEM_UR 8
+#define GNN_REMOTE_SMEM_UR 4
 #endif
 #ifndef GNN_REMOTE_SPLIT_UR
 #define GNN_REMOTE_SPLIT_UR 8
@@ -495,6 +495,64 @@ constexpr int rows_block() {
 #define GNN_SLICE_CHUNKS 96
 #endif
 
+// Rows per group for the kernels with messages when a row is one slice: a
+// group walks RK consecutive rows, their bounds read at once (lane k: row k),
+// so no row waits on its own bounds.
+#ifndef GNN_ROWS_MULTI
+#define GNN_ROWS_MULTI 8
+#endif
+
+template <int G, int CPL, int MODE, int U, int UR, int RK>
+__device__ __forceinline__ void rows_group(
+    int64_t grp, int n, const int64_t* __restrict__ rowptr, const int32_t* __restrict__ col,
+    const float* __restrict__ val, const int32_t* __restrict__ local_cnt,
+    const float4* __restrict__ H4, int64_t ldh4, int F, int nch, const SlotMsgs& msg,
+    const int64_t* __restrict__ own_ptr, const int32_t* __restrict__ own_slot, const RowSplit& sp,
+    int c0, int c1, float* __restrict__ M, int64_t ldm, __nv_bfloat16* __restrict__ Mb,
+    int64_t ldmb, int nch_b, int relu, const float* __restrict__ hmask, int64_t ldhm, int gl,
+    uint32_t gmask, uint4* rec, int* recb) {
+  const int64_t row0 = grp * RK;
+  if (row0 >= n) return;  // uniform across the group
+  long long my_b = 0, my_e = 0;
+  int my_lc = 0;
+  auto load_bounds = [&](int64_t first) {
+    my_b = my_e = 0;
+    my_lc = 0;
+    if (first + gl < n && first + gl < row0 + RK) {
+      my_b = __ldg(rowptr + first + gl);
+      my_e = __ldg(rowptr + first + gl + 1);
+      my_lc = __ldg(local_cnt + first + gl);
+    }
+  };
+  load_bounds(row0);
+#pragma unroll 1
+  for (int j = 0; j < RK; ++j) {
+    const int64_t row = row0 + j;
+    if (row >= n) break;  // uniform
+    const int jj = j % G;
+    if (j > 0 && jj == 0) load_bounds(row);
+    const int64_t beg = __shfl_sync(gmask, my_b, jj, G), end = __shfl_sync(gmask, my_e, jj, G);
+    const int lc = __shfl_sync(gmask, my_lc, jj, G);
+    if (sp.T > 0 && end - beg > sp.T) continue;  // a long row: its pieces cover it
+    float4 acc[CPL];
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int64_t mid = beg + lc;
+    gather_local<G, CPL, U>(beg, min(end, mid), col, val, H4, ldh4, c0, min(c1, nch), gl, gmask, acc);
+    if constexpr (MODE == kFwdRemote) {
+      if (GNN_REMOTE_SMEM)
+        gather_remote_smem<G, CPL, GNN_REMOTE_SMEM_UR>(max(beg, mid), end, col, val, c0,
+                                                       min(c1, nch), msg, gl, gmask, acc, rec, recb);
+      else
+        gather_remote<G, CPL, UR>(max(beg, mid), end, col, val, c0, min(c1, nch), msg, gl, gmask,
+                                  acc);
+    }
+    if constexpr (MODE == kBwdOwned)
+      add_owned<G, CPL, UR>(row, own_ptr, own_slot, msg, c0, min(c1, nch), gl, gmask, acc);
+    store_row<G, CPL>(row, acc, F, nch, nch_b, c0, c1, gl, M, ldm, Mb, ldmb, relu, hmask, ldhm);
+  }
+}
+
 // 1024 resident threads per SM (64 registers each); the 3-chunk forward with
 // remote rows needs up to 80 and keeps 768.
 template <int G, int CPL, int MODE, int U, int UR>
@@ -521,6 +579,18 @@ __global__ void __launch_bounds__(rows_block<MODE>(), ((MODE == 1 && CPL == 3) ?
 #pragma unroll
   for (int i = 0; i < CPL; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 
+  __shared__ uint4 srec[(MODE == kFwdRemote && GNN_REMOTE_SMEM) ? rows_block<MODE>() : 1];
+  __shared__ int sbits[(MODE == kFwdRemote && GNN_REMOTE_SMEM) ? rows_block<MODE>() : 1];
+  uint4* rec = srec + ((MODE == kFwdRemote && GNN_REMOTE_SMEM) ? (threadIdx.x & ~31) : 0);
+  int* recb = sbits + ((MODE == kFwdRemote && GNN_REMOTE_SMEM) ? (threadIdx.x & ~31) : 0);
+  if constexpr (MODE != kPlain && GNN_ROWS_MULTI > 1) {
+    if (sl.ns == 1 && unit >= sp.n_pieces) {
+      rows_group<G, CPL, MODE, U, UR, GNN_ROWS_MULTI>(
+          unit - sp.n_pieces, n, rowptr, col, val, local_cnt, H4, ldh4, F, nch, msg, own_ptr,
+          own_slot, sp, c0, c1, M, ldm, Mb, ldmb, nch_b, relu, hmask, ldhm, gl, gmask, rec, recb);
+      return;
+    }
+  }
   const bool piece = unit < sp.n_pieces;
   int64_t row, beg, end;
   if (piece) {  // a piece of a long row -> partial row `unit`
@@ -540,12 +610,8 @@ __global__ void __launch_bounds__(rows_block<MODE>(), ((MODE == 1 && CPL == 3) ?
   gather_local<G, CPL, U>(beg, min(end, mid), col, val, H4, ldh4, c0, min(c1, nch), gl, gmask, acc);
   if constexpr (MODE == kFwdRemote) {
     if (GNN_REMOTE_SMEM) {
-      __shared__ uint4 srec[rows_block<MODE>()];
-      __shared__ int sbits[rows_block<MODE>()];
       gather_remote_smem<G, CPL, GNN_REMOTE_SMEM_UR>(max(beg, mid), end, col, val, c0,
-                                                     min(c1, nch), msg, gl, gmask, acc,
-                                                     srec + (threadIdx.x & ~31),
-                                                     sbits + (threadIdx.x & ~31));
+                                                     min(c1, nch), msg, gl, gmask, acc, rec, recb);
     } else if (GNN_REMOTE_SPLIT)
       gather_remote_split<G, CPL, GNN_REMOTE_SPLIT_UR>(max(beg, mid), end, col, val, c0,
                                                         min(c1, nch), msg, gl, gmask, acc);
@@ -649,14 +715,22 @@ __device__ __forceinline__ void halo_group_slots(
   const uint32_t gmask = group_mask(G, lane);
   const int nch = (F + 3) >> 2;
   const int64_t count = s_hi - s_lo;
+  // HK consecutive slots of the visiting order: their first entries are
+  // neighbouring gradient rows, which the group then re-reads from cache
   const int64_t i0 = ((block * blockDim.x + threadIdx.x) / G) * HK;
   if (i0 >= count) return;  // uniform across the group
+  // the slots' ids and bounds, G slots at a time (lane k holds slot k of the chunk)
   long long my_s = 0, my_b = 0, my_e = 0;
-  if (gl < HK && i0 + gl < count) {
-    my_s = order ? (long long)__ldg(order + i0 + gl) : (long long)(s_lo + i0 + gl);
-    my_b = __ldg(srp + my_s);
-    my_e = __ldg(srp + my_s + 1);
-  }
+  auto load_bounds = [&](int64_t j0) {
+    my_s = my_b = my_e = 0;
+    const int64_t i = i0 + j0 + gl;
+    if (i < count && j0 + gl < HK) {
+      my_s = order ? (long long)__ldg(order + i) : (long long)(s_lo + i);
+      my_b = __ldg(srp + my_s);
+      my_e = __ldg(srp + my_s + 1);
+    }
+  };
+  load_bounds(0);
   // the first entry batch of the group's first slot
   int v_next = 0;
   float w_next = 0.f;
@@ -670,8 +744,9 @@ __device__ __forceinline__ void halo_group_slots(
 #pragma unroll 1
   for (int j = 0; j < HK; ++j) {
     if (i0 + j >= count) break;  // uniform
-    const int64_t s = __shfl_sync(gmask, my_s, j, G);
-    const int64_t beg = __shfl_sync(gmask, my_b, j, G), end = __shfl_sync(gmask, my_e, j, G);
+    const int jj = j % G;  // the slot's lane in the current chunk
+    const int64_t s = __shfl_sync(gmask, my_s, jj, G);
+    const int64_t beg = __shfl_sync(gmask, my_b, jj, G), end = __shfl_sync(gmask, my_e, jj, G);
     const bool skip = long_len > 0 && end - beg > long_len;  // summed by a long-slot block
     float4 acc[CPL];
 #pragma unroll
@@ -720,7 +795,9 @@ __device__ __forceinline__ void halo_group_slots(
     v_next = 0;
     w_next = 0.f;
     if (j + 1 < HK && i0 + j + 1 < count) {
-      const int64_t nb = __shfl_sync(gmask, my_b, j + 1, G), ne = __shfl_sync(gmask, my_e, j + 1, G);
+      if (jj + 1 == G) load_bounds(j + 1);  // the next chunk of G slots
+      const int jn = (j + 1) % G;
+      const int64_t nb = __shfl_sync(gmask, my_b, jn, G), ne = __shfl_sync(gmask, my_e, jn, G);
       if (nb + gl < ne) {
         v_next = __ldg(scol + nb + gl);
         w_next = __ldg(sval + nb + gl);
@@ -739,10 +816,19 @@ __device__ __forceinline__ void halo_group_slots(
 }
 
 #ifndef GNN_HALO_MULTI
-#define GNN_HALO_MULTI 1
+#define GNN_HALO_MULTI 64
 #endif
+// Slots per group, measured at F = 256 (two chunks per lane): 64 on the
+// R-MAT graph's 37.9M slots (67.4 -> 46.7 ms), 16 on the DC-SBM-shaped
+// graphs' 0.8M-3.4M slots (Yelp-shaped 0.71 -> 0.69 ms, products-shaped
+// 3.14 -> 2.58 ms; 64 there is slower than one).  The other row layouts
+// measured slower with more than one slot per group and keep one.
+constexpr int halo_slots_per_group(int G, int CPL, bool many_slots) {
+  return (G == 32 && CPL == 2) ? (many_slots ? GNN_HALO_MULTI : 16) : 1;
+}
+constexpr int64_t kManySlots = int64_t(1) << 24;
 
-template <int G, int CPL, int U, int HK = GNN_HALO_MULTI>
+template <int G, int CPL, int U, int HK>
 __global__ void __launch_bounds__(256, (G == 32 && CPL <= 3) ? 4 : 1) halo_quant_pack_kernel(
     int64_t S, const int64_t* __restrict__ srp, const int32_t* __restrict__ scol,
     const float* __restrict__ sval, const float* __restrict__ Gm, int64_t ldg, int F,
@@ -899,7 +985,10 @@ static gnn_status dispatch_rows(const gnn_csr& csr, const int32_t* colv, const f
   constexpr int block = rows_block<MODE>();
 #define GNN_ROWS(G_, CPL_, U_, UR_)                                                            \
   do {                                                                                         \
-    const int64_t groups = ((int64_t)csr.n + sp.n_pieces) * sl.ns;                             \
+    const int64_t row_units = (MODE != kPlain && sl.ns == 1)                                   \
+                                  ? ((int64_t)csr.n + GNN_ROWS_MULTI - 1) / GNN_ROWS_MULTI     \
+                                  : (int64_t)csr.n;                                            \
+    const int64_t groups = (row_units + sp.n_pieces) * sl.ns;                                  \
     const int64_t grid = (groups * G_ + block - 1) / block;                                    \
     spmm_rows_kernel<G_, CPL_, MODE, U_, UR_><<<(unsigned)grid, block, 0, st>>>(               \
         csr.n, csr.rowptr, colv, valv, local_cnt, H, ldh, F, msg, own_ptr, own_slot, sp, sl,   \
@@ -1035,12 +1124,19 @@ gnn_status launch_halo_quant_pack_ex(const gnn_boundary& b, const float* Gm, int
   const size_t smem = use_long ? (size_t)E * nch * sizeof(float4) : 0;
   const size_t smem_q = (size_t)nch * sizeof(float4);
   const size_t dyn = smem > smem_q ? smem : (use_long ? smem_q : 0);
-#define GNN_HALO(G_, CPL_, U_)                                                                   \
+#define GNN_HALO_K(G_, CPL_, U_, HK_)                                                            \
   do {                                                                                           \
-    const int64_t grid = n_long + (((count + GNN_HALO_MULTI - 1) / GNN_HALO_MULTI) * G_ + block - 1) / block; \
-    halo_quant_pack_kernel<G_, CPL_, U_><<<(unsigned)grid, block, dyn, st>>>(                    \
+    const int64_t grid = n_long + (((count + (HK_) - 1) / (HK_)) * G_ + block - 1) / block;      \
+    halo_quant_pack_kernel<G_, CPL_, U_, HK_><<<(unsigned)grid, block, dyn, st>>>(               \
         S, b.slot_rowptr, b.slot_col, sval, Gm, ldg, F, b.slot_bits, b.slot_off, seed,           \
         packed_ws, meta_ws, n_long, b.long_slots, long_len, E, score_r, a_r, order, s_lo, s_hi); \
+  } while (0)
+#define GNN_HALO(G_, CPL_, U_)                                                                   \
+  do {                                                                                           \
+    if (count >= kManySlots)                                                                     \
+      GNN_HALO_K(G_, CPL_, U_, halo_slots_per_group(G_, CPL_, true));                            \
+    else                                                                                         \
+      GNN_HALO_K(G_, CPL_, U_, halo_slots_per_group(G_, CPL_, false));                           \
   } while (0)
   if (slots <= 32) GNN_HALO(8, 4, 2);
   else {
