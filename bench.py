@@ -102,19 +102,25 @@ def gemm_bytes(n, F_in, F_out):
 
 
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.md")
-TRAFFIC_SOURCES = ("spmm.cu", "quant.cu", "device.cuh")
+# the sources each kernel kind is built from
+TRAFFIC_SOURCES = {"quant": ("quant.cu", "device.cuh"), "spmm_fwd": ("spmm.cu", "device.cuh"),
+                   "halo": ("spmm.cu", "device.cuh"), "spmm_bwd": ("spmm.cu", "device.cuh")}
 
 
-def traffic_source_hash():
-    """Hash of the aggregation and quantiser kernel sources: committed DRAM
-    counters count only while the kernels they were taken on are unchanged."""
+def traffic_source_hash(kind, read=None):
+    """Hash of the sources a kernel kind is built from: committed DRAM
+    counters count only while the kernels they were taken on are unchanged.
+    ``read(name) -> bytes`` reads a source (default: today's files)."""
     import hashlib
 
     csrc = os.path.join(ROOT, "sparse_aggregation_message_gb300", "csrc")
+    if read is None:
+        def read(f):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                return fh.read()
     h = hashlib.sha256()
-    for f in TRAFFIC_SOURCES:
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(fh.read())
+    for f in TRAFFIC_SOURCES[kind]:
+        h.update(read(f))
     return h.hexdigest()[:16]
 
 
@@ -127,13 +133,14 @@ def committed_traffic(workload, base_bits=None, path=TRAFFIC_FILE):
 
     if not os.path.exists(path):
         return {}
-    want_h = traffic_source_hash()
     out = {}
     with open(path) as f:
         for ln in f:
             m = re.match(r"^traffic workload=(\S+) base=(\d+) kind=(\S+) bytes_per_launch=(\d+) "
                          r"source=([0-9a-f]+)\s*$", ln.strip())
-            if not m or m.group(1) != workload or m.group(5) != want_h:
+            if not m or m.group(1) != workload or m.group(3) not in TRAFFIC_SOURCES:
+                continue
+            if m.group(5) != traffic_source_hash(m.group(3)):
                 continue
             if base_bits is not None and int(m.group(2)) != int(base_bits):
                 continue
