@@ -828,6 +828,216 @@ constexpr int halo_slots_per_group(int G, int CPL, bool many_slots) {
 }
 constexpr int64_t kManySlots = int64_t(1) << 24;
 
+// One long slot summed by a whole block: the block's threads load E entry
+// rows at a time into shared memory (all loads in flight together), then
+// thread t adds chunk t of those rows in entry order; warp 0 quantises.
+template <int CPLQ>
+__device__ __forceinline__ void halo_long_block(
+    int blk, const int64_t* __restrict__ srp, const int32_t* __restrict__ scol,
+    const float* __restrict__ sval, const float4* __restrict__ G4, int64_t ldg4, int F,
+    const uint8_t* __restrict__ slot_bits, const int64_t* __restrict__ slot_off, uint32_t seed,
+    uint8_t* __restrict__ packed, float2* __restrict__ meta, const int32_t* __restrict__ long_slots,
+    int E, const float* __restrict__ score_r, const float* __restrict__ a_r, int64_t s_lo,
+    int64_t s_hi, float4* tile) {
+  __shared__ int sv[32];
+  __shared__ float sw[32];
+  const int lane = threadIdx.x & 31;
+  const int nch = (F + 3) >> 2;
+  const int64_t s = __ldg(long_slots + blk);
+  if (s < s_lo || s >= s_hi) return;  // outside the requested slot range (block-uniform)
+  const int64_t beg = __ldg(srp + s), end = __ldg(srp + s + 1);
+  const int t = threadIdx.x;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int64_t base = beg; base < end; base += E) {
+    const int cnt = (int)min((int64_t)E, end - base);
+    if (t < cnt) {
+      sv[t] = __ldg(scol + base + t);
+      sw[t] = __ldg(sval + base + t);
+    }
+    __syncthreads();
+    for (int idx = t; idx < cnt * nch; idx += blockDim.x) {
+      const int e = idx / nch, c = idx - e * nch;
+      tile[idx] = __ldg(G4 + (int64_t)sv[e] * ldg4 + c);
+    }
+    __syncthreads();
+    if (t < nch) {
+      for (int e = 0; e < cnt; ++e) mul_add4(acc, sw[e], tile[e * nch + t]);
+    }
+    __syncthreads();
+  }
+  if (t < nch) {
+    if (score_r) add_score_term(acc, __ldg(score_r + s), a_r, t, F);
+    tile[t] = acc;
+  }
+  __syncthreads();
+  if (t < 32) {
+    float4 v[CPLQ];
+#pragma unroll
+    for (int i = 0; i < CPLQ; ++i) {
+      const int c = lane + 32 * i;
+      v[i] = c < nch ? tile[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    quantize_pack_row<32, CPLQ>(v, F, __ldg(slot_bits + s), row_key(seed, (uint32_t)s),
+                                packed + __ldg(slot_off + s), meta + s, lane, 0xffffffffu);
+  }
+}
+
+// Ordinary slots through a per-warp ring of R + 1 gradient rows in shared
+// memory.  A warp takes HK (<= 32) consecutive slots of the visiting order
+// and walks their entries as one stream: entry k + R is requested (each lane
+// copies its own chunks with 16-byte asynchronous copies) as entry k is
+// added, so R rows stay in flight at every step -- also while a finished
+// slot is quantised -- and no register holds a row in flight.  Each lane
+// reads back only the chunks it copied, so no barrier is needed; the row a
+// copy overwrites was added one step earlier.  Every slot's sum keeps its
+// fixed order (entries ascending, product and sum each rounded).
+template <int CPL, int R, int HK>
+__device__ __forceinline__ void halo_ring_slots(
+    int64_t block, const int64_t* __restrict__ srp, const int32_t* __restrict__ scol,
+    const float* __restrict__ sval, const float4* __restrict__ G4, int64_t ldg4, int F,
+    const uint8_t* __restrict__ slot_bits, const int64_t* __restrict__ slot_off, uint32_t seed,
+    uint8_t* __restrict__ packed, float2* __restrict__ meta, int long_len,
+    const float* __restrict__ score_r, const float* __restrict__ a_r,
+    const int32_t* __restrict__ order, int64_t s_lo, int64_t s_hi, float4* ring, float* wring) {
+  constexpr uint32_t FULL = 0xffffffffu;
+  const int lane = threadIdx.x & 31;
+  const int nch = (F + 3) >> 2;
+  const int64_t count = s_hi - s_lo;
+  const int64_t i0 = ((block * blockDim.x + threadIdx.x) >> 5) * HK;
+  if (i0 >= count) return;  // uniform across the warp
+  const int nslots = (int)min((int64_t)HK, count - i0);
+  // slot table: lane k holds slot k of the warp's run (long slots: no entries here)
+  long long my_s = 0, my_b = 0, my_e = 0;
+  if (lane < nslots) {
+    my_s = order ? (long long)__ldg(order + i0 + lane) : (long long)(s_lo + i0 + lane);
+    my_b = __ldg(srp + my_s);
+    my_e = __ldg(srp + my_s + 1);
+    if (long_len > 0 && my_e - my_b > long_len) my_e = my_b;
+  }
+  // fetch cursor: slot fk, entry fe of [.., fend); lane l of the batch holds
+  // (col, val) of entry fbase + l
+  int fk = 0;
+  long long fe = __shfl_sync(FULL, my_b, 0), fend = __shfl_sync(FULL, my_e, 0), fbase = 0;
+  int vb = 0;
+  float wb = 0.f;
+  auto load_batch = [&]() {
+    fbase = fe;
+    vb = 0;
+    wb = 0.f;
+    if (fbase + lane < fend) {
+      vb = __ldg(scol + fbase + lane);
+      wb = __ldg(sval + fbase + lane);
+    }
+  };
+  auto next_fetch_slot = [&]() {
+    while (fe == fend && fk < nslots) {
+      ++fk;
+      if (fk < nslots) {
+        fe = __shfl_sync(FULL, my_b, fk);
+        fend = __shfl_sync(FULL, my_e, fk);
+      }
+    }
+    if (fk < nslots) load_batch();
+  };
+  next_fetch_slot();
+  int t_fetch = 0, t_cons = 0;
+  auto fetch_one = [&]() {
+    const int r = t_fetch % (R + 1);
+    if (fk < nslots) {
+      const int idx = (int)(fe - fbase);
+      const int v = __shfl_sync(FULL, vb, idx);
+      wring[r * 32 + lane] = __shfl_sync(FULL, wb, idx);
+      const float4* src = G4 + (int64_t)v * ldg4;
+      float4* dst = ring + r * (32 * CPL);
+#pragma unroll
+      for (int i = 0; i < CPL; ++i) {
+        const int c = lane + 32 * i;
+        if (c < nch) cp_async16(dst + c, src + c);
+      }
+      ++fe;
+      if (fe == fend) next_fetch_slot();
+      else if (fe - fbase == 32) load_batch();  // slots longer than 32 entries: the next 32
+    }
+    cp_async_commit();
+    ++t_fetch;
+  };
+#pragma unroll 1
+  for (int k = 0; k < R; ++k) fetch_one();
+  float4 acc[CPL];
+#pragma unroll
+  for (int i = 0; i < CPL; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  int ck = 0;
+  long long ce = __shfl_sync(FULL, my_b, 0), cend = __shfl_sync(FULL, my_e, 0);
+#pragma unroll 1
+  while (ck < nslots) {
+    if (ce == cend) {  // slot ck complete (or summed by a long-slot block)
+      if (cend > __shfl_sync(FULL, my_b, ck)) {
+        const int64_t s = __shfl_sync(FULL, my_s, ck);
+        if (score_r) {
+          const float rs = __ldg(score_r + s);
+#pragma unroll
+          for (int i = 0; i < CPL; ++i)
+            if (lane + 32 * i < nch) add_score_term(acc[i], rs, a_r, lane + 32 * i, F);
+        }
+        quantize_pack_row<32, CPL>(acc, F, __ldg(slot_bits + s), row_key(seed, (uint32_t)s),
+                                   packed + __ldg(slot_off + s), meta + s, lane, FULL);
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      ++ck;
+      if (ck < nslots) {
+        ce = __shfl_sync(FULL, my_b, ck);
+        cend = __shfl_sync(FULL, my_e, ck);
+      }
+      continue;
+    }
+    cp_async_wait<R - 1>();
+    const int r = t_cons % (R + 1);
+    const float w = wring[r * 32 + lane];
+    const float4* src = ring + r * (32 * CPL);
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+      const int c = lane + 32 * i;
+      if (c < nch) mul_add4(acc[i], w, src[c]);
+    }
+    ++ce;
+    ++t_cons;
+    fetch_one();
+  }
+  cp_async_wait<0>();
+}
+
+// Shared memory of a ring block: per warp (R + 1) rows of 32 * CPL chunks
+// and (R + 1) x 32 weights.
+constexpr size_t halo_ring_warp_bytes(int CPL, int R) {
+  return (size_t)(R + 1) * 32 * CPL * 16 + (size_t)(R + 1) * 32 * 4;
+}
+
+template <int CPL, int R, int HK>
+__global__ void __launch_bounds__(256) halo_ring_kernel(
+    int64_t S, const int64_t* __restrict__ srp, const int32_t* __restrict__ scol,
+    const float* __restrict__ sval, const float* __restrict__ Gm, int64_t ldg, int F,
+    const uint8_t* __restrict__ slot_bits, const int64_t* __restrict__ slot_off, uint32_t seed,
+    uint8_t* __restrict__ packed, float2* __restrict__ meta, int n_long,
+    const int32_t* __restrict__ long_slots, int long_len, int E, const float* __restrict__ score_r,
+    const float* __restrict__ a_r, const int32_t* __restrict__ order, int64_t s_lo, int64_t s_hi) {
+  extern __shared__ float4 tile[];
+  const float4* G4 = reinterpret_cast<const float4*>(Gm);
+  const int64_t ldg4 = ldg >> 2;
+  if ((int)blockIdx.x < n_long) {
+    halo_long_block<CPL>(blockIdx.x, srp, scol, sval, G4, ldg4, F, slot_bits, slot_off, seed,
+                         packed, meta, long_slots, E, score_r, a_r, s_lo, s_hi, tile);
+    return;
+  }
+  const int warp = threadIdx.x >> 5;
+  char* base = reinterpret_cast<char*>(tile) + (size_t)warp * halo_ring_warp_bytes(CPL, R);
+  float4* ring = reinterpret_cast<float4*>(base);
+  float* wring = reinterpret_cast<float*>(base + (size_t)(R + 1) * 32 * CPL * 16);
+  halo_ring_slots<CPL, R, HK>(blockIdx.x - n_long, srp, scol, sval, G4, ldg4, F, slot_bits,
+                              slot_off, seed, packed, meta, long_len, score_r, a_r, order, s_lo,
+                              s_hi, ring, wring);
+}
+
 template <int G, int CPL, int U, int HK>
 __global__ void __launch_bounds__(256, (G == 32 && CPL <= 3) ? 4 : 1) halo_quant_pack_kernel(
     int64_t S, const int64_t* __restrict__ srp, const int32_t* __restrict__ scol,
@@ -844,45 +1054,8 @@ __global__ void __launch_bounds__(256, (G == 32 && CPL <= 3) ? 4 : 1) halo_quant
   const int64_t ldg4 = ldg >> 2;
 
   if ((int)blockIdx.x < n_long) {
-    __shared__ int sv[32];
-    __shared__ float sw[32];
-    const int64_t s = __ldg(long_slots + blockIdx.x);
-    if (s < s_lo || s >= s_hi) return;  // outside the requested slot range (block-uniform)
-    const int64_t beg = __ldg(srp + s), end = __ldg(srp + s + 1);
-    const int t = threadIdx.x;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int64_t base = beg; base < end; base += E) {
-      const int cnt = (int)min((int64_t)E, end - base);
-      if (t < cnt) {
-        sv[t] = __ldg(scol + base + t);
-        sw[t] = __ldg(sval + base + t);
-      }
-      __syncthreads();
-      for (int idx = t; idx < cnt * nch; idx += blockDim.x) {
-        const int e = idx / nch, c = idx - e * nch;
-        tile[idx] = __ldg(G4 + (int64_t)sv[e] * ldg4 + c);
-      }
-      __syncthreads();
-      if (t < nch) {
-        for (int e = 0; e < cnt; ++e) mul_add4(acc, sw[e], tile[e * nch + t]);
-      }
-      __syncthreads();
-    }
-    if (t < nch) {
-      if (score_r) add_score_term(acc, __ldg(score_r + s), a_r, t, F);
-      tile[t] = acc;
-    }
-    __syncthreads();
-    if (t < 32) {
-      float4 v[CPLQ];
-#pragma unroll
-      for (int i = 0; i < CPLQ; ++i) {
-        const int c = lane + 32 * i;
-        v[i] = c < nch ? tile[c] : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-      quantize_pack_row<32, CPLQ>(v, F, __ldg(slot_bits + s), row_key(seed, (uint32_t)s),
-                                  packed + __ldg(slot_off + s), meta + s, lane, 0xffffffffu);
-    }
+    halo_long_block<CPLQ>(blockIdx.x, srp, scol, sval, G4, ldg4, F, slot_bits, slot_off, seed,
+                          packed, meta, long_slots, E, score_r, a_r, s_lo, s_hi, tile);
     return;
   }
 
@@ -1101,6 +1274,60 @@ gnn_status launch_halo_quant_pack(const gnn_boundary& b, const float* Gm, int64_
                                    nullptr, st);
 }
 
+// Backward messages of 32-lane row layouts through the ring kernel
+// (GNN_HALO_RING 1) or through register gathers (0).
+#ifndef GNN_HALO_RING
+#define GNN_HALO_RING 1
+#endif
+#ifndef GNN_RING_R
+#define GNN_RING_R 3
+#endif
+// Rows in flight per warp of the ring kernel, by chunks per lane (shared
+// memory per warp: (R + 1) rows of 512 * CPL bytes).  Measured on the R-MAT
+// graph at F = 256 (37.9M slots, 256-thread blocks, 64 registers): R = 2, 3,
+// 4, 5, 7 took 48.5, 45.9, 49.0, 46.4, 55.7 ms against 50.8 ms for the
+// register kernel; deeper rings cost resident warps (shared memory) faster
+// than they add rows in flight.
+constexpr int halo_ring_depth(int CPL) { return CPL <= 2 ? GNN_RING_R : (CPL <= 4 ? 3 : 2); }
+constexpr int kRingSlotsPerWarp = 32;
+// Where the ring pays (measured): wide rows (F = 602, 5 chunks per lane:
+// 7.9 against 11.5 ms on the Reddit-shaped graph) and the 16.8M-slot R-MAT
+// graph at F = 256 (46.2 against 52.8 ms).  On the Yelp-shaped graph's 0.8M
+// slots at F = 300 the register kernel is faster (0.85 against 1.00 ms).
+static bool halo_use_ring(int G, int CPL, int64_t count) {
+  return GNN_HALO_RING && G == 32 && CPL <= 8 && (CPL >= 4 || count >= (int64_t(1) << 24));
+}
+
+template <int CPL>
+static gnn_status launch_halo_ring(const gnn_boundary& b, const float* Gm, int64_t ldg, int F,
+                                   uint32_t seed, uint8_t* packed_ws, float2* meta_ws,
+                                   const float* sval, const float* score_r, const float* a_r,
+                                   cudaStream_t st, int64_t s_lo, int64_t s_hi,
+                                   const int32_t* order, int n_long, int long_len, int E,
+                                   size_t long_smem) {
+  constexpr int R = halo_ring_depth(CPL);
+  constexpr int block = 256;
+  const size_t ring = (size_t)(block / 32) * halo_ring_warp_bytes(CPL, R);
+  const size_t dyn = ring > long_smem ? ring : long_smem;
+  static bool attr_set[8] = {};  // per device
+  int dev = 0;
+  GNN_CUDA(cudaGetDevice(&dev));
+  if (dev >= 8 || !attr_set[dev]) {
+    // long-slot blocks stage at most 48 KB; the ring needs `ring` bytes
+    const int need = (int)(ring > 49152 ? ring : 49152);
+    GNN_CUDA(cudaFuncSetAttribute(halo_ring_kernel<CPL, R, kRingSlotsPerWarp>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, need));
+    if (dev < 8) attr_set[dev] = true;
+  }
+  const int64_t count = s_hi - s_lo;
+  const int64_t warps = (count + kRingSlotsPerWarp - 1) / kRingSlotsPerWarp;
+  const int64_t grid = n_long + (warps + block / 32 - 1) / (block / 32);
+  halo_ring_kernel<CPL, R, kRingSlotsPerWarp><<<(unsigned)grid, block, dyn, st>>>(
+      b.n_slots, b.slot_rowptr, b.slot_col, sval, Gm, ldg, F, b.slot_bits, b.slot_off, seed,
+      packed_ws, meta_ws, n_long, b.long_slots, long_len, E, score_r, a_r, order, s_lo, s_hi);
+  return GNN_OK;  // the caller checks and counts the launch
+}
+
 gnn_status launch_halo_quant_pack_ex(const gnn_boundary& b, const float* Gm, int64_t ldg, int F,
                                      uint32_t seed, uint8_t* packed_ws, float2* meta_ws,
                                      const float* sval, const float* score_r, const float* a_r,
@@ -1133,7 +1360,12 @@ gnn_status launch_halo_quant_pack_ex(const gnn_boundary& b, const float* Gm, int
   } while (0)
 #define GNN_HALO(G_, CPL_, U_)                                                                   \
   do {                                                                                           \
-    if (count >= kManySlots)                                                                     \
+    if (halo_use_ring(G_, CPL_, count)) {                                                        \
+      gnn_status rs = launch_halo_ring<CPL_>(b, Gm, ldg, F, seed, packed_ws, meta_ws, sval,       \
+                                             score_r, a_r, st, s_lo, s_hi, order, n_long,         \
+                                             long_len, E, smem);                                  \
+      if (rs != GNN_OK) return rs;                                                               \
+    } else if (count >= kManySlots)                                                              \
       GNN_HALO_K(G_, CPL_, U_, halo_slots_per_group(G_, CPL_, true));                            \
     else                                                                                         \
       GNN_HALO_K(G_, CPL_, U_, halo_slots_per_group(G_, CPL_, false));                           \
