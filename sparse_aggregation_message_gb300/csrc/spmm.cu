@@ -1294,8 +1294,11 @@ constexpr int kRingSlotsPerWarp = 32;
 // 7.9 against 11.5 ms on the Reddit-shaped graph) and the 16.8M-slot R-MAT
 // graph at F = 256 (46.2 against 52.8 ms).  On the Yelp-shaped graph's 0.8M
 // slots at F = 300 the register kernel is faster (0.85 against 1.00 ms).
+#ifndef GNN_RING_MIN_SLOTS
+#define GNN_RING_MIN_SLOTS (int64_t(1) << 24)
+#endif
 static bool halo_use_ring(int G, int CPL, int64_t count) {
-  return GNN_HALO_RING && G == 32 && CPL <= 8 && (CPL >= 4 || count >= (int64_t(1) << 24));
+  return GNN_HALO_RING && G == 32 && CPL <= 8 && (CPL >= 4 || count >= GNN_RING_MIN_SLOTS);
 }
 
 template <int CPL>
