@@ -165,13 +165,26 @@ def load(build_if_missing: bool = True):
         _build.build()
     if not os.path.exists(_build.LIB):
         raise RuntimeError(f"libgnnagg.so not found at {_build.LIB}; run build() first")
-    lib = ctypes.CDLL(_build.LIB)
+    _LIB = open_lib(_build.LIB)
+    return _LIB
+
+
+def open_lib(path: str):
+    """A library handle for `path` with the C prototypes attached."""
+    lib = ctypes.CDLL(path)
     for name, (res, args) in PROTOTYPES.items():
         fn = getattr(lib, name)
         fn.restype = res
         fn.argtypes = args
-    _LIB = lib
     return lib
+
+
+def use_lib(lib):
+    """Route every binding call through `lib` (a handle from open_lib);
+    returns the handle used before.  For tests of build variants."""
+    global _LIB
+    old, _LIB = _LIB, lib
+    return old
 
 
 class GnnError(RuntimeError):
