@@ -386,7 +386,7 @@ def run_gpu(args, rank, world, local_rank):
                 continue
             if timed:
                 rec(("quant", l, 0))
-            G.gnn_quant_pack(Hs[l], F, bnd.slot_node, S, bnd.slot_bits, so, 2 * l, packed, meta)
+            G.gnn_quant_pack_owned(bnd, Hs[l], F, 2 * l, packed, meta, slot_off=so)
             if timed:
                 rec(("quant", l, 1))
             if bl is not None:
@@ -877,7 +877,7 @@ def main():
 
     spmm_ms = per["spmm_fwd"] + per["halo"] + per["spmm_bwd"]
     gemm_ms = per["gemm_fwd"] + per["mask_dM_dW"]
-    names = {"quant": "quant_pack_kernel (gnn_quant_pack: forward messages)",
+    names = {"quant": "quant_pack_owned_kernel / quant_pack_kernel (gnn_quant_pack_owned: forward messages)",
              "spmm_fwd": "spmm_rows_kernel (gnn_spmm_fwd: aggregation with in-gather dequantisation)",
              "halo": "halo_quant_pack_kernel (gnn_halo_quant_pack: backward halo partials, "
                      "quantised and packed)",

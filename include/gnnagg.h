@@ -251,6 +251,19 @@ gnn_status gnn_quant_pack(const float* X, int64_t ldx, int32_t F,
                           uint32_t seed, uint8_t* packed, float* meta,
                           gnn_stream_t stream);
 
+/* The forward messages of every slot of `bnd` -- the bytes
+ * gnn_quant_pack(X, ldx, F, bnd->slot_node, bnd->n_slots, bnd->slot_bits,
+ * bnd->slot_off, seed, packed, meta) writes -- formed node by node along the
+ * owner lists (own_slot): a node sent to k partitions is read, and its min,
+ * max, scale and quotients (x - mn) / scale formed, once for its k slots;
+ * each slot then draws its codes with its own row key.  SYLVIE guide section
+ * 6 (the quantiser) and section 3 (one boundary node, several receiving
+ * partitions).  Needs own_slot, slot_node, slot_bits, slot_off; checks as
+ * gnn_quant_pack. */
+gnn_status gnn_quant_pack_owned(const gnn_boundary* bnd, const float* X, int64_t ldx,
+                                int32_t F, uint32_t seed, uint8_t* packed, float* meta,
+                                gnn_stream_t stream);
+
 /* The division (x - min) / scale exactly as the quantiser performs it:
  * q[i] = a[i] / b[i] rounded to nearest fp32, for verification against
  * IEEE division.  For 2^-76 <= b <= 2^100 the library forms it from the

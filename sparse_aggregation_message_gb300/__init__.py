@@ -19,7 +19,7 @@ LdrState = GnnLdrState
 __all__ = [
     "Csr", "Boundary", "BitRule", "GnnError", "load", "build",
     "gnn_csr_build", "gnn_csr_split", "gnn_spmm_workspace", "spmm_ws", "gnn_spmm_fwd_noalloc", "gnn_boundary_index", "gnn_boundary_long_slots", "gnn_boundary_set_bits", "gnn_slot_offsets",
-    "gnn_quant_pack", "gnn_dequant_unpack", "gnn_spmm_fwd", "gnn_spmm_bwd", "gnn_sync_check", "gnn_kernel_launches",
+    "gnn_quant_pack", "gnn_quant_pack_owned", "gnn_dequant_unpack", "gnn_spmm_fwd", "gnn_spmm_bwd", "gnn_sync_check", "gnn_kernel_launches",
     "rowbytes", "ld_for", "ldb_for", "gnn_dense_workspace", "gnn_dense_fwd", "gnn_dense_bwd",
     "gnn_layer_workspace", "gnn_layer_fwd", "gnn_layer_bwd",
     "gnn_halo_quant_pack", "gnn_spmm_bwd_local", "gnn_quant_pack_slots", "gnn_halo_quant_pack_slots", "gnn_layer_fwd_async", "gnn_layer_bwd_async",
@@ -306,6 +306,16 @@ def gnn_quant_pack(X, F: int, row_idx, n_rows: int, row_bits, row_off, seed: int
                    stream=None) -> None:
     call("gnn_quant_pack", _ptr(X), X.stride(0), F, _ptr(row_idx), n_rows, _ptr(row_bits),
          _ptr(row_off), seed & 0xFFFFFFFF, _ptr(packed), _ptr(meta), _stream(stream))
+
+
+def gnn_quant_pack_owned(bnd: Boundary, X, F: int, seed: int, packed, meta, slot_off=None,
+                         stream=None) -> None:
+    """Every slot's forward message (the bytes gnn_quant_pack writes for the
+    slot rows), formed node by node: each boundary node's row is prepared once
+    for all the partitions it is sent to."""
+    cb = bnd.c(slot_off, F if slot_off is not None else None)
+    call("gnn_quant_pack_owned", ctypes.byref(cb), _ptr(X), X.stride(0), F, seed & 0xFFFFFFFF,
+         _ptr(packed), _ptr(meta), _stream(stream))
 
 
 def gnn_quant_divide(a, b, q, stream=None) -> None:

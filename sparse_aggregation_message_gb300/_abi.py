@@ -80,6 +80,7 @@ PROTOTYPES = {
     "gnn_slot_offsets_workspace": (ctypes.c_int, [c_i64, P_size]),
     "gnn_slot_offsets": (ctypes.c_int, [c_vp, c_i64, c_i32, c_vp, c_vp, c_size, c_vp]),
     "gnn_quant_pack": (ctypes.c_int, [c_vp, c_i64, c_i32, c_vp, c_i64, c_vp, c_vp, c_u32, c_vp, c_vp, c_vp]),
+    "gnn_quant_pack_owned": (ctypes.c_int, [P_bnd, c_vp, c_i64, c_i32, c_u32, c_vp, c_vp, c_vp]),
     "gnn_dequant_unpack": (ctypes.c_int, [c_vp, c_vp, c_vp, c_vp, c_i64, c_i32, c_vp, c_i64, c_vp]),
     "gnn_spmm_workspace": (ctypes.c_int, [P_csr, c_i32, P_size]),
     "gnn_spmm_fwd": (ctypes.c_int, [P_csr, P_bnd, c_vp, c_i64, c_i32, c_vp, c_vp, c_vp, c_i64, c_vp, c_i64,

@@ -138,6 +138,147 @@ __device__ __forceinline__ uint32_t fmix32_tail(uint32_t h) {
 // j = 4c + k (k < 4) is fmix32(key ^ j); j and 4c differ only in their two
 // low bits, so key ^ j = (key ^ 4c) ^ k and (key ^ j) >> 16 = (key ^ 4c) >> 16,
 // and fmix32's first step gives A_c ^ k with A_c formed once per chunk.
+template <int G, int CPL, int B>
+__device__ __forceinline__ void pack_codes_t(const float4 (&t)[CPL], int F, bool flat, uint32_t key,
+                                           uint32_t* __restrict__ words, int gl, uint32_t gmask) {
+  constexpr uint32_t TOP = (1u << B) - 1u;
+  constexpr int PER_WORD = 8 / B;  // chunks per 32-bit word
+  const int nch = (F + 3) >> 2;
+  const int slots = (int)(rowbytes_dev(B, F) * 2u) / B;  // chunk slots of the padded row
+#pragma unroll
+  for (int i = 0; i < CPL; ++i) {
+    const int c = gl + i * G;
+    uint32_t part = 0;
+    if (c < nch && !flat) {
+      // all four codes, then the fields of elements >= F cleared (their
+      // quotients come from in-row values, so no element is special-cased)
+      const uint32_t kc = key ^ (uint32_t)(4 * c);
+      const uint32_t a = kc ^ (kc >> 16);
+      const float2 m01 = make_float2(static_cast<float>(fmix32_tail(a) >> 8),
+                                     static_cast<float>(fmix32_tail(a ^ 1u) >> 8));
+      const float2 m23 = make_float2(static_cast<float>(fmix32_tail(a ^ 2u) >> 8),
+                                     static_cast<float>(fmix32_tail(a ^ 3u) >> 8));
+      const float2 e24 = dup2(5.9604644775390625e-08f);
+      const float2 r01 = fma2_rn(m01, e24, make_float2(t[i].x, t[i].y));
+      const float2 r23 = fma2_rn(m23, e24, make_float2(t[i].z, t[i].w));
+      // floor(t + u) >= 0 and below 2^24: round down while converting
+      part = min(__float2uint_rd(r01.x), TOP) | (min(__float2uint_rd(r01.y), TOP) << B) |
+             (min(__float2uint_rd(r23.x), TOP) << (2 * B)) |
+             (min(__float2uint_rd(r23.y), TOP) << (3 * B));
+      const int nv = F - 4 * c;  // elements of chunk c below F, >= 1
+      if (nv < 4) part &= (1u << (B * nv)) - 1u;
+    }
+    if (PER_WORD > 1) {
+      part <<= (c % PER_WORD) * 4 * B;
+#pragma unroll
+      for (int o = 1; o < PER_WORD; o <<= 1) part |= __shfl_xor_sync(gmask, part, o);
+    }
+    if (c < slots && (c % PER_WORD) == 0) words[(c * B) >> 3] = part;
+  }
+}
+
+// The per-row part of the quantiser for the group's row held in v[]
+// (elements >= F ignored) at width b < 32: min and max (a zero stored as +0),
+// scale = (mx - mn) / (2^b - 1) (0 for a constant row: flat), and the
+// quotients t = (x - mn) / scale of every element, correctly rounded.  The
+// codes of any row key follow from t alone (pack_codes_t), so a row sent to
+// several partitions is prepared once.  All lanes of the group must call.
+template <int G, int CPL>
+__device__ __forceinline__ void quant_prepare(const float4 (&v)[CPL], int F, int b, int gl,
+                                              uint32_t gmask, float4 (&t)[CPL], float& mn_out,
+                                              float& scale_out, bool& flat_out) {
+  const int nch = (F + 3) >> 2;
+  // elements >= F of the last chunk take the chunk's first element: min,
+  // max and the codes of the other elements are unchanged by in-row values
+  float4 x[CPL];
+  float mn = __int_as_float(0x7f800000), mx = -__int_as_float(0x7f800000);
+#pragma unroll
+  for (int i = 0; i < CPL; ++i) {
+    const int c = gl + i * G;
+    x[i] = v[i];
+    const int nv = F - 4 * c;
+    if (nv < 4) {
+      if (nv < 2) x[i].y = x[i].x;
+      if (nv < 3) x[i].z = x[i].x;
+      x[i].w = x[i].x;
+    }
+    if (c < nch) {
+      // three-input min / max (sm_100+): two instructions per chunk each
+      // instead of four (the quantiser is bound by this pipe: measured 0.8%)
+      float a, b2;
+      asm("min.f32 %0, %1, %2, %3;" : "=f"(a) : "f"(mn), "f"(x[i].x), "f"(x[i].y));
+      asm("min.f32 %0, %1, %2, %3;" : "=f"(mn) : "f"(a), "f"(x[i].z), "f"(x[i].w));
+      asm("max.f32 %0, %1, %2, %3;" : "=f"(b2) : "f"(mx), "f"(x[i].x), "f"(x[i].y));
+      asm("max.f32 %0, %1, %2, %3;" : "=f"(mx) : "f"(b2), "f"(x[i].z), "f"(x[i].w));
+    }
+  }
+#pragma unroll
+  for (int o = G / 2; o > 0; o >>= 1) {
+    mn = fminf(mn, __shfl_xor_sync(gmask, mn, o));
+    mx = fmaxf(mx, __shfl_xor_sync(gmask, mx, o));
+  }
+  if (__float_as_uint(mn) == 0x80000000u) mn = 0.f;  // a zero min/max is stored as +0
+  if (__float_as_uint(mx) == 0x80000000u) mx = 0.f;
+  const float top = static_cast<float>((1u << b) - 1u);  // exact: 2^b - 1 < 2^24
+  const bool flat = !(mx > mn);
+  const float scale = flat ? 0.f : __fdiv_rn(__fsub_rn(mx, mn), top);
+  const Divisor dv = make_divisor(scale);
+  // x - min (as x + (-min): the same IEEE result), then the division
+  const float2 nmn = dup2(-mn);
+#pragma unroll
+  for (int i = 0; i < CPL; ++i) {
+    const int c = gl + i * G;
+    t[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (c < nch && !flat) {
+      float2 t01, t23;
+      if (dv.fast) {
+        t01 = div2_rn<true>(add2_rn(make_float2(x[i].x, x[i].y), nmn), dv);
+        t23 = div2_rn<true>(add2_rn(make_float2(x[i].z, x[i].w), nmn), dv);
+      } else {
+        t01 = div2_rn<false>(add2_rn(make_float2(x[i].x, x[i].y), nmn), dv);
+        t23 = div2_rn<false>(add2_rn(make_float2(x[i].z, x[i].w), nmn), dv);
+      }
+      t[i] = make_float4(t01.x, t01.y, t23.x, t23.y);
+    }
+  }
+  mn_out = mn;
+  scale_out = scale;
+  flat_out = flat;
+}
+
+// Codes of the prepared row t at width b (< 32) with row key `key`, packed
+// into the 16-byte aligned row at `words`.
+template <int G, int CPL>
+__device__ __forceinline__ void pack_codes_b(const float4 (&t)[CPL], int F, int b, bool flat,
+                                             uint32_t key, uint32_t* __restrict__ words, int gl,
+                                             uint32_t gmask) {
+  switch (b) {
+    case 1: pack_codes_t<G, CPL, 1>(t, F, flat, key, words, gl, gmask); break;
+    case 2: pack_codes_t<G, CPL, 2>(t, F, flat, key, words, gl, gmask); break;
+    case 4: pack_codes_t<G, CPL, 4>(t, F, flat, key, words, gl, gmask); break;
+    default: pack_codes_t<G, CPL, 8>(t, F, flat, key, words, gl, gmask); break;
+  }
+}
+
+// Width 32: the row's fp32 values, elements >= F zeroed.
+template <int G, int CPL>
+__device__ __forceinline__ void store_raw_row(const float4 (&v)[CPL], int F, uint8_t* __restrict__ out,
+                                              int gl) {
+  const int nch = (F + 3) >> 2;
+#pragma unroll
+  for (int i = 0; i < CPL; ++i) {
+    const int c = gl + i * G;
+    if (c < nch) {
+      float4 x = v[i];
+      const int j0 = 4 * c;
+      if (j0 + 1 >= F) x.y = 0.f;
+      if (j0 + 2 >= F) x.z = 0.f;
+      if (j0 + 3 >= F) x.w = 0.f;
+      reinterpret_cast<float4*>(out)[c] = x;
+    }
+  }
+}
+
 template <int G, int CPL, int B, bool FAST>
 __device__ __forceinline__ void pack_codes(const float4 (&v)[CPL], int F, float mn, const Divisor& dv,
                                            bool flat, uint32_t key, uint32_t* __restrict__ words,
@@ -258,6 +399,28 @@ __device__ __forceinline__ void quantize_pack_row(const float4 (&v)[CPL], int F,
       default: pack_codes<G, CPL, 8, false>(x, F, mn, dv, flat, key, words, gl, gmask); break;
     }
   }
+  if (gl == 0) *meta = make_float2(mn, scale);
+}
+
+// quantize_pack_row (above) as quant_prepare then pack_codes_t: the same
+// bytes; the ring kernel of the backward messages measured faster with it
+// (37.8 against 42.1 ms on the R-MAT graph), the per-slot quantiser slower
+// (16.3 against 14.2 ms), so each takes its own.
+template <int G, int CPL>
+__device__ __forceinline__ void quantize_pack_row_split(const float4 (&v)[CPL], int F, int b,
+                                                  uint32_t key, uint8_t* __restrict__ out,
+                                                  float2* __restrict__ meta, int gl,
+                                                  uint32_t gmask) {
+  if (b == 32) {
+    store_raw_row<G, CPL>(v, F, out, gl);
+    if (gl == 0) *meta = make_float2(0.f, 0.f);
+    return;
+  }
+  float4 t[CPL];
+  float mn, scale;
+  bool flat;
+  quant_prepare<G, CPL>(v, F, b, gl, gmask, t, mn, scale, flat);
+  pack_codes_b<G, CPL>(t, F, b, flat, key, reinterpret_cast<uint32_t*>(out), gl, gmask);
   if (gl == 0) *meta = make_float2(mn, scale);
 }
 

@@ -836,8 +836,8 @@ extern "C" gnn_status gnn_gat_layer_fwd(const gnn_csr* csr, const gnn_boundary* 
   gat_node_scores_kernel<<<warps_grid(n), kBlock, 0, st>>>(n, Y, ldy, F_out, a_l, a_r, w.s_l, w.s_r);
   GNN_CHECK_LAUNCH();
   if (slots) {
-    s = launch_quant_pack(Y, ldy, F_out, bnd->slot_node, bnd->n_slots, bnd->slot_bits, bnd->slot_off,
-                          seed, packed, reinterpret_cast<float2*>(meta), st);
+    s = launch_quant_pack_owned(*bnd, Y, ldy, F_out, seed, packed, reinterpret_cast<float2*>(meta),
+                                st);
     if (s != GNN_OK) return s;
     gat_slot_scores_kernel<<<warps_grid(bnd->n_slots), kBlock, 0, st>>>(
         bnd->n_slots, packed, reinterpret_cast<const float2*>(meta), bnd->slot_off, bnd->slot_bits,

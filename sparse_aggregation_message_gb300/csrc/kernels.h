@@ -18,6 +18,10 @@ gnn_status launch_quant_pack_range(const float* X, int64_t ldx, int F, const int
                                    const int64_t* off, uint32_t seed, uint8_t* packed,
                                    float2* meta, cudaStream_t st);
 
+// Every slot's forward message, node by node along the owner lists.
+gnn_status launch_quant_pack_owned(const gnn_boundary& b, const float* X, int64_t ldx, int F,
+                                   uint32_t seed, uint8_t* packed, float2* meta, cudaStream_t st);
+
 gnn_status launch_dequant_unpack(const uint8_t* packed, const float2* meta, const int64_t* off,
                                  const uint8_t* bits, int64_t n_rows, int F, float* out,
                                  int64_t ldo, cudaStream_t st);

@@ -208,8 +208,8 @@ extern "C" gnn_status gnn_layer_fwd(const gnn_csr* csr, const gnn_boundary* bnd,
     GNN_REQUIRE(packed_ws && meta_ws && ((uintptr_t)packed_ws & 15) == 0 && ((uintptr_t)meta_ws & 7) == 0,
                 "gnn_layer_fwd: packed_ws/meta_ws required with a boundary");
     GNN_REQUIRE(ldh >= F_in && ldh % 4 == 0 && ((uintptr_t)H_in & 15) == 0, "gnn_layer_fwd: bad H_in");
-    s = launch_quant_pack(H_in, ldh, F_in, bnd->slot_node, bnd->n_slots, bnd->slot_bits,
-                          bnd->slot_off, seed, packed_ws, reinterpret_cast<float2*>(meta_ws), st);
+    s = launch_quant_pack_owned(*bnd, H_in, ldh, F_in, seed, packed_ws,
+                                reinterpret_cast<float2*>(meta_ws), st);
     if (s != GNN_OK) return s;
   }
   s = gnn_spmm_fwd(csr, bnd, H_in, ldh, F_in, packed_ws, meta_ws, nullptr, 0, Mb, ldmb, w.spmm,
@@ -300,8 +300,8 @@ extern "C" gnn_status gnn_layer_fwd_async(const gnn_csr* csr, const gnn_boundary
   if ((s = fork_to(f, st, ax)) != GNN_OK) return s;
   // from here on `stream` always waits for `aux` before returning, error or not
   if (bnd->n_slots > 0)
-    s = launch_quant_pack(H_in, ldh, F_in, bnd->slot_node, bnd->n_slots, bnd->slot_bits,
-                          bnd->slot_off, seed, packed_next, reinterpret_cast<float2*>(meta_next), ax);
+    s = launch_quant_pack_owned(*bnd, H_in, ldh, F_in, seed, packed_next,
+                                reinterpret_cast<float2*>(meta_next), ax);
   if (s == GNN_OK)
     s = gnn_spmm_fwd(csr, bnd, H_in, ldh, F_in, packed_prev, meta_prev, nullptr, 0, Mb, ldmb,
                      w.spmm, spmm_workspace_bytes(*csr, F_in), stream);
@@ -415,8 +415,8 @@ extern "C" gnn_status gnn_layer_fwd_tf(const gnn_csr* csr, const gnn_boundary* b
                 "gnn_layer_fwd_tf: boundary offsets must be for F_out");
     GNN_REQUIRE(packed_ws && meta_ws && ((uintptr_t)packed_ws & 15) == 0 && ((uintptr_t)meta_ws & 7) == 0,
                 "gnn_layer_fwd_tf: packed_ws/meta_ws required with a boundary");
-    s = launch_quant_pack(Y, ldy, F_out, bnd->slot_node, bnd->n_slots, bnd->slot_bits,
-                          bnd->slot_off, seed, packed_ws, reinterpret_cast<float2*>(meta_ws), st);
+    s = launch_quant_pack_owned(*bnd, Y, ldy, F_out, seed, packed_ws,
+                                reinterpret_cast<float2*>(meta_ws), st);
     if (s != GNN_OK) return s;
   } else if (bnd) {
     GNN_REQUIRE(bnd->F == F_out, "gnn_layer_fwd_tf: boundary offsets must be for F_out");

@@ -828,6 +828,20 @@ constexpr int halo_slots_per_group(int G, int CPL, bool many_slots) {
 }
 constexpr int64_t kManySlots = int64_t(1) << 24;
 
+#ifndef GNN_RING_SPLIT
+#define GNN_RING_SPLIT 1
+#endif
+template <int G, int CPL>
+__device__ __forceinline__ void quantize_pack_row_sel(const float4 (&v)[CPL], int F, int b,
+                                                      uint32_t key, uint8_t* __restrict__ out,
+                                                      float2* __restrict__ meta, int gl,
+                                                      uint32_t gmask) {
+  if (GNN_RING_SPLIT)
+    quantize_pack_row_split<G, CPL>(v, F, b, key, out, meta, gl, gmask);
+  else
+    quantize_pack_row<G, CPL>(v, F, b, key, out, meta, gl, gmask);
+}
+
 // One long slot summed by a whole block: the block's threads load E entry
 // rows at a time into shared memory (all loads in flight together), then
 // thread t adds chunk t of those rows in entry order; warp 0 quantises.
@@ -877,8 +891,8 @@ __device__ __forceinline__ void halo_long_block(
       const int c = lane + 32 * i;
       v[i] = c < nch ? tile[c] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    quantize_pack_row<32, CPLQ>(v, F, __ldg(slot_bits + s), row_key(seed, (uint32_t)s),
-                                packed + __ldg(slot_off + s), meta + s, lane, 0xffffffffu);
+    quantize_pack_row_sel<32, CPLQ>(v, F, __ldg(slot_bits + s), row_key(seed, (uint32_t)s),
+                                    packed + __ldg(slot_off + s), meta + s, lane, 0xffffffffu);
   }
 }
 
@@ -998,7 +1012,7 @@ __device__ __forceinline__ void halo_ring_stream(
         for (int i = 0; i < CPL; ++i)
           if (lane + 32 * i < nch) add_score_term(acc[i], rs, a_r, lane + 32 * i, F);
       }
-      quantize_pack_row<32, CPL>(acc, F, __ldg(slot_bits + s), row_key(seed, (uint32_t)s),
+      quantize_pack_row_sel<32, CPL>(acc, F, __ldg(slot_bits + s), row_key(seed, (uint32_t)s),
                                  packed + __ldg(slot_off + s), meta + s, lane, FULL);
 #pragma unroll
       for (int i = 0; i < CPL; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);

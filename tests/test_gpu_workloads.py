@@ -5,8 +5,9 @@ gated owner-side aggregation).
 
 Per workload, against the oracle:
   * CSR, boundary index, widths and offsets: bit-exact, every array in full;
-  * forward and backward messages: the ENTIRE packed buffer (padding
-    included) and every slot's meta bit-exact, from the oracle's C routines;
+  * forward messages (gnn_quant_pack_owned, as the bench forms them) and
+    backward messages: the ENTIRE packed buffer (padding included) and every
+    slot's meta bit-exact, from the oracle's C routines;
   * forward aggregation, backward aggregation and the gated bf16 backward on
     a seeded sample of 2^16 rows plus every row with more than 1,000 entries,
     within |d| <= 1e-5*sum|terms| + 1e-7 (bf16: plus half a bf16 step);
@@ -154,7 +155,7 @@ def test_workload_parity(name):
             # ---- a3: forward messages, the whole buffer
             packed = t.zeros(max(Q, 16), dtype=t.uint8, device="cuda")
             meta = t.zeros((max(S, 1), 2), device="cuda")
-            G.gnn_quant_pack(Hd, F, bnd.slot_node, S, bnd.slot_bits, off_d, seed_f, packed, meta)
+            G.gnn_quant_pack_owned(bnd, Hd, F, seed_f, packed, meta, slot_off=off_d)
             G.gnn_sync_check()
             fp, fm = C.quant_pack(Hh, F, ob["slot_node"], sb, off, seed_f)
             compare_messages(packed, meta, fp, fm, off, f"{tag} forward messages")
